@@ -1,0 +1,430 @@
+#!/usr/bin/env python3
+"""Benchmark of the lightning-attention hot path on GB300.
+
+One "step" is one call of the prefill entry point over the MiniMax-01-shaped
+layer: 1 sequence x 8192 tokens x 64 heads x d = 128, bf16 inputs, fp32
+accumulation, bf16 output plus the fp32 final state [64, 128, 128].  The
+JSON line's ``value`` is prefill tokens/s with inputs already resident in
+HBM; ``decode`` holds the batched decode step (128 sequences x 64 heads,
+fp32 state, 1000 consecutive steps); ``e2e`` repeats the prefill through the
+same public call with the inputs in pinned host memory and the host<->device
+copies inside the timed region; ``roofline`` relates the prefill kernel's
+time to the HBM roofline (its bound) and ``tensor`` to the bf16 tensor peak;
+``cpu_baseline`` is the fp64 CPU oracle timed on the host cores.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs an independent replica on its own GPU (the
+path has no exchange step); rank 0 prints the line with the max time over
+ranks and the tokens of all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("prefill tokens/s + % bf16 tensor peak; decode tokens/s + % HBM BW (1×GB300)")
+PREFILL_KERNEL_SRC = os.path.join(ROOT, "lightning_attention_attn_gb300", "csrc", "prefill_tc.cu")
+DECODE_KERNEL_SRC = os.path.join(ROOT, "lightning_attention_attn_gb300", "csrc", "decode.cu")
+
+
+# ---------------------------------------------------------------- helpers
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return dict(hbm=float(j["hbm_gbs"]), bf16=float(j["bf16_tflops"]),
+                    bf16_sustained=float(j.get("bf16_tflops_sustained", j["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+def src_hash(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def ncu_traffic(kernel_key, src):
+    """DRAM bytes per launch from the committed ncu summary, only while the
+    kernel source is the one that was profiled."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        j = json.load(f)
+    e = j.get(kernel_key)
+    if not e or e.get("source_sha256_16") != src_hash(src):
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons in the background."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, ws):
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x, ws):
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ------------------------------------------------------- workload figures
+def prefill_alg(T, H, d, B, nseq):
+    """Algorithmic bytes and flops of one prefill launch.
+    bytes: q, k, v read + o written (bf16) = 8 d per token-head, plus the fp32
+    final state H d^2 4 per sequence.  flops: 4 d^2 (Q KV and K^T V) plus
+    2 (B + 1) d (causal half of Q K^T and P V) per token-head."""
+    byts = T * H * 8 * d + nseq * H * d * d * 4
+    flops = T * H * (4 * d * d + 2 * (B + 1) * d)
+    return byts, flops
+
+
+def decode_alg(Bn, H, d):
+    """State read + write (fp32) plus q, k, v read and o written (bf16)."""
+    return Bn * H * (2 * d * d * 4 + 4 * d * 2)
+
+
+# ------------------------------------------------------------- our arm
+def cpu_baseline(inp, min_seconds=10.0):
+    """The fp64 oracle (recurrent form) on the same 8K-token workload, all
+    heads, repeated until at least min_seconds of CPU work."""
+    import oracle
+    threads = oracle.max_threads()
+    T = inp.total_tokens
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        oracle.recurrent(inp.q, inp.k, inp.v, inp.decay, inp.cu_seqlens.cpu())
+        n += 1
+        dt = time.perf_counter() - t0
+        if dt >= min_seconds or n >= 20:
+            break
+    return {"value": n * T / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"full prefill_8k workload (1 x 8192 tokens x 64 heads x d=128, "
+                      f"bf16 inputs upcast to fp64), recurrent form, {n} run(s), {dt:.1f} s"}
+
+
+def run_ours(args, ws, rank, local):
+    import torch
+    import lightning_attention_attn_gb300 as la
+    from lightning_attention_attn_gb300 import build as labuild
+    from lightning_attention_attn_gb300 import workloads as wl
+
+    la.load(labuild.build())
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    pk = peaks()
+
+    cfg = wl.PREFILL_8K
+    T, H, d = cfg["lengths"][0], cfg["num_heads"], cfg["head_dim"]
+    B = 128
+    inp = wl.prefill_inputs(cfg["lengths"], H, d, dtype=torch.bfloat16, seed=0, device=dev)
+    out = torch.empty_like(inp.q)
+    fs = torch.empty((1, H, d, d), dtype=torch.float32, device=dev)
+
+    def step():
+        la.prefill(inp.q, inp.k, inp.v, inp.decay, inp.cu_seqlens, chunk=0, out=out,
+                   final_state=fs, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    la.device_status(stream)
+    torch.cuda.synchronize()
+
+    K = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        # untimed soak right before the timed steps, so the clock samples
+        # (every 50 ms) cover the GPU under this load even when K steps
+        # take only milliseconds
+        t_soak = time.perf_counter()
+        while time.perf_counter() - t_soak < 1.0:
+            for _ in range(50):
+                step()
+            torch.cuda.synchronize()
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for i in range(K):
+            evs[i][0].record(stream)
+            step()
+            evs[i][1].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    barrier(ws)
+    la.device_status(stream)
+    total_ms = t_start.elapsed_time(t_end)
+    launch_ms = [a.elapsed_time(b) for a, b in evs]
+    avg_launch_s = sum(launch_ms) / K / 1e3
+    total_ms = max_over_ranks(total_ms, ws)
+    tokens = sum_over_ranks(float(T * K), ws)
+    value = tokens / (total_ms / 1e3)
+
+    byts, flops = prefill_alg(T, H, d, B, 1)
+    achieved_gbs = byts / avg_launch_s / 1e9
+    traffic = ncu_traffic("prefill_tc_kernel", PREFILL_KERNEL_SRC)
+    roofline = {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": pk["hbm"],
+                "unit": "GB/s", "frac": round(achieved_gbs / pk["hbm"], 4),
+                "traffic": traffic, "peak_source": pk["source"],
+                "kernel": "prefill_tc_kernel", "alg_bytes_per_launch": byts,
+                "launch_ms": round(avg_launch_s * 1e3, 4)}
+    tflops = flops / avg_launch_s / 1e12
+    t_roof = max(byts / (pk["hbm"] * 1e9), flops / (pk["bf16"] * 1e12))
+    tensor = {"alg_flops_per_launch": flops, "achieved_tflops": round(tflops, 2),
+              "peak_tflops": pk["bf16"], "frac_of_bf16_peak": round(tflops / pk["bf16"], 4),
+              "frac_of_roofline": round(t_roof / avg_launch_s, 4)}
+
+    # ---------------- decode: 128 seqs x 64 heads, 1000 consecutive steps
+    dcfg = wl.DECODE_128
+    dsteps = dcfg["steps"]
+    dinp = wl.decode_inputs(dcfg["batch"], dcfg["num_heads"], dcfg["head_dim"], steps=dsteps,
+                            dtype=torch.bfloat16, seed=0, device=dev)
+    dout = torch.empty_like(dinp.q[0])
+
+    def dstep(t):
+        la.decode(dinp.q[t], dinp.k[t], dinp.v[t], dinp.decay, dinp.state, out=dout,
+                  stream=stream)
+
+    for t in range(5):
+        dstep(t)
+    torch.cuda.synchronize()
+    d0 = torch.cuda.Event(enable_timing=True)
+    d1 = torch.cuda.Event(enable_timing=True)
+    d0.record(stream)
+    for t in range(dsteps):
+        dstep(t)
+    d1.record(stream)
+    torch.cuda.synchronize()
+    dms = d0.elapsed_time(d1) / dsteps
+    dbytes = decode_alg(dcfg["batch"], dcfg["num_heads"], dcfg["head_dim"])
+    dgbs = dbytes / (dms / 1e3) / 1e9
+    decode = {"value": round(dcfg["batch"] / (dms / 1e3), 1), "unit": "tokens/s",
+              "ms_per_step": round(dms, 5), "steps": dsteps,
+              "config": {"workload": "decode_128", "batch": dcfg["batch"], "heads": 64,
+                         "head_dim": 128, "state": "fp32 [128,64,128,128]", "io": "bf16"},
+              "roofline": {"bound": "hbm", "achieved": round(dgbs, 1), "peak": pk["hbm"],
+                           "unit": "GB/s", "frac": round(dgbs / pk["hbm"], 4),
+                           "traffic": ncu_traffic("decode_kernel", DECODE_KERNEL_SRC),
+                           "kernel": "decode_kernel", "alg_bytes_per_launch": dbytes}}
+    del dinp
+
+    # ---------------- end to end through the public call, host buffers
+    hq, hk, hv = (t.cpu().pin_memory() for t in (inp.q, inp.k, inp.v))
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    hfs = torch.empty(fs.shape, dtype=fs.dtype).pin_memory()
+
+    def e2e_step():
+        inp.q.copy_(hq, non_blocking=True)
+        inp.k.copy_(hk, non_blocking=True)
+        inp.v.copy_(hv, non_blocking=True)
+        step()
+        hout.copy_(out, non_blocking=True)
+        hfs.copy_(fs, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(ws)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e_ms = max_over_ranks(e0.elapsed_time(e1), ws)
+    h2d = 3 * hq.numel() * hq.element_size()
+    d2h = hout.numel() * hout.element_size() + hfs.numel() * hfs.element_size()
+    e2e = {"value": round(tokens / (e_ms / 1e3), 1), "unit": "tokens/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(total_ms / K, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1); q, k scaled by d^-1/2; lambda_h = exp(-2^(-8(h+1)/64)))",
+        "config": {"workload": "prefill_8k", "batch": 1, "seq_len": T, "heads": H,
+                   "head_dim": d, "chunk": B, "value_slices_per_head": 2,
+                   "inputs_vs_l2": "q, k, v = 384 MiB > 129 MB L2; no flush needed",
+                   "parallelism": f"replicas x{ws}"},
+        "roofline": roofline, "tensor": tensor, "decode": decode, "e2e": e2e,
+        "gpu_launches": K,
+    }
+    clocks = clk.summary()
+    line["clocks"] = clocks
+    line["config"]["clocks_window"] = "1 s untimed soak of the same step + the timed steps"
+    if rank == 0:
+        host = wl.PrefillInputs(inp.q.cpu(), inp.k.cpu(), inp.v.cpu(), inp.decay.cpu(),
+                                inp.cu_seqlens.cpu())
+        line["cpu_baseline"] = cpu_baseline(host)
+    return line
+
+
+# --------------------------------------------------------- reference arm
+def run_reference(args, ws, rank):
+    """The oracle (fp64, CPU, as it stands) on a bounded sample of the same
+    workload: each step is the first 1024 tokens of the 8K layer, all 64
+    heads, recurrent form.  Rank 0 only."""
+    if rank != 0:
+        return None
+    import torch
+    import oracle
+    from lightning_attention_attn_gb300 import workloads as wl
+    S = 1024
+    inp = wl.prefill_inputs([S], 64, 128, dtype=torch.bfloat16, seed=0)
+    threads = oracle.max_threads()
+    for _ in range(args.warmup):
+        oracle.recurrent(inp.q, inp.k, inp.v, inp.decay, inp.cu_seqlens)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.recurrent(inp.q, inp.k, inp.v, inp.decay, inp.cu_seqlens)
+    dt = time.perf_counter() - t0
+    value = S * args.steps / dt
+    sample = (f"first {S} tokens of the prefill_8k workload per step, all 64 heads, "
+              f"fp64 recurrent form, {threads} threads")
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "tokens/s",
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (same recipe as our arm)",
+            "config": {"workload": "prefill_8k", "batch": 1, "seq_len": 8192, "heads": 64,
+                       "head_dim": 128, "parallelism": "cpu oracle, rank 0"},
+            "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        # the CPU oracle runs on rank 0 only; other ranks exit without work
+        ws = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        line = run_reference(args, ws, rank)
+        if rank == 0 and line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    ws, rank, local = dist_setup()
+    line = run_ours(args, ws, rank, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

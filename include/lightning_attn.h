@@ -1,0 +1,154 @@
+/*
+ * lightning_attn.h -- C ABI of the GB300 (sm_103a) lightning-attention library
+ * (liblightning_attn.so).
+ *
+ * The operation (MiniMax-01 technical report, CSDN full translation, §2.2.1
+ * "Lightning Attention", eqs. 4-5, with the per-head diagonal decay of the
+ * Fig. 12 caption): for every sequence and head h, with lambda = decay[h],
+ *
+ *     o_t = sum_{u <= t} lambda^(t-u) (q_t . k_u) v_u            (left product)
+ *         = q_t kv_t,  kv_t = lambda kv_{t-1} + k_t^T v_t,  kv_{-1} = 0
+ *                                                         (right product)
+ *
+ * computed chunkwise: inside a chunk the masked left product
+ * [(Q_i K_i^T) (.) M] V_i, across chunks the right product through a d x d
+ * state carried on chip (§2.2.1 "intra-block" / "inter-block").  Packed
+ * variable-length batches follow §3.2 ("data packing"): each sequence starts
+ * from a zero state.  Decode is the recursion applied to one new token per
+ * sequence, updating a cached state in place (§3.3.1 fused decode KV update,
+ * §3.3.2 separate prefill and decode kernels).
+ *
+ * Conventions for every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *     allocates no device memory and keeps no per-call state.
+ *   - Work is enqueued on `stream` (a cudaStream_t passed as void*; NULL means
+ *     the legacy default stream).  Calls never synchronise; results are ready
+ *     when the stream reaches that point.
+ *   - Argument errors are detected on the host before anything is launched
+ *     and return LA_ERR_INVALID_ARG / LA_ERR_UNSUPPORTED with nothing written.
+ *     A failed launch returns LA_ERR_CUDA.  Errors that only the GPU can see
+ *     (e.g. a cu_seqlens array that is not monotone) are not checked: results
+ *     are then unspecified but every access stays inside the buffers whose
+ *     sizes the arguments state.
+ *   - Every pointer must be 16-byte aligned.  Outputs must not alias inputs.
+ *   - No C++ exception crosses this boundary.
+ *   - lightning_attn_last_error() returns a human-readable reason for the
+ *     last non-LA_OK status returned on the calling host thread.
+ */
+#ifndef LIGHTNING_ATTN_H
+#define LIGHTNING_ATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum la_status {
+    LA_OK = 0,
+    LA_ERR_INVALID_ARG = 1,   /* null / misaligned pointer, bad size or dtype */
+    LA_ERR_UNSUPPORTED = 2,   /* valid request this build has no kernel for   */
+    LA_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed          */
+    LA_ERR_TIMEOUT = 4        /* reserved: a bounded device-side wait gave up  */
+} la_status;
+
+typedef enum la_dtype {
+    LA_DTYPE_BF16 = 0,        /* q, k, v, out are bf16; fp32 accumulation */
+    LA_DTYPE_FP32 = 1         /* q, k, v, out are fp32; fp32 FFMA throughout */
+} la_dtype;
+
+/*
+ * Chunkwise prefill over a packed batch of sequences.
+ *   (MiniMax-01 report §2.2.1 block split; §3.2 data packing; §3.3.1 fused
+ *    prefill preprocessing -- here the tile staging and the decay values are
+ *    produced inside the kernel.)
+ *
+ * q, k, v      [total_tokens, num_heads, head_dim], dtype `dtype`, row-major;
+ *              token-major packed: sequence s owns rows
+ *              [cu_seqlens[s], cu_seqlens[s+1]).
+ * decay        [num_heads] fp32, lambda_h, each in (0, 1] (not checked on the
+ *              device; values outside give the formula's value, possibly
+ *              inf/nan).
+ * cu_seqlens   [num_seqs + 1] int32 DEVICE array, cu_seqlens[0] = 0,
+ *              non-decreasing, cu_seqlens[num_seqs] = total_tokens.  Empty
+ *              sequences are allowed (their final state is zero).
+ * num_seqs     >= 0 (0: nothing is done).
+ * total_tokens >= 0.
+ * num_heads    >= 1.
+ * head_dim     64 or 128.
+ * chunk        block size B: 0 picks the default for the path
+ *              (128 on the tensor-core path, 64 otherwise); the tensor-core
+ *              path (bf16, head_dim 128) takes 128; the fp32 / CUDA-core path
+ *              takes 16, 32 or 64.  The result does not depend on B beyond
+ *              rounding (K3 report reading notes, CP for linear attention:
+ *              any chunk split is mathematically equivalent).
+ * dtype        LA_DTYPE_BF16 or LA_DTYPE_FP32.
+ * out          [total_tokens, num_heads, head_dim], dtype `dtype`: o_t.
+ * final_state  nullable; [num_seqs, num_heads, head_dim, head_dim] fp32:
+ *              final_state[s][h][i][j] = sum_u lambda_h^(L_s-1-u) k_u[i] v_u[j]
+ *              (the state after the last token of sequence s, i.e. the prefix
+ *              cache a following decode step continues from).
+ * stream       cudaStream_t as void*.
+ */
+la_status lightning_attn_prefill(const void *q, const void *k, const void *v,
+                                 const float *decay, const int32_t *cu_seqlens,
+                                 int32_t num_seqs, int32_t total_tokens,
+                                 int32_t num_heads, int32_t head_dim,
+                                 int32_t chunk, la_dtype dtype, void *out,
+                                 float *final_state, void *stream);
+
+/*
+ * One decode step for a batch of sequences, each with one new token.
+ *   (MiniMax-01 report §3.3.2: length-1 inputs get their own memory-bound
+ *    kernel; §3.3.1: the KV computation and the prefix-KV-cache update are
+ *    fused into one kernel.)
+ *
+ * For every b < batch, h < num_heads, with lambda = decay[h]:
+ *     state[b][h] <- lambda * state[b][h] + k[b][h]^T v[b][h]     (in place)
+ *     out[b][h]    = q[b][h] . state[b][h]                 (after the update)
+ *
+ * q, k, v, out [batch, num_heads, head_dim], dtype `dtype`.
+ * decay        [num_heads] fp32.
+ * state        [batch, num_heads, head_dim, head_dim] fp32, read and written.
+ * batch >= 0 (0: nothing is done), num_heads >= 1, head_dim 64 or 128.
+ */
+la_status lightning_attn_decode(const void *q, const void *k, const void *v,
+                                const float *decay, float *state,
+                                int32_t batch, int32_t num_heads,
+                                int32_t head_dim, la_dtype dtype, void *out,
+                                void *stream);
+
+/*
+ * Synchronises `stream`, then reports whether a kernel of this library raised
+ * its device error word since the last call (and clears it).  The
+ * tensor-core prefill bounds every wait of its pipeline (about 2 s); a wait
+ * that gives up ends the kernel cleanly (the context stays usable), leaves the
+ * outputs of that launch unspecified and makes this call return
+ * LA_ERR_TIMEOUT.  Returns LA_ERR_CUDA if the synchronisation fails.
+ */
+la_status lightning_attn_device_status(void *stream);
+
+/*
+ * Failure-detection self test: launches one CTA that waits on a barrier
+ * nothing will ever complete, with the same bounded wait the prefill
+ * pipeline uses, giving up after timeout_ns.  A following
+ * lightning_attn_device_status() must return LA_ERR_TIMEOUT.
+ */
+la_status lightning_attn_selftest_wait_timeout(uint64_t timeout_ns, void *stream);
+
+/* Static English name of a status code; never NULL. */
+const char *lightning_attn_status_string(la_status status);
+
+/* Reason for the last non-OK status on this host thread ("" if none). */
+const char *lightning_attn_last_error(void);
+
+/* ABI version of this header: (major << 16) | minor. */
+int32_t lightning_attn_version(void);
+
+#define LIGHTNING_ATTN_VERSION ((1 << 16) | 0)
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIGHTNING_ATTN_H */

@@ -1,1 +1,184 @@
-"""GB300-native lightning attention (chunkwise decayed causal linear attention)."""
+"""GB300-native lightning attention: chunkwise decayed causal linear attention.
+
+Python binding over the C ABI of ``liblightning_attn.so`` (declared in
+``include/lightning_attn.h``).  This module only marshals arguments -- torch
+tensors become device pointers and sizes, the current CUDA stream becomes a
+``cudaStream_t`` -- every step of the computation runs in the library's CUDA
+kernels.  There is no fallback: if the library is not built, or a call is not
+supported, an exception is raised.
+
+    o_t = sum_{u <= t} lambda_h^(t-u) (q_t . k_u) v_u     (per sequence, head)
+
+(MiniMax-01 technical report, §2.2.1 Lightning Attention, eqs. 4-5 with the
+per-head diagonal decay of Fig. 12; §3.3 inference kernels.)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+import torch
+
+from . import workloads  # noqa: F401  (seeded input recipes)
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "liblightning_attn.so")
+HEADER = os.path.join(os.path.dirname(_PKG), "include", "lightning_attn.h")
+
+LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_CUDA, LA_ERR_TIMEOUT = range(5)
+LA_DTYPE_BF16, LA_DTYPE_FP32 = 0, 1
+
+_lock = threading.Lock()
+_lib = None
+
+
+class LightningAttnError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(message)
+        self.status = status
+
+
+def header_functions(path: str = HEADER) -> list[str]:
+    """Names of the functions the public header declares."""
+    text = open(path).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^\s*(?:const\s+)?[\w]+\s*\*?\s*(lightning_attn_\w+)\s*\(", text, flags=re.M)
+
+
+def load(path: str = LIB_PATH):
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"lightning-attention CUDA library not found at {path}; build it with "
+                    "`python -m lightning_attention_attn_gb300.build`")
+            lib = ctypes.CDLL(path)
+            vp, i32 = ctypes.c_void_p, ctypes.c_int32
+            lib.lightning_attn_prefill.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32,
+                                                   i32, ctypes.c_int, vp, vp, vp]
+            lib.lightning_attn_prefill.restype = ctypes.c_int
+            lib.lightning_attn_decode.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32,
+                                                  ctypes.c_int, vp, vp]
+            lib.lightning_attn_decode.restype = ctypes.c_int
+            lib.lightning_attn_status_string.argtypes = [ctypes.c_int]
+            lib.lightning_attn_status_string.restype = ctypes.c_char_p
+            lib.lightning_attn_last_error.argtypes = []
+            lib.lightning_attn_last_error.restype = ctypes.c_char_p
+            lib.lightning_attn_version.argtypes = []
+            lib.lightning_attn_version.restype = ctypes.c_int32
+            lib.lightning_attn_device_status.argtypes = [vp]
+            lib.lightning_attn_device_status.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _check(status: int, what: str):
+    if status != LA_OK:
+        lib = load()
+        name = lib.lightning_attn_status_string(status).decode()
+        msg = lib.lightning_attn_last_error().decode()
+        raise LightningAttnError(status, f"{what}: {name}: {msg}")
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return LA_DTYPE_BF16
+    if t.dtype == torch.float32:
+        return LA_DTYPE_FP32
+    raise TypeError(f"unsupported dtype {t.dtype} (bf16 or fp32)")
+
+
+def _dev(t: torch.Tensor, name: str) -> int:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor (got {t.device})")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def prefill(q, k, v, decay, cu_seqlens=None, *, chunk: int = 0, out=None,
+            final_state=None, return_state: bool = True, stream=None):
+    """Chunkwise lightning-attention prefill.
+
+    q, k, v: [T, H, d] (bf16 or fp32, same dtype, CUDA, contiguous), packed
+    token-major; cu_seqlens: int32 [nseq + 1] on the device (None = one
+    sequence of length T); decay: fp32 [H].  Returns ``(out, final_state)``
+    with out [T, H, d] in the input dtype and final_state fp32
+    [nseq, H, d, d] (None if ``return_state`` is False).
+    """
+    if q.dim() != 3:
+        raise ValueError("q must be [T, H, d]")
+    T, H, d = q.shape
+    for name, t in (("k", k), ("v", v)):
+        if t.shape != q.shape or t.dtype != q.dtype:
+            raise ValueError(f"{name} must match q in shape and dtype")
+    if cu_seqlens is None:
+        cu_seqlens = torch.tensor([0, T], dtype=torch.int32, device=q.device)
+    if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1:
+        raise ValueError("cu_seqlens must be a 1-D int32 tensor")
+    if decay.dtype != torch.float32 or decay.numel() != H:
+        raise ValueError("decay must be fp32 [H]")
+    nseq = cu_seqlens.numel() - 1
+    if out is None:
+        out = torch.empty_like(q)
+    if final_state is None and return_state:
+        final_state = torch.empty((nseq, H, d, d), dtype=torch.float32, device=q.device)
+    lib = load()
+    st = lib.lightning_attn_prefill(
+        _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(decay, "decay"),
+        _dev(cu_seqlens, "cu_seqlens"), nseq, T, H, d, int(chunk), _dtype_code(q),
+        _dev(out, "out"), None if final_state is None else _dev(final_state, "final_state"),
+        _stream_handle(stream))
+    _check(st, "lightning_attn_prefill")
+    return out, final_state
+
+
+def decode(q, k, v, decay, state, *, out=None, stream=None):
+    """One decode step: state <- lambda state + k^T v (in place), out = q state.
+
+    q, k, v: [B, H, d]; state: fp32 [B, H, d, d] (updated in place);
+    decay: fp32 [H].  Returns out [B, H, d] in the input dtype.
+    """
+    if q.dim() != 3:
+        raise ValueError("q must be [B, H, d]")
+    Bn, H, d = q.shape
+    for name, t in (("k", k), ("v", v)):
+        if t.shape != q.shape or t.dtype != q.dtype:
+            raise ValueError(f"{name} must match q in shape and dtype")
+    if state.dtype != torch.float32 or tuple(state.shape) != (Bn, H, d, d):
+        raise ValueError("state must be fp32 [B, H, d, d]")
+    if decay.dtype != torch.float32 or decay.numel() != H:
+        raise ValueError("decay must be fp32 [H]")
+    if out is None:
+        out = torch.empty_like(q)
+    lib = load()
+    st = lib.lightning_attn_decode(
+        _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(decay, "decay"),
+        _dev(state, "state"), Bn, H, d, _dtype_code(q), _dev(out, "out"),
+        _stream_handle(stream))
+    _check(st, "lightning_attn_decode")
+    return out
+
+
+def device_status(stream=None) -> None:
+    """Synchronises ``stream`` and raises if a kernel reported a device-side
+    error (a bounded wait that gave up)."""
+    _check(load().lightning_attn_device_status(_stream_handle(stream)),
+           "lightning_attn_device_status")
+
+
+def version() -> tuple[int, int]:
+    v = int(load().lightning_attn_version())
+    return v >> 16, v & 0xFFFF

@@ -1,0 +1,137 @@
+// C-ABI front end of liblightning_attn.so: argument validation on the host,
+// dispatch to the kernels, status mapping.  See include/lightning_attn.h for
+// the contract of every entry point.
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <string>
+
+#include <cuda_runtime.h>
+
+#include "../../include/lightning_attn.h"
+#include "la_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+la_status fail(la_status s, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+la_status fail(la_status s, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return s;
+}
+
+la_status from_cuda(cudaError_t e, const char *what) {
+    if (e == cudaSuccess) return LA_OK;
+    if (e == cudaErrorNotSupported)
+        return fail(LA_ERR_UNSUPPORTED, "%s: no kernel for this configuration", what);
+    return fail(LA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+const char *lightning_attn_status_string(la_status s) {
+    switch (s) {
+        case LA_OK: return "LA_OK";
+        case LA_ERR_INVALID_ARG: return "LA_ERR_INVALID_ARG";
+        case LA_ERR_UNSUPPORTED: return "LA_ERR_UNSUPPORTED";
+        case LA_ERR_CUDA: return "LA_ERR_CUDA";
+        case LA_ERR_TIMEOUT: return "LA_ERR_TIMEOUT";
+    }
+    return "LA_ERR_UNKNOWN";
+}
+
+const char *lightning_attn_last_error(void) { return g_last_error.c_str(); }
+
+int32_t lightning_attn_version(void) { return LIGHTNING_ATTN_VERSION; }
+
+la_status lightning_attn_prefill(const void *q, const void *k, const void *v,
+                                 const float *decay, const int32_t *cu_seqlens,
+                                 int32_t num_seqs, int32_t total_tokens,
+                                 int32_t num_heads, int32_t head_dim,
+                                 int32_t chunk, la_dtype dtype, void *out,
+                                 float *final_state, void *stream) {
+    if (num_seqs < 0) return fail(LA_ERR_INVALID_ARG, "num_seqs < 0 (%d)", num_seqs);
+    if (total_tokens < 0) return fail(LA_ERR_INVALID_ARG, "total_tokens < 0 (%d)", total_tokens);
+    if (num_heads < 1) return fail(LA_ERR_INVALID_ARG, "num_heads < 1 (%d)", num_heads);
+    if (head_dim != 64 && head_dim != 128)
+        return fail(LA_ERR_INVALID_ARG, "head_dim must be 64 or 128 (got %d)", head_dim);
+    if (dtype != LA_DTYPE_BF16 && dtype != LA_DTYPE_FP32)
+        return fail(LA_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+    if (chunk != 0 && chunk != 16 && chunk != 32 && chunk != 64 && chunk != 128 && chunk != 256)
+        return fail(LA_ERR_INVALID_ARG, "chunk must be 0, 16, 32, 64, 128 or 256 (got %d)", chunk);
+    if (num_seqs == 0) return LA_OK;
+    if (!cu_seqlens || !decay) return fail(LA_ERR_INVALID_ARG, "null decay or cu_seqlens");
+    if (total_tokens > 0 && (!q || !k || !v || !out))
+        return fail(LA_ERR_INVALID_ARG, "null q, k, v or out");
+    if ((q && !aligned16(q)) || (k && !aligned16(k)) || (v && !aligned16(v)) ||
+        (out && !aligned16(out)) || (final_state && !aligned16(final_state)) ||
+        !aligned16(decay) || !aligned16(cu_seqlens))
+        return fail(LA_ERR_INVALID_ARG, "every pointer must be 16-byte aligned");
+    if ((long long)num_seqs * num_heads > 0x7fffffffLL / 4)
+        return fail(LA_ERR_INVALID_ARG, "num_seqs * num_heads too large");
+
+    la::PrefillArgs a{q, k, v, decay, cu_seqlens, num_seqs, total_tokens, num_heads,
+                      head_dim, chunk, out, final_state, static_cast<cudaStream_t>(stream)};
+    if (total_tokens == 0) {  // every sequence is empty: states are zero
+        if (!final_state) return LA_OK;
+        const size_t bytes = (size_t)num_seqs * num_heads * head_dim * head_dim * sizeof(float);
+        return from_cuda(cudaMemsetAsync(final_state, 0, bytes, a.stream), "prefill (empty)");
+    }
+    const bool tc = dtype == LA_DTYPE_BF16 && head_dim == 128 && (chunk == 0 || chunk == 128);
+    if (tc) return from_cuda(la::prefill_tc_bf16(a), "prefill (tcgen05)");
+    if (chunk == 128 || chunk == 256)
+        return fail(LA_ERR_UNSUPPORTED,
+                    "chunk %d needs the tensor-core path (bf16, head_dim 128)", chunk);
+    if (dtype == LA_DTYPE_FP32) return from_cuda(la::prefill_simt_f32(a), "prefill (fp32)");
+    return from_cuda(la::prefill_simt_bf16(a), "prefill (bf16, CUDA cores)");
+}
+
+la_status lightning_attn_decode(const void *q, const void *k, const void *v,
+                                const float *decay, float *state, int32_t batch,
+                                int32_t num_heads, int32_t head_dim, la_dtype dtype,
+                                void *out, void *stream) {
+    if (batch < 0) return fail(LA_ERR_INVALID_ARG, "batch < 0 (%d)", batch);
+    if (num_heads < 1) return fail(LA_ERR_INVALID_ARG, "num_heads < 1 (%d)", num_heads);
+    if (head_dim != 64 && head_dim != 128)
+        return fail(LA_ERR_INVALID_ARG, "head_dim must be 64 or 128 (got %d)", head_dim);
+    if (dtype != LA_DTYPE_BF16 && dtype != LA_DTYPE_FP32)
+        return fail(LA_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+    if (batch == 0) return LA_OK;
+    if (!q || !k || !v || !decay || !state || !out)
+        return fail(LA_ERR_INVALID_ARG, "null pointer argument");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(decay) ||
+        !aligned16(state) || !aligned16(out))
+        return fail(LA_ERR_INVALID_ARG, "every pointer must be 16-byte aligned");
+    if ((long long)batch * num_heads > 0x7fffffffLL)
+        return fail(LA_ERR_INVALID_ARG, "batch * num_heads too large");
+    la::DecodeArgs a{q, k, v, decay, state, batch, num_heads, head_dim, out,
+                     static_cast<cudaStream_t>(stream)};
+    if (dtype == LA_DTYPE_FP32) return from_cuda(la::decode_f32(a), "decode (fp32)");
+    return from_cuda(la::decode_bf16(a), "decode (bf16)");
+}
+
+la_status lightning_attn_device_status(void *stream) {
+    unsigned int err = 0;
+    const la_status st =
+        from_cuda(la::take_device_error(static_cast<cudaStream_t>(stream), &err), "device_status");
+    if (st != LA_OK) return st;
+    if (err) return fail(LA_ERR_TIMEOUT, "a bounded device-side wait gave up");
+    return LA_OK;
+}
+
+la_status lightning_attn_selftest_wait_timeout(uint64_t timeout_ns, void *stream) {
+    return from_cuda(la::selftest_wait_timeout(timeout_ns, static_cast<cudaStream_t>(stream)),
+                     "selftest_wait_timeout");
+}
+
+}  // extern "C"

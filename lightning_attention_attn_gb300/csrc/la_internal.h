@@ -1,0 +1,46 @@
+// Internal interface between the C-ABI front end (api.cu) and the kernels.
+// Not installed; the public interface is include/lightning_attn.h.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace la {
+
+struct PrefillArgs {
+    const void *q, *k, *v;      // [T, H, D]
+    const float *decay;         // [H]
+    const int32_t *cu_seqlens;  // [nseq + 1], device
+    int nseq, total_tokens, num_heads, head_dim, chunk;
+    void *out;                  // [T, H, D]
+    float *final_state;         // [nseq, H, D, D] or nullptr
+    cudaStream_t stream;
+};
+
+struct DecodeArgs {
+    const void *q, *k, *v;      // [B, H, D]
+    const float *decay;         // [H]
+    float *state;               // [B, H, D, D]
+    int batch, num_heads, head_dim;
+    void *out;                  // [B, H, D]
+    cudaStream_t stream;
+};
+
+// CUDA-core chunkwise prefill; chunk in {16, 32, 64}, head_dim in {64, 128}.
+cudaError_t prefill_simt_f32(const PrefillArgs &a);
+cudaError_t prefill_simt_bf16(const PrefillArgs &a);
+
+// tcgen05 / TMEM / TMA prefill; bf16, head_dim 128, chunk 128.
+// Returns cudaErrorNotSupported when the tensor-map encoder is unavailable.
+cudaError_t prefill_tc_bf16(const PrefillArgs &a);
+
+// Synchronises `stream`, then reads and clears the device error word.
+cudaError_t take_device_error(cudaStream_t stream, unsigned int *err);
+// Launches a kernel whose bounded wait must time out after timeout_ns.
+cudaError_t selftest_wait_timeout(uint64_t timeout_ns, cudaStream_t stream);
+
+// Memory-bound decode step; head_dim in {64, 128}.
+cudaError_t decode_f32(const DecodeArgs &a);
+cudaError_t decode_bf16(const DecodeArgs &a);
+
+}  // namespace la

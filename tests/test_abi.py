@@ -1,0 +1,127 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+the public header declares, and rejects bad arguments on the host before
+touching the device."""
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+import lightning_attention_attn_gb300 as la
+from lightning_attention_attn_gb300 import build as labuild
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = labuild.build()
+    return la.load(path)
+
+
+def test_header_declares_expected_calls():
+    names = la.header_functions()
+    for n in ("lightning_attn_prefill", "lightning_attn_decode",
+              "lightning_attn_status_string", "lightning_attn_last_error",
+              "lightning_attn_version", "lightning_attn_device_status",
+              "lightning_attn_selftest_wait_timeout"):
+        assert n in names, n
+
+
+def test_library_exports_every_header_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", la.LIB_PATH],
+                         capture_output=True, text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for name in la.header_functions():
+        assert name in exported, f"{name} declared in the header but not exported"
+        assert hasattr(lib, name)
+
+
+def test_version(lib):
+    assert la.version() == (1, 0)
+
+
+def test_status_strings(lib):
+    for code, name in enumerate(["LA_OK", "LA_ERR_INVALID_ARG", "LA_ERR_UNSUPPORTED",
+                                 "LA_ERR_CUDA", "LA_ERR_TIMEOUT"]):
+        assert lib.lightning_attn_status_string(code).decode() == name
+    assert lib.lightning_attn_status_string(99).decode() == "LA_ERR_UNKNOWN"
+
+
+A = 0x10000  # a 16-byte aligned fake address: validation must fail before any use
+
+
+def _prefill(lib, **kw):
+    args = dict(q=A, k=A, v=A, decay=A, cu=A, nseq=1, T=8, H=2, d=128, chunk=0,
+                dtype=la.LA_DTYPE_BF16, out=A, fs=A, stream=None)
+    args.update(kw)
+    return lib.lightning_attn_prefill(args["q"], args["k"], args["v"], args["decay"],
+                                      args["cu"], args["nseq"], args["T"], args["H"],
+                                      args["d"], args["chunk"], args["dtype"], args["out"],
+                                      args["fs"], args["stream"])
+
+
+@pytest.mark.parametrize("kw, status", [
+    (dict(nseq=-1), la.LA_ERR_INVALID_ARG),
+    (dict(T=-5), la.LA_ERR_INVALID_ARG),
+    (dict(H=0), la.LA_ERR_INVALID_ARG),
+    (dict(d=96), la.LA_ERR_INVALID_ARG),
+    (dict(dtype=7), la.LA_ERR_INVALID_ARG),
+    (dict(chunk=48), la.LA_ERR_INVALID_ARG),
+    (dict(q=None), la.LA_ERR_INVALID_ARG),
+    (dict(out=None), la.LA_ERR_INVALID_ARG),
+    (dict(cu=None), la.LA_ERR_INVALID_ARG),
+    (dict(decay=None), la.LA_ERR_INVALID_ARG),
+    (dict(q=A + 4), la.LA_ERR_INVALID_ARG),
+    (dict(fs=A + 8), la.LA_ERR_INVALID_ARG),
+    (dict(dtype=la.LA_DTYPE_FP32, chunk=128), la.LA_ERR_UNSUPPORTED),
+    (dict(d=64, chunk=256), la.LA_ERR_UNSUPPORTED),
+    (dict(nseq=0), la.LA_OK),  # nothing to do: returns before any CUDA call
+])
+def test_prefill_host_validation(lib, kw, status):
+    assert _prefill(lib, **kw) == status
+    if status != la.LA_OK:
+        assert lib.lightning_attn_last_error().decode() != ""
+
+
+def _decode(lib, **kw):
+    args = dict(q=A, k=A, v=A, decay=A, state=A, B=4, H=2, d=128,
+                dtype=la.LA_DTYPE_BF16, out=A, stream=None)
+    args.update(kw)
+    return lib.lightning_attn_decode(args["q"], args["k"], args["v"], args["decay"],
+                                     args["state"], args["B"], args["H"], args["d"],
+                                     args["dtype"], args["out"], args["stream"])
+
+
+@pytest.mark.parametrize("kw, status", [
+    (dict(B=-1), la.LA_ERR_INVALID_ARG),
+    (dict(H=0), la.LA_ERR_INVALID_ARG),
+    (dict(d=32), la.LA_ERR_INVALID_ARG),
+    (dict(dtype=3), la.LA_ERR_INVALID_ARG),
+    (dict(state=None), la.LA_ERR_INVALID_ARG),
+    (dict(out=A + 2), la.LA_ERR_INVALID_ARG),
+    (dict(B=0), la.LA_OK),
+])
+def test_decode_host_validation(lib, kw, status):
+    assert _decode(lib, **kw) == status
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    import importlib
+    mod = importlib.import_module("lightning_attention_attn_gb300")
+    with pytest.raises(RuntimeError, match="not found"):
+        # a fresh loader pointed at a missing file must raise, never fall back
+        saved = mod._lib
+        mod._lib = None
+        try:
+            mod.load(str(tmp_path / "missing.so"))
+        finally:
+            mod._lib = saved
+
+
+def test_product_path_does_not_import_oracle():
+    pkg = os.path.dirname(la.__file__)
+    for root, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(root, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "lightning_oracle" not in text, f

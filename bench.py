@@ -364,6 +364,36 @@ def run_ours(args, ws, rank, local):
     return line
 
 
+def run_only(args):
+    """W + K back-to-back launches of one kernel on its measured workload
+    (the 8K-token layer for prefill, the 128-sequence batch for decode), for
+    profilers: no clocks, no e2e, no CPU baseline."""
+    import torch
+    import lightning_attention_attn_gb300 as la
+    from lightning_attention_attn_gb300 import build as labuild
+    from lightning_attention_attn_gb300 import workloads as wl
+    la.load(labuild.build())
+    if args.only == "prefill":
+        cfg = wl.PREFILL_8K
+        inp = wl.prefill_inputs(cfg["lengths"], cfg["num_heads"], cfg["head_dim"],
+                                dtype=torch.bfloat16, seed=0, device="cuda")
+        out = torch.empty_like(inp.q)
+        fs = torch.empty((1, cfg["num_heads"], 128, 128), device="cuda")
+        for _ in range(args.warmup + args.steps):
+            la.prefill(inp.q, inp.k, inp.v, inp.decay, inp.cu_seqlens, out=out, final_state=fs)
+    else:
+        cfg = wl.DECODE_128
+        n = args.warmup + args.steps
+        dinp = wl.decode_inputs(cfg["batch"], cfg["num_heads"], cfg["head_dim"], steps=n,
+                                dtype=torch.bfloat16, seed=0, device="cuda")
+        out = torch.empty_like(dinp.q[0])
+        for t in range(n):
+            la.decode(dinp.q[t], dinp.k[t], dinp.v[t], dinp.decay, dinp.state, out=out)
+    torch.cuda.synchronize()
+    la.device_status()
+    return 0
+
+
 # --------------------------------------------------------- reference arm
 def run_reference(args, ws, rank):
     """The oracle (fp64, CPU, as it stands) on a bounded sample of the same
@@ -406,7 +436,12 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--only", choices=["prefill", "decode"], default=None,
+                    help="profiling aid: run just W + K launches of one kernel on its "
+                         "workload and print nothing else")
     args = ap.parse_args(argv)
+    if args.only:
+        return run_only(args)
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.impl == "reference":

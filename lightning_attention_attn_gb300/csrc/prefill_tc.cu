@@ -15,27 +15,40 @@
 // Work decomposition.  One CTA per (sequence, head, 64-wide value slice):
 // o[:, j] and KV[:, j] only depend on v[:, j], so splitting d_v = 128 in two
 // doubles the CTAs (128 for one 64-head sequence) while Q/K tiles are shared
-// by the two sibling CTAs through L2.  Per 128-token chunk the CTA runs four
-// tcgen05 MMAs (M = 128):
-//     S   = Q K^T          128x128x128  -> TMEM (double buffered)
-//     dKV = K^T Vhat       128x 64x128  -> TMEM   (Vhat = Lambda_K V)
-//     O2  = Q KVb          128x 64x128  -> TMEM   (KVb = bf16 copy of KV_{i-1})
-//     O1  = P V            128x 64x128  -> TMEM   (P = bf16 of S (.) M)
-// and the fp32 state lives in registers of the state warpgroup for the
-// whole sequence; only a bf16 copy of it (the MMA operand) goes to shared
-// memory.  Nothing but q, k, v (read once per CTA) and out / final state
-// (written once) touches HBM.
+// by the two sibling CTAs through L2.  Per 128-token chunk the CTA issues 32
+// tcgen05 MMAs (M = 128, fp32 accumulators in TMEM):
+//     S   = Q K^T                   128x128x128  bf16   (double buffered)
+//     dKV = K^T [Vhat_hi | Vhat_lo] 128x128x128  bf16   (Vhat = Lambda_K V)
+//     O2  = Q [KV_hi | KV_lo]       128x128x128  bf16   (KV = state after i-1)
+//     O1  = P V                     128x 64x128  fp16   (P read from TMEM)
+// A tcgen05.mma instruction costs about the same for N = 64 and N = 128, so
+// the values the tensor core can only take at 8 significant bits (Vhat and
+// the fp32 state copy) are passed as hi = bf16(x), lo = bf16(x - hi)
+// concatenated along N: one N = 128 instruction instead of two N = 64 ones,
+// and the two halves of the result are summed in fp32.  P and V go through
+// the tensor core as fp16 (11 significant bits), each with an exact
+// power-of-two scale chosen so the values sit at the top of the fp16 range
+// (P per row, V per chunk): no overflow, no subnormal loss, and the scale is
+// undone in fp32 in the epilogue.  The fp32 state itself lives in registers
+// of the state warpgroup for the whole sequence.  Nothing but q, k, v (read
+// once per CTA) and out / final state (written once) touches HBM.
+//
+// TMEM (512 columns): S buffer b = columns [128b, 128b + 128): S (fp32), then
+// P (fp16 pairs) over its first 64 columns and O1 (fp32) in its last 64;
+// O2 = [256, 384); dKV = [384, 512).
 //
 // Warp roles (320 threads):
-//   warps 0-3  mask warpgroup: S -> P = bf16(S (.) M) into shared memory
-//   warps 4-7  state warpgroup: Vhat, KV update, KVb, output epilogue
-//   warp  8    TMA producer (2-stage ring of Q, K, V tiles)
+//   warps 0-3  mask warpgroup: S -> P = fp16(2^-e_j S (.) M) into TMEM
+//   warps 4-7  state warpgroup: Vhat / fp16 V, KV update, KV copy, output
+//   warp  8    TMA producer: Q, K, V two-slot rings; output TMA stores
 //   warp  9    MMA issuer (one thread)
-// Every wait is bounded: a wait that gives up sets a CTA-wide abort flag, all
-// roles leave their loops, in-flight TMA loads and MMAs are drained, TMEM is
-// freed, and a device error word is raised for lightning_attn_device_status.
+// Every wait is bounded and warp-uniform: a wait that gives up sets a CTA-wide
+// abort flag, all roles leave their loops, in-flight TMA copies and MMAs are
+// drained, TMEM is freed, and a device error word is raised for
+// lightning_attn_device_status.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -63,48 +76,56 @@ constexpr int kMmaWarp = 9;
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
 
 // Shared memory (offsets from a 1024-byte aligned base).  Operand tiles are
-// 128-byte swizzled rows of 64 bf16, 8-row atoms of 1024 bytes.
-constexpr uint32_t kHalf = BC * 128;                  // 128 rows x 128 B = 16 KB
-constexpr uint32_t kQBytes = 2 * kHalf;               // Q: d split in two 64-col halves
-constexpr uint32_t kKBytes = 2 * kHalf;
-constexpr uint32_t kVBytes = kHalf;                   // V slice: 64 cols
-constexpr uint32_t kStageBytes = kQBytes + kKBytes + kVBytes;  // 80 KB
-constexpr int kStages = 2;
-constexpr uint32_t kOffP = kStages * kStageBytes;     // P: 128 x 128 bf16, two halves
-constexpr uint32_t kOffVhat = kOffP + 2 * kHalf;      // Vhat: 128 tokens x 64
-constexpr uint32_t kOffKVb = kOffVhat + kHalf;        // KVb: 128 d_k x 64
-constexpr uint32_t kOffCtrl = kOffKVb + kHalf;
+// 128-byte swizzled rows of 64 16-bit values in 8-row, 1024-byte atoms.
+constexpr uint32_t kHalf = BC * 128;            // 128 rows x 128 B = 16 KB
+constexpr uint32_t kOffQ = 0;                   // 2 slots x (two 64-col halves)
+constexpr uint32_t kOffK = kOffQ + 4 * kHalf;   // 2 slots x (two halves)
+constexpr uint32_t kOffV = kOffK + 4 * kHalf;   // 2 slots x 64 cols; fp16 after
+                                                // conversion; then output staging
+constexpr uint32_t kOffVhat = kOffV + 2 * kHalf;   // hi, lo: 128 tokens x 64
+constexpr uint32_t kOffKVb = kOffVhat + 2 * kHalf; // hi, lo: 128 d_k x 64
+constexpr uint32_t kOffCtrl = kOffKVb + 2 * kHalf;
 
 struct Ctrl {
-    uint64_t full[kStages], empty[kStages];
-    uint64_t s_full[2], s_free[2];
-    uint64_t p_full, p_free, o_full, o_free;
-    uint64_t dkv_full, dkv_free, vhat_full, kv_full, kv_free, mma_done;
+    uint64_t full_q[2], full_k[2], full_v[2], empty_q[2], empty_k[2], out_staged[2];
+    uint64_t s_full[2], s_free[2], p_full[2], vmax_ready[2];
+    uint64_t o_full, o2_free, dkv_full, dkv_free, vhat_full, kv_full, kv_free, mma_done;
     uint32_t tmem_base;
     int abort;
     int seq_slot;
     int pad;
-    float pw[BC + 4];  // pw[e] = lambda^e, e = 0..BC
+    float pw[BC + 4];         // pw[e] = lambda^e, e = 0..BC
+    float rowscale[2][BC];    // 2^e_j of P's rows, per S buffer
+    float vmax[2][4];         // per-warp max |v| of a chunk, double buffered
 };
 constexpr uint32_t kSmemBytes = kOffCtrl + sizeof(Ctrl) + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
-// TMEM columns (fp32 accumulators, lane = row).
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO1 = 256, kColO2 = 320, kColDKV = 384;
+constexpr uint32_t kColO2 = 256, kColDKV = 384;
 
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, 0, 0);   // Q (K-major) x K (K-major)
-constexpr uint32_t kIdescKV = idesc_bf16_f32(128, DV, 1, 1);   // K^T (M-major) x Vhat (N-major)
-constexpr uint32_t kIdescO2 = idesc_bf16_f32(128, DV, 0, 1);   // Q (K-major) x KVb (N-major)
-constexpr uint32_t kIdescPV = idesc_bf16_f32(128, DV, 0, 1);   // P (K-major) x V (N-major)
+constexpr uint32_t kIdescKV = idesc_bf16_f32(128, 128, 1, 1);  // K^T (M-major) x Vhat (N-major)
+constexpr uint32_t kIdescO2 = idesc_bf16_f32(128, 128, 0, 1);  // Q (K-major) x KV (N-major)
+constexpr uint32_t kIdescPV = idesc_fp16_f32(128, DV, 0, 1);   // P (TMEM) x V (N-major)
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
 }
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
 __device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
     __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162 *>(&u);
     return __bfloat1622float2(v);
+}
+// hi = bf16(x), lo = bf16(x - hi), packed in pairs
+__device__ __forceinline__ void split_bf16(float a, float b, uint32_t &hi, uint32_t &lo) {
+    const __nv_bfloat16 ha = __float2bfloat16_rn(a), hb = __float2bfloat16_rn(b);
+    hi = (uint32_t)__bfloat16_as_ushort(ha) | ((uint32_t)__bfloat16_as_ushort(hb) << 16);
+    lo = pack_bf16(a - __bfloat162float(ha), b - __bfloat162float(hb));
 }
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
@@ -120,12 +141,31 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
                  : "memory");
     return v;
 }
+// Exact power-of-two scale exponent: for m > 0 finite, returns e with
+// m * 2^-e in [2^14, 2^15) (the top of the fp16 range), clamped to
+// [-126, 126] so that both 2^e and 2^-e are normal floats; 0 for m == 0 or
+// a non-finite m.
+__device__ __forceinline__ int fp16_scale_exp(float m) {
+    if (!(m > 0.f) || m > 3.0e38f) return 0;
+    const int eb = (int)((__float_as_uint(m) >> 23) & 0xff);
+    const int e = (eb == 0 ? -126 : eb - 127) - 14;
+    return max(-126, min(126, e));
+}
+__device__ __forceinline__ float exp2i(int e) {  // 2^e for -126 <= e <= 127
+    return __uint_as_float((uint32_t)(e + 127) << 23);
+}
+// A bounded wait whose outcome is the same for every lane of the warp (so
+// the warp stays converged for the .sync.aligned tcgen05 instructions).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
+    const bool ok = mbar_wait(bar, parity, abort, kTimeoutNs);
+    return __all_sync(0xffffffffu, ok);
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const float *__restrict__ decay,
-                  const int32_t *__restrict__ cu, int nseq, int T, int H,
-                  __nv_bfloat16 *__restrict__ out, float *__restrict__ final_state) {
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                  const float *__restrict__ decay, const int32_t *__restrict__ cu, int nseq, int T,
+                  int H, __nv_bfloat16 *__restrict__ out, float *__restrict__ final_state) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *base = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -145,21 +185,26 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     const float lam = __ldg(decay + h);
 
     auto bar = [&](const uint64_t &b) { return smem_u32(&b); };
+    auto qslot = [&](int st) { return sb + kOffQ + st * 2 * kHalf; };
+    auto kslot = [&](int st) { return sb + kOffK + st * 2 * kHalf; };
+    auto vslot = [&](int st) { return sb + kOffV + st * kHalf; };
 
     // ---- set-up ----
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kStages; ++i) {
-            mbar_init(bar(cs.full[i]), 1);
-            mbar_init(bar(cs.empty[i]), 1);
-        }
         for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(cs.full_q[i]), 1);
+            mbar_init(bar(cs.full_k[i]), 1);
+            mbar_init(bar(cs.full_v[i]), 1);
+            mbar_init(bar(cs.empty_q[i]), 1);
+            mbar_init(bar(cs.empty_k[i]), 1);
+            mbar_init(bar(cs.out_staged[i]), 128);
             mbar_init(bar(cs.s_full[i]), 1);
             mbar_init(bar(cs.s_free[i]), 128);
+            mbar_init(bar(cs.p_full[i]), 128);
+            mbar_init(bar(cs.vmax_ready[i]), 128);
         }
-        mbar_init(bar(cs.p_full), 128);
-        mbar_init(bar(cs.p_free), 1);
         mbar_init(bar(cs.o_full), 1);
-        mbar_init(bar(cs.o_free), 128);
+        mbar_init(bar(cs.o2_free), 128);
         mbar_init(bar(cs.dkv_full), 1);
         mbar_init(bar(cs.dkv_free), 128);
         mbar_init(bar(cs.vhat_full), 128);
@@ -170,10 +215,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         fence_mbar_init();
     }
     for (int e = threadIdx.x; e <= BC; e += kThreads) cs.pw[e] = powf(lam, (float)e);
-    // P's blocks strictly above the diagonal are never written: zero them once.
-    for (int e = threadIdx.x; e < (int)(2 * kHalf / 16); e += kThreads)
-        st_shared_v4(sb + kOffP + e * 16, 0u, 0u, 0u, 0u);
-    fence_proxy_async_smem();
     if (warp == 0) {
         tmem_alloc(smem_u32(&cs.tmem_base), kTmemCols);
         tmem_relinquish();
@@ -190,39 +231,66 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             tma_prefetch_desc(&tmQ);
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
-            int issued = 0;
-            for (int i = 0; i < nch; ++i) {
+            tma_prefetch_desc(&tmO);
+            // Output tile of chunk c, staged by the state warpgroup in V slot
+            // c & 1, goes out with one TMA store; the slot is reusable once
+            // the store has read it.  Short (last) chunks are written by the
+            // state warpgroup directly, row by row.
+            auto store_out = [&](int c) -> bool {
+                if (!mbar_wait(bar(cs.out_staged[c & 1]), (c >> 1) & 1, abort_flag, kTimeoutNs))
+                    return false;
+                if (L - c * BC >= BC) {
+                    tma_store_2d(&tmO, vslot(c & 1), h * D + vs * DV, t0 + c * BC);
+                    bulk_commit_group();
+                    bulk_wait_read_all();
+                }
+                return true;
+            };
+            int nq = 0, nk = 0, nv = 0;
+            bool ok = true;
+            for (int i = 0; i < nch && ok; ++i) {
                 const int st = i & 1;
                 const uint32_t sph = (i >> 1) & 1;
-                if (!mbar_wait(bar(cs.empty[st]), sph ^ 1, abort_flag, kTimeoutNs)) break;
-                const uint32_t stage = sb + st * kStageBytes;
-                const uint32_t fb = bar(cs.full[st]);
-                mbar_arrive_expect_tx(fb, kStageBytes);
                 const int y = t0 + i * BC;
-                tma_load_2d(stage, &tmQ, fb, h * D, y);
-                tma_load_2d(stage + kHalf, &tmQ, fb, h * D + 64, y);
-                tma_load_2d(stage + kQBytes, &tmK, fb, h * D, y);
-                tma_load_2d(stage + kQBytes + kHalf, &tmK, fb, h * D + 64, y);
-                tma_load_2d(stage + kQBytes + kKBytes, &tmV, fb, h * D + vs * DV, y);
-                ++issued;
+                if (!(ok = mbar_wait(bar(cs.empty_q[st]), sph ^ 1, abort_flag, kTimeoutNs))) break;
+                mbar_arrive_expect_tx(bar(cs.full_q[st]), 2 * kHalf);
+                tma_load_2d(qslot(st), &tmQ, bar(cs.full_q[st]), h * D, y);
+                tma_load_2d(qslot(st) + kHalf, &tmQ, bar(cs.full_q[st]), h * D + 64, y);
+                ++nq;
+                if (!(ok = mbar_wait(bar(cs.empty_k[st]), sph ^ 1, abort_flag, kTimeoutNs))) break;
+                mbar_arrive_expect_tx(bar(cs.full_k[st]), 2 * kHalf);
+                tma_load_2d(kslot(st), &tmK, bar(cs.full_k[st]), h * D, y);
+                tma_load_2d(kslot(st) + kHalf, &tmK, bar(cs.full_k[st]), h * D + 64, y);
+                ++nk;
+                if (i >= 2 && !(ok = store_out(i - 2))) break;
+                mbar_arrive_expect_tx(bar(cs.full_v[st]), kHalf);
+                tma_load_2d(vslot(st), &tmV, bar(cs.full_v[st]), h * D + vs * DV, y);
+                ++nv;
             }
+            for (int c = max(0, nch - 2); ok && c < nch; ++c) ok = store_out(c);
+            bulk_wait_all();
             // Never leave with a load still landing in shared memory.
             int no_abort = 0;
-            for (int i = max(0, issued - kStages); i < issued; ++i)
-                mbar_wait(bar(cs.full[i & 1]), (i >> 1) & 1, &no_abort, kTimeoutNs);
+            for (int c = max(0, nq - 2); c < nq; ++c)
+                mbar_wait(bar(cs.full_q[c & 1]), (c >> 1) & 1, &no_abort, kTimeoutNs);
+            for (int c = max(0, nk - 2); c < nk; ++c)
+                mbar_wait(bar(cs.full_k[c & 1]), (c >> 1) & 1, &no_abort, kTimeoutNs);
+            for (int c = max(0, nv - 2); c < nv; ++c)
+                mbar_wait(bar(cs.full_v[c & 1]), (c >> 1) & 1, &no_abort, kTimeoutNs);
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
         // ================= MMA issuer =================
         if (lane == 0) {
-            const uint32_t pa = sb + kOffP, vha = sb + kOffVhat, kvb = sb + kOffKVb;
+            const uint32_t vha = sb + kOffVhat, kvb = sb + kOffKVb;
             for (int i = 0; i < nch; ++i) {
                 const int st = i & 1;
                 const uint32_t sph = (i >> 1) & 1, ph = i & 1;
-                const uint32_t qa = sb + st * kStageBytes, ka = qa + kQBytes, va = ka + kKBytes;
-                const uint32_t colS = st ? kColS1 : kColS0;
-                if (!mbar_wait(bar(cs.full[st]), sph, abort_flag, kTimeoutNs)) break;
-                // S_i = Q_i K_i^T
+                const uint32_t qa = qslot(st), ka = kslot(st), va = vslot(st);
+                const uint32_t colS = st * 128;
+                // S_i = Q_i K_i^T (buffer free once the epilogue of chunk i-2 read O1)
+                if (!mbar_wait(bar(cs.full_q[st]), sph, abort_flag, kTimeoutNs)) break;
+                if (!mbar_wait(bar(cs.full_k[st]), sph, abort_flag, kTimeoutNs)) break;
                 if (!mbar_wait(bar(cs.s_free[st]), sph ^ 1, abort_flag, kTimeoutNs)) break;
                 tc_fence_after();
 #pragma unroll
@@ -232,7 +300,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
                              sdesc_sw128(ka + off, 16, 1024), kIdescS, kk > 0);
                 }
                 mma_commit(bar(cs.s_full[st]));
-                // dKV_i = K_i^T Vhat_i
+                // dKV_i = K_i^T [Vhat_hi | Vhat_lo]
                 if (!mbar_wait(bar(cs.vhat_full), ph, abort_flag, kTimeoutNs)) break;
                 if (!mbar_wait(bar(cs.dkv_free), ph ^ 1, abort_flag, kTimeoutNs)) break;
                 tc_fence_after();
@@ -241,9 +309,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
                     mma_bf16(tmem + kColDKV, sdesc_sw128(ka + kk * 2048, kHalf, 1024),
                              sdesc_sw128(vha + kk * 2048, kHalf, 1024), kIdescKV, kk > 0);
                 mma_commit(bar(cs.dkv_full));
-                // O2_i = Q_i KVb_{i-1}
+                mma_commit(bar(cs.empty_k[st]));
+                // O2_i = Q_i [KV_hi | KV_lo] (the state after chunk i-1)
                 if (!mbar_wait(bar(cs.kv_full), ph, abort_flag, kTimeoutNs)) break;
-                if (!mbar_wait(bar(cs.o_free), ph ^ 1, abort_flag, kTimeoutNs)) break;
+                if (!mbar_wait(bar(cs.o2_free), ph ^ 1, abort_flag, kTimeoutNs)) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
@@ -252,18 +321,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
                              sdesc_sw128(kvb + kk * 2048, kHalf, 1024), kIdescO2, kk > 0);
                 }
                 mma_commit(bar(cs.kv_free));
-                // O1_i = P_i V_i
-                if (!mbar_wait(bar(cs.p_full), ph, abort_flag, kTimeoutNs)) break;
+                mma_commit(bar(cs.empty_q[st]));
+                // O1_i = P_i V_i (fp16; P in the first half of the S buffer,
+                // O1 into its second half)
+                if (!mbar_wait(bar(cs.p_full[st]), sph, abort_flag, kTimeoutNs)) break;
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < BC / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-                    mma_bf16(tmem + kColO1, sdesc_sw128(pa + off, 16, 1024),
-                             sdesc_sw128(va + kk * 2048, kHalf, 1024), kIdescPV, kk > 0);
-                }
+                for (int kk = 0; kk < BC / 16; ++kk)
+                    mma_bf16_tmem_a(tmem + colS + 64, tmem + colS + kk * 8,
+                                    sdesc_sw128(va + kk * 2048, kHalf, 1024), kIdescPV, kk > 0);
                 mma_commit(bar(cs.o_full));
-                mma_commit(bar(cs.p_free));
-                mma_commit(bar(cs.empty[st]));
             }
             // All MMAs must be finished before TMEM is released.
             mma_commit(bar(cs.mma_done));
@@ -278,77 +345,134 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         float colf[32];  // lambda^(31-c)
 #pragma unroll
         for (int c = 0; c < 32; ++c) colf[c] = cs.pw[31 - c];
+        // p_jl = S_jl lambda^(j-l) for l <= j, l < Lc; 0 otherwise.  Off the
+        // diagonal block lambda^(j-l) = lambda^(j-(32cb+31)) lambda^(31-c),
+        // both exponents >= 0.
+        auto masked = [&](const float (&sv)[32], int cb, int Lc, float (&p)[32]) {
+            if (cb < warp) {
+                const float rowf = cs.pw[j - cb * 32 - 31];
+#pragma unroll
+                for (int c = 0; c < 32; ++c) p[c] = sv[c] * (rowf * colf[c]);
+            } else {
+#pragma unroll
+                for (int c = 0; c < 32; ++c)
+                    p[c] = (c <= lane) ? sv[c] * cs.pw[max(lane - c, 0)] : 0.f;
+            }
+            if (Lc < BC) {
+#pragma unroll
+                for (int c = 0; c < 32; ++c)
+                    if (cb * 32 + c >= Lc) p[c] = 0.f;
+            }
+        };
         for (int i = 0; i < nch; ++i) {
-            const int sbuf = i & 1;
-            const uint32_t sph = (i >> 1) & 1, ph = i & 1;
+            const int st = i & 1;
+            const uint32_t sph = (i >> 1) & 1;
             const int Lc = min(BC, L - i * BC);
-            const uint32_t colS = sbuf ? kColS1 : kColS0;
-            if (!mbar_wait(bar(cs.s_full[sbuf]), sph, abort_flag, kTimeoutNs)) break;
+            const uint32_t colS = st * 128;
+            if (!warp_wait(bar(cs.s_full[st]), sph, abort_flag)) break;
             tc_fence_after();
-            if (!mbar_wait(bar(cs.p_free), ph ^ 1, abort_flag, kTimeoutNs)) break;
-            for (int cb = 0; cb <= warp; ++cb) {  // column blocks on/below the diagonal
-                float sv[32];
+            // pass 1: row max of |p|
+            float mx = 0.f;
+            for (int cb = 0; cb <= warp; ++cb) {
+                float sv[32], p[32];
                 tmem_ld32(tmem + lane_off + colS + cb * 32, sv);
                 tmem_wait_ld();
-                float p[32];
-                if (cb < warp) {
-                    // lambda^(j-l) = lambda^(j-(32cb+31)) * lambda^(31-c), both exponents >= 0
-                    const float rowf = cs.pw[j - cb * 32 - 31];
+                masked(sv, cb, Lc, p);
 #pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                        p[c] = (cb * 32 + c < Lc) ? sv[c] * (rowf * colf[c]) : 0.f;
+                for (int c = 0; c < 32; ++c) mx = fmaxf(mx, fabsf(p[c]));
+            }
+            const int e = fp16_scale_exp(mx);
+            const float inv = exp2i(-e);
+            // pass 2: P = fp16(p 2^-e) into TMEM columns [16 cb, 16 cb + 16)
+            for (int cb = 0; cb < 4; ++cb) {
+                uint32_t pk[16];
+                if (cb <= warp) {
+                    float sv[32], p[32];
+                    tmem_ld32(tmem + lane_off + colS + cb * 32, sv);
+                    tmem_wait_ld();
+                    masked(sv, cb, Lc, p);
+#pragma unroll
+                    for (int m = 0; m < 16; ++m) pk[m] = pack_f16(p[2 * m] * inv, p[2 * m + 1] * inv);
                 } else {
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        const float m = cs.pw[max(lane - c, 0)];
-                        p[c] = (c <= lane && cb * 32 + c < Lc) ? sv[c] * m : 0.f;
-                    }
+                    for (int m = 0; m < 16; ++m) pk[m] = 0u;
                 }
-                const uint32_t row = sb + kOffP + (cb >> 1) * kHalf + j * 128;
-#pragma unroll
-                for (int c16 = 0; c16 < 4; ++c16) {
-                    const uint32_t phys = (uint32_t)(((cb & 1) * 4 + c16) ^ (j & 7));
-                    st_shared_v4(row + phys * 16, pack_bf16(p[8 * c16 + 0], p[8 * c16 + 1]),
-                                 pack_bf16(p[8 * c16 + 2], p[8 * c16 + 3]),
-                                 pack_bf16(p[8 * c16 + 4], p[8 * c16 + 5]),
-                                 pack_bf16(p[8 * c16 + 6], p[8 * c16 + 7]));
-                }
+                tmem_st16(tmem + lane_off + colS + cb * 16, pk);
             }
+            cs.rowscale[st][j] = exp2i(e);
+            tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bar(cs.s_free[sbuf]));
-            fence_proxy_async_smem();
-            mbar_arrive(bar(cs.p_full));
+            mbar_arrive(bar(cs.p_full[st]));
         }
     } else {
         // ================= state warpgroup =================
-        const int r = (warp - kStateWarp0) * 32 + lane;  // TMEM lane: d_k row / token row
-        const uint32_t lane_off = (uint32_t)((warp - kStateWarp0) * 32) << 16;
+        const int w4 = warp - kStateWarp0;
+        const int r = w4 * 32 + lane;  // TMEM lane: d_k row / token row
+        const uint32_t lane_off = (uint32_t)(w4 * 32) << 16;
         const uint32_t vha = sb + kOffVhat, kvb = sb + kOffKVb;
         float kv[DV];
 #pragma unroll
         for (int c = 0; c < DV; ++c) kv[c] = 0.f;
+        float vscale0 = 1.f, vscale1 = 1.f;  // 2^f of the chunks with even / odd index
         // KV_{-1} = 0
 #pragma unroll
-        for (int c = 0; c < 8; ++c) st_shared_v4(kvb + r * 128 + c * 16, 0u, 0u, 0u, 0u);
+        for (int c = 0; c < 8; ++c) {
+            st_shared_v4(kvb + r * 128 + c * 16, 0u, 0u, 0u, 0u);
+            st_shared_v4(kvb + kHalf + r * 128 + c * 16, 0u, 0u, 0u, 0u);
+        }
         fence_proxy_async_smem();
         mbar_arrive(bar(cs.kv_full));
 
-        // Vhat_i = Lambda_K V_i: row r (token r) scaled by lambda^(Lc-1-r).
+        // Chunk i's V tile (row r = token r): Vhat = Lambda_K V as a hi/lo
+        // bf16 pair, and V itself converted in place to fp16 with the chunk's
+        // power-of-two scale.  Rows past the chunk end are zero in both.
         auto make_vhat = [&](int i) -> bool {
             const int st = i & 1;
-            if (!mbar_wait(bar(cs.full[st]), (i >> 1) & 1, abort_flag, kTimeoutNs)) return false;
+            if (!warp_wait(bar(cs.full_v[st]), (i >> 1) & 1, abort_flag)) return false;
             const int Lc = min(BC, L - i * BC);
-            const float g = (r < Lc) ? cs.pw[Lc - 1 - r] : 0.f;
-            const uint32_t src = sb + st * kStageBytes + kQBytes + kKBytes + r * 128;
-            const uint32_t dst = vha + r * 128;
+            const bool live = r < Lc;
+            const float g = live ? cs.pw[Lc - 1 - r] : 0.f;
+            const uint32_t row = vslot(st) + r * 128;
+            uint4 x[8];
+            float m = 0.f;
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
-                const uint32_t ch = (uint32_t)((c + r) & 7) * 16;  // rotate: no bank conflicts
-                const uint4 x = ld_shared_v4(src + ch);
-                float2 a = unpack_bf16(x.x), b = unpack_bf16(x.y), e = unpack_bf16(x.z),
-                       f = unpack_bf16(x.w);
-                st_shared_v4(dst + ch, pack_bf16(a.x * g, a.y * g), pack_bf16(b.x * g, b.y * g),
-                             pack_bf16(e.x * g, e.y * g), pack_bf16(f.x * g, f.y * g));
+                x[c] = ld_shared_v4(row + (uint32_t)((c + r) & 7) * 16);  // rotated: no conflicts
+                const uint32_t w[4] = {x[c].x, x[c].y, x[c].z, x[c].w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float2 f = unpack_bf16(w[q]);
+                    m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
+                }
+            }
+            if (!live) m = 0.f;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            if (lane == 0) cs.vmax[i & 1][w4] = m;
+            mbar_arrive(bar(cs.vmax_ready[i & 1]));
+            if (!warp_wait(bar(cs.vmax_ready[i & 1]), (i >> 1) & 1, abort_flag)) return false;
+            const float mt = fmaxf(fmaxf(cs.vmax[i & 1][0], cs.vmax[i & 1][1]),
+                                   fmaxf(cs.vmax[i & 1][2], cs.vmax[i & 1][3]));
+            const int f = fp16_scale_exp(mt);
+            const float inv = live ? exp2i(-f) : 0.f;
+            if (i & 1)
+                vscale1 = exp2i(f);
+            else
+                vscale0 = exp2i(f);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const uint32_t ch = (uint32_t)((c + r) & 7) * 16;
+                const uint32_t w[4] = {x[c].x, x[c].y, x[c].z, x[c].w};
+                uint32_t hi[4], lo[4], hv[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float2 f2 = unpack_bf16(w[q]);
+                    split_bf16(f2.x * g, f2.y * g, hi[q], lo[q]);
+                    hv[q] = pack_f16(f2.x * inv, f2.y * inv);
+                }
+                st_shared_v4(vha + r * 128 + ch, hi[0], hi[1], hi[2], hi[3]);
+                st_shared_v4(vha + kHalf + r * 128 + ch, lo[0], lo[1], lo[2], lo[3]);
+                st_shared_v4(row + ch, hv[0], hv[1], hv[2], hv[3]);
             }
             fence_proxy_async_smem();
             mbar_arrive(bar(cs.vhat_full));
@@ -357,62 +481,76 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
 
         bool ok = nch > 0 ? make_vhat(0) : true;
         for (int i = 0; ok && i < nch; ++i) {
-            const uint32_t ph = i & 1;
+            const int st = i & 1;
+            const uint32_t sph = (i >> 1) & 1, ph = i & 1;
             const int Lc = min(BC, L - i * BC);
-            // ---- KV_i = lambda^{Lc} KV_{i-1} + dKV_i ----
-            if (!mbar_wait(bar(cs.dkv_full), ph, abort_flag, kTimeoutNs)) break;
+            // ---- KV_i = lambda^{Lc} KV_{i-1} + dKV_hi + dKV_lo ----
+            if (!warp_wait(bar(cs.dkv_full), ph, abort_flag)) break;
             tc_fence_after();
             const float dec = cs.pw[Lc];
 #pragma unroll
-            for (int hlf = 0; hlf < 2; ++hlf) {
-                float d32[32];
-                tmem_ld32(tmem + lane_off + kColDKV + hlf * 32, d32);
+            for (int q = 0; q < 4; ++q) {
+                float a[16], b[16];
+                tmem_ld16(tmem + lane_off + kColDKV + q * 16, a);
+                tmem_ld16(tmem + lane_off + kColDKV + 64 + q * 16, b);
                 tmem_wait_ld();
 #pragma unroll
-                for (int c = 0; c < 32; ++c) kv[hlf * 32 + c] = fmaf(dec, kv[hlf * 32 + c], d32[c]);
+                for (int c = 0; c < 16; ++c)
+                    kv[q * 16 + c] = fmaf(dec, kv[q * 16 + c], a[c] + b[c]);
             }
             tc_fence_before();
             mbar_arrive(bar(cs.dkv_free));
-            // ---- bf16 copy of KV_i for the next chunk's Q KV (after O2_i read KV_{i-1}) ----
-            if (!mbar_wait(bar(cs.kv_free), ph, abort_flag, kTimeoutNs)) break;
+            // ---- hi/lo copy of KV_i for the next chunk's Q KV (after O2_i read KV_{i-1}) ----
+            if (!warp_wait(bar(cs.kv_free), ph, abort_flag)) break;
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
                 const uint32_t phys = (uint32_t)(c ^ (r & 7));
-                st_shared_v4(kvb + r * 128 + phys * 16, pack_bf16(kv[8 * c + 0], kv[8 * c + 1]),
-                             pack_bf16(kv[8 * c + 2], kv[8 * c + 3]),
-                             pack_bf16(kv[8 * c + 4], kv[8 * c + 5]),
-                             pack_bf16(kv[8 * c + 6], kv[8 * c + 7]));
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    split_bf16(kv[8 * c + 2 * q], kv[8 * c + 2 * q + 1], hi[q], lo[q]);
+                st_shared_v4(kvb + r * 128 + phys * 16, hi[0], hi[1], hi[2], hi[3]);
+                st_shared_v4(kvb + kHalf + r * 128 + phys * 16, lo[0], lo[1], lo[2], lo[3]);
             }
             fence_proxy_async_smem();
             mbar_arrive(bar(cs.kv_full));
             // ---- next chunk's Vhat, so its dKV MMA can start early ----
-            if (i + 1 < nch && !make_vhat(i + 1)) break;
-            // ---- output: o_j = O1_j + lambda^(j+1) O2_j ----
-            if (!mbar_wait(bar(cs.o_full), ph, abort_flag, kTimeoutNs)) break;
+            if (i + 1 < nch && !(ok = make_vhat(i + 1))) break;
+            // ---- output: o_j = 2^(e_j + f) O1_j + lambda^(j+1) (O2hi_j + O2lo_j) ----
+            if (!warp_wait(bar(cs.o_full), ph, abort_flag)) break;
+            if (!warp_wait(bar(cs.p_full[st]), sph, abort_flag)) break;  // orders rowscale
             tc_fence_after();
+            const float s1 = cs.rowscale[st][r] * ((i & 1) ? vscale1 : vscale0);
             const float qf = cs.pw[r + 1];
+            const bool full = Lc == BC;
+            const uint32_t stage = vslot(st) + r * 128;
             __nv_bfloat16 *orow = out + ((long)(t0 + i * BC + r) * H + h) * D + vs * DV;
 #pragma unroll
-            for (int hlf = 0; hlf < 2; ++hlf) {
-                float a[32], b[32];
-                tmem_ld32(tmem + lane_off + kColO1 + hlf * 32, a);
-                tmem_ld32(tmem + lane_off + kColO2 + hlf * 32, b);
+            for (int q = 0; q < 4; ++q) {
+                float a[16], b[16], c2[16];
+                tmem_ld16(tmem + lane_off + st * 128 + 64 + q * 16, a);
+                tmem_ld16(tmem + lane_off + kColO2 + q * 16, b);
+                tmem_ld16(tmem + lane_off + kColO2 + 64 + q * 16, c2);
                 tmem_wait_ld();
-                if (r < Lc) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + hlf * 32);
+                uint32_t w[8];
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        uint4 w;
-                        w.x = pack_bf16(fmaf(qf, b[8 * c + 0], a[8 * c + 0]), fmaf(qf, b[8 * c + 1], a[8 * c + 1]));
-                        w.y = pack_bf16(fmaf(qf, b[8 * c + 2], a[8 * c + 2]), fmaf(qf, b[8 * c + 3], a[8 * c + 3]));
-                        w.z = pack_bf16(fmaf(qf, b[8 * c + 4], a[8 * c + 4]), fmaf(qf, b[8 * c + 5], a[8 * c + 5]));
-                        w.w = pack_bf16(fmaf(qf, b[8 * c + 6], a[8 * c + 6]), fmaf(qf, b[8 * c + 7], a[8 * c + 7]));
-                        dst[c] = w;
-                    }
+                for (int m = 0; m < 8; ++m)
+                    w[m] = pack_bf16(fmaf(qf, b[2 * m] + c2[2 * m], s1 * a[2 * m]),
+                                     fmaf(qf, b[2 * m + 1] + c2[2 * m + 1], s1 * a[2 * m + 1]));
+                if (full) {
+                    st_shared_v4(stage + (uint32_t)((2 * q) ^ (r & 7)) * 16, w[0], w[1], w[2], w[3]);
+                    st_shared_v4(stage + (uint32_t)((2 * q + 1) ^ (r & 7)) * 16, w[4], w[5], w[6], w[7]);
+                } else if (r < Lc) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + q * 16);
+                    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
                 }
             }
             tc_fence_before();
-            mbar_arrive(bar(cs.o_free));
+            mbar_arrive(bar(cs.o2_free));
+            mbar_arrive(bar(cs.s_free[st]));
+            if (full) fence_proxy_async_smem();
+            mbar_arrive(bar(cs.out_staged[st]));
         }
         if (final_state && !*abort_flag) {
             float4 *dst = reinterpret_cast<float4 *>(final_state + (((long)s * H + h) * D + r) * D +
@@ -487,10 +625,11 @@ __global__ void wait_timeout_selftest_kernel(uint64_t timeout_ns) {
 
 cudaError_t prefill_tc_bf16(const PrefillArgs &a) {
     if (a.head_dim != D || (a.chunk != 0 && a.chunk != BC)) return cudaErrorNotSupported;
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo;
     if (!make_map(&mq, a.q, a.total_tokens, a.num_heads) ||
         !make_map(&mk, a.k, a.total_tokens, a.num_heads) ||
-        !make_map(&mv, a.v, a.total_tokens, a.num_heads))
+        !make_map(&mv, a.v, a.total_tokens, a.num_heads) ||
+        !make_map(&mo, a.out, a.total_tokens, a.num_heads))
         return cudaErrorInvalidValue;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -506,7 +645,7 @@ cudaError_t prefill_tc_bf16(const PrefillArgs &a) {
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffffL) return cudaErrorInvalidConfiguration;
     prefill_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, a.stream>>>(
-        mq, mk, mv, a.decay, a.cu_seqlens, a.nseq, a.total_tokens, a.num_heads,
+        mq, mk, mv, mo, a.decay, a.cu_seqlens, a.nseq, a.total_tokens, a.num_heads,
         static_cast<__nv_bfloat16 *>(a.out), a.final_state);
     return cudaGetLastError();
 }

@@ -2,8 +2,9 @@
 
 Every case calls the CUDA library through its C ABI (the Python binding only
 marshals pointers) and compares element by element with the oracle on the
-same seeded inputs: max|err| <= 2e-2 * RMS(ref) for bf16, 1e-4 * RMS(ref)
-for fp32 (outputs and final states separately).
+same seeded inputs: |err| <= 2e-2 * RMS(ref) (+ the bf16 storage rounding
+2^-8 |ref| of each output element) for bf16 inputs, 1e-4 * RMS(ref) for fp32
+(outputs and final states separately); see parity.py.
 """
 import numpy as np
 import pytest
@@ -13,7 +14,8 @@ import oracle
 import lightning_attention_attn_gb300 as la
 from lightning_attention_attn_gb300 import build as labuild
 from lightning_attention_attn_gb300 import workloads as wl
-from parity import TOL_BF16, TOL_FP32, assert_close, rel_err, to64
+from parity import (TOL_BF16, TOL_FP32, U_BF16, assert_close, excess_err, rel_err,
+                    storage_u, to64)
 
 pytestmark = pytest.mark.gpu
 
@@ -37,12 +39,13 @@ def run_case(lengths, H, d, dtype, chunk=0, decay=None, seed=0, heads=None):
 
 
 def check(out, st, ref, ref_st, tol, heads=None, what=""):
+    u_out, u_st = storage_u(out), storage_u(st)
     o, s = to64(out), to64(st)
     if heads is not None:
         o, ref = o[:, heads], ref[:, heads]
         s, ref_st = s[:, heads], ref_st[:, heads]
-    e1 = assert_close(o, ref, tol, f"{what} out")
-    e2 = assert_close(s, ref_st, tol, f"{what} final state")
+    e1 = assert_close(o, ref, tol, f"{what} out", u=u_out)
+    e2 = assert_close(s, ref_st, tol, f"{what} final state", u=u_st)
     return e1, e2
 
 
@@ -180,10 +183,12 @@ def test_prefill_8k_layer_full_parity():
     inp, out, st, ref, ref_st = run_case(cfg["lengths"], cfg["num_heads"], cfg["head_dim"],
                                          cfg["dtype"], chunk=0, seed=0)
     e1, e2 = check(out, st, ref, ref_st, TOL_BF16, what="8k")
-    # per-head diagnostic: fast-decay heads have a much smaller RMS
+    # per-head diagnostic: fast-decay heads have a much smaller RMS, so the
+    # whole-tensor normaliser is lenient for them; hold each head to its own
     o, r = to64(out), ref
-    worst = max(rel_err(o[:, h], r[:, h]) for h in range(64))
-    assert worst <= 5 * TOL_BF16, worst
+    worst = max(excess_err(o[:, h], r[:, h], U_BF16) for h in range(64))
+    print(f"[parity] 8k worst per-head arithmetic error {worst:.3e}")
+    assert worst <= TOL_BF16, worst
 
 
 @pytest.mark.slow

@@ -40,7 +40,7 @@
 // Warp roles (320 threads):
 //   warps 0-3  mask warpgroup: S -> P = fp16(2^-e_j S (.) M) into TMEM
 //   warps 4-7  state warpgroup: Vhat / fp16 V, KV update, KV copy, output
-//   warp  8    TMA producer: Q, K, V two-slot rings; output TMA stores
+//   warp  8    TMA producer: Q, K, V two-slot rings
 //   warp  9    MMA issuer (one thread)
 // Every wait is bounded and warp-uniform: a wait that gives up sets a CTA-wide
 // abort flag, all roles leave their loops, in-flight TMA copies and MMAs are
@@ -81,13 +81,13 @@ constexpr uint32_t kHalf = BC * 128;            // 128 rows x 128 B = 16 KB
 constexpr uint32_t kOffQ = 0;                   // 2 slots x (two 64-col halves)
 constexpr uint32_t kOffK = kOffQ + 4 * kHalf;   // 2 slots x (two halves)
 constexpr uint32_t kOffV = kOffK + 4 * kHalf;   // 2 slots x 64 cols; fp16 after
-                                                // conversion; then output staging
+                                                // conversion
 constexpr uint32_t kOffVhat = kOffV + 2 * kHalf;   // hi, lo: 128 tokens x 64
 constexpr uint32_t kOffKVb = kOffVhat + 2 * kHalf; // hi, lo: 128 d_k x 64
 constexpr uint32_t kOffCtrl = kOffKVb + 2 * kHalf;
 
 struct Ctrl {
-    uint64_t full_q[2], full_k[2], full_v[2], empty_q[2], empty_k[2], out_staged[2];
+    uint64_t full_q[2], full_k[2], full_v[2], empty_q[2], empty_k[2], empty_v[2];
     uint64_t s_full[2], s_free[2], p_full[2], vmax_ready[2];
     uint64_t o_full, o2_free, dkv_full, dkv_free, vhat_full, kv_full, kv_free, mma_done;
     uint32_t tmem_base;
@@ -141,14 +141,21 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
                  : "memory");
     return v;
 }
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
 // Exact power-of-two scale exponent: for m > 0 finite, returns e with
-// m * 2^-e in [2^14, 2^15) (the top of the fp16 range), clamped to
-// [-126, 126] so that both 2^e and 2^-e are normal floats; 0 for m == 0 or
-// a non-finite m.
-__device__ __forceinline__ int fp16_scale_exp(float m) {
+// m * 2^-e in [2^top, 2^(top+1)), clamped to [-126, 126] so that both 2^e and
+// 2^-e are normal floats; 0 for m == 0 or a non-finite m.
+__device__ __forceinline__ int fp16_scale_exp(float m, int top) {
     if (!(m > 0.f) || m > 3.0e38f) return 0;
     const int eb = (int)((__float_as_uint(m) >> 23) & 0xff);
-    const int e = (eb == 0 ? -126 : eb - 127) - 14;
+    const int e = (eb == 0 ? -126 : eb - 127) - top;
     return max(-126, min(126, e));
 }
 __device__ __forceinline__ float exp2i(int e) {  // 2^e for -126 <= e <= 127
@@ -185,6 +192,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     const float lam = __ldg(decay + h);
 
     auto bar = [&](const uint64_t &b) { return smem_u32(&b); };
+    const uint32_t pw_s = smem_u32(&cs.pw[0]);          // lambda^e at pw_s + 4 e
+    const uint32_t rowscale_s = smem_u32(&cs.rowscale[0][0]);
+    const uint32_t vmax_s = smem_u32(&cs.vmax[0][0]);
+    auto pw = [&](int e) { return ld_shared_f32(pw_s + 4u * (uint32_t)e); };
     auto qslot = [&](int st) { return sb + kOffQ + st * 2 * kHalf; };
     auto kslot = [&](int st) { return sb + kOffK + st * 2 * kHalf; };
     auto vslot = [&](int st) { return sb + kOffV + st * kHalf; };
@@ -197,7 +208,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             mbar_init(bar(cs.full_v[i]), 1);
             mbar_init(bar(cs.empty_q[i]), 1);
             mbar_init(bar(cs.empty_k[i]), 1);
-            mbar_init(bar(cs.out_staged[i]), 128);
+            mbar_init(bar(cs.empty_v[i]), 1);
             mbar_init(bar(cs.s_full[i]), 1);
             mbar_init(bar(cs.s_free[i]), 128);
             mbar_init(bar(cs.p_full[i]), 128);
@@ -232,20 +243,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
             tma_prefetch_desc(&tmO);
-            // Output tile of chunk c, staged by the state warpgroup in V slot
-            // c & 1, goes out with one TMA store; the slot is reusable once
-            // the store has read it.  Short (last) chunks are written by the
-            // state warpgroup directly, row by row.
-            auto store_out = [&](int c) -> bool {
-                if (!mbar_wait(bar(cs.out_staged[c & 1]), (c >> 1) & 1, abort_flag, kTimeoutNs))
-                    return false;
-                if (L - c * BC >= BC) {
-                    tma_store_2d(&tmO, vslot(c & 1), h * D + vs * DV, t0 + c * BC);
-                    bulk_commit_group();
-                    bulk_wait_read_all();
-                }
-                return true;
-            };
             int nq = 0, nk = 0, nv = 0;
             bool ok = true;
             for (int i = 0; i < nch && ok; ++i) {
@@ -262,13 +259,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
                 tma_load_2d(kslot(st), &tmK, bar(cs.full_k[st]), h * D, y);
                 tma_load_2d(kslot(st) + kHalf, &tmK, bar(cs.full_k[st]), h * D + 64, y);
                 ++nk;
-                if (i >= 2 && !(ok = store_out(i - 2))) break;
+                if (!(ok = mbar_wait(bar(cs.empty_v[st]), sph ^ 1, abort_flag, kTimeoutNs))) break;
                 mbar_arrive_expect_tx(bar(cs.full_v[st]), kHalf);
                 tma_load_2d(vslot(st), &tmV, bar(cs.full_v[st]), h * D + vs * DV, y);
                 ++nv;
             }
-            for (int c = max(0, nch - 2); ok && c < nch; ++c) ok = store_out(c);
-            bulk_wait_all();
             // Never leave with a load still landing in shared memory.
             int no_abort = 0;
             for (int c = max(0, nq - 2); c < nq; ++c)
@@ -331,6 +326,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
                     mma_bf16_tmem_a(tmem + colS + 64, tmem + colS + kk * 8,
                                     sdesc_sw128(va + kk * 2048, kHalf, 1024), kIdescPV, kk > 0);
                 mma_commit(bar(cs.o_full));
+                mma_commit(bar(cs.empty_v[st]));
             }
             // All MMAs must be finished before TMEM is released.
             mma_commit(bar(cs.mma_done));
@@ -340,66 +336,85 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         __syncwarp();
     } else if (warp < kStateWarp0) {
         // ================= mask warpgroup: S -> P =================
-        const int j = warp * 32 + lane;  // token row within the chunk
+        // Thread j owns row j of the chunk (TMEM lane j).  p_jl = S_jl
+        // lambda^(j-l) for l <= j, l < Lc, else 0.  P goes to TMEM as fp16
+        // scaled by 2^-e_j, a power of two chosen from an upper bound of the
+        // row's |p| (pass 1: max |S| of each column block times the block's
+        // largest decay factor) so the row's values sit below 2^12: no
+        // overflow, and 11 significant bits for everything within 2^25 of
+        // the bound.  Pass 2 masks, scales and packs one 32-column block at a
+        // time into TMEM columns [16 cb, 16 cb + 16) of the S buffer: blocks
+        // are visited in increasing cb, so block cb overwrites S columns of
+        // block cb / 2 <= cb, already read.
+        const int j = warp * 32 + lane;
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-        float colf[32];  // lambda^(31-c)
+        float colf[32];  // lambda^(31-c): off the diagonal block,
+#pragma unroll           // lambda^(j-l) = lambda^(j-(32cb+31)) lambda^(31-c)
+        for (int c = 0; c < 32; ++c) colf[c] = pw(31 - c);
+        uint32_t zero[16];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) colf[c] = cs.pw[31 - c];
-        // p_jl = S_jl lambda^(j-l) for l <= j, l < Lc; 0 otherwise.  Off the
-        // diagonal block lambda^(j-l) = lambda^(j-(32cb+31)) lambda^(31-c),
-        // both exponents >= 0.
-        auto masked = [&](const float (&sv)[32], int cb, int Lc, float (&p)[32]) {
-            if (cb < warp) {
-                const float rowf = cs.pw[j - cb * 32 - 31];
-#pragma unroll
-                for (int c = 0; c < 32; ++c) p[c] = sv[c] * (rowf * colf[c]);
-            } else {
-#pragma unroll
-                for (int c = 0; c < 32; ++c)
-                    p[c] = (c <= lane) ? sv[c] * cs.pw[max(lane - c, 0)] : 0.f;
-            }
-            if (Lc < BC) {
-#pragma unroll
-                for (int c = 0; c < 32; ++c)
-                    if (cb * 32 + c >= Lc) p[c] = 0.f;
-            }
-        };
+        for (int m = 0; m < 16; ++m) zero[m] = 0u;
         for (int i = 0; i < nch; ++i) {
             const int st = i & 1;
             const uint32_t sph = (i >> 1) & 1;
             const int Lc = min(BC, L - i * BC);
-            const uint32_t colS = st * 128;
+            const uint32_t scol = tmem + lane_off + st * 128;
             if (!warp_wait(bar(cs.s_full[st]), sph, abort_flag)) break;
             tc_fence_after();
-            // pass 1: row max of |p|
-            float mx = 0.f;
+            // pass 1: bound of max |p| over the row
+            float bound = 0.f;
+#pragma unroll 1
             for (int cb = 0; cb <= warp; ++cb) {
-                float sv[32], p[32];
-                tmem_ld32(tmem + lane_off + colS + cb * 32, sv);
+                float sv[32];
+                tmem_ld32(scol + cb * 32, sv);
                 tmem_wait_ld();
-                masked(sv, cb, Lc, p);
+                const int lim = min(cb == warp ? lane : 31, Lc - 1 - cb * 32);  // last valid c
+                float m = 0.f;
 #pragma unroll
-                for (int c = 0; c < 32; ++c) mx = fmaxf(mx, fabsf(p[c]));
+                for (int c = 0; c < 32; ++c)
+                    if (c <= lim) m = fmaxf(m, fabsf(sv[c]));
+                bound = fmaxf(bound, cb == warp ? m : m * pw(j - cb * 32 - 31));
             }
-            const int e = fp16_scale_exp(mx);
+            const int e = fp16_scale_exp(bound, 11);
             const float inv = exp2i(-e);
-            // pass 2: P = fp16(p 2^-e) into TMEM columns [16 cb, 16 cb + 16)
-            for (int cb = 0; cb < 4; ++cb) {
+            // pass 2: the blocks below the diagonal in increasing order, then
+            // the diagonal block (P block cb lands in S block cb / 2 <= cb,
+            // which has been read by then)
+#pragma unroll 1
+            for (int cb = 0; cb < warp; ++cb) {
+                float sv[32];
+                tmem_ld32(scol + cb * 32, sv);
+                tmem_wait_ld();
+                const float rowf = pw(j - cb * 32 - 31) * inv;
+                const int lim = Lc - 1 - cb * 32;
                 uint32_t pk[16];
-                if (cb <= warp) {
-                    float sv[32], p[32];
-                    tmem_ld32(tmem + lane_off + colS + cb * 32, sv);
-                    tmem_wait_ld();
-                    masked(sv, cb, Lc, p);
 #pragma unroll
-                    for (int m = 0; m < 16; ++m) pk[m] = pack_f16(p[2 * m] * inv, p[2 * m + 1] * inv);
-                } else {
-#pragma unroll
-                    for (int m = 0; m < 16; ++m) pk[m] = 0u;
+                for (int m = 0; m < 16; ++m) {
+                    const int c = 2 * m;
+                    const float a = (c <= lim) ? sv[c] * (rowf * colf[c]) : 0.f;
+                    const float b = (c + 1 <= lim) ? sv[c + 1] * (rowf * colf[c + 1]) : 0.f;
+                    pk[m] = pack_f16(a, b);
                 }
-                tmem_st16(tmem + lane_off + colS + cb * 16, pk);
+                tmem_st16(scol + cb * 16, pk);
             }
-            cs.rowscale[st][j] = exp2i(e);
+            {
+                float sv[32];
+                tmem_ld32(scol + warp * 32, sv);
+                tmem_wait_ld();
+                const int lim = min(lane, Lc - 1 - warp * 32);
+                uint32_t pk[16];
+#pragma unroll
+                for (int m = 0; m < 16; ++m) {
+                    const int c = 2 * m;
+                    const float a = (c <= lim) ? sv[c] * (pw(max(lane - c, 0)) * inv) : 0.f;
+                    const float b = (c + 1 <= lim) ? sv[c + 1] * (pw(max(lane - c - 1, 0)) * inv) : 0.f;
+                    pk[m] = pack_f16(a, b);
+                }
+                tmem_st16(scol + warp * 16, pk);
+            }
+#pragma unroll 1
+            for (int cb = warp + 1; cb < 4; ++cb) tmem_st16(scol + cb * 16, zero);
+            st_shared_f32(rowscale_s + 4u * (uint32_t)(st * BC + j), exp2i(e));
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(bar(cs.p_full[st]));
@@ -423,56 +438,89 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         fence_proxy_async_smem();
         mbar_arrive(bar(cs.kv_full));
 
-        // Chunk i's V tile (row r = token r): Vhat = Lambda_K V as a hi/lo
-        // bf16 pair, and V itself converted in place to fp16 with the chunk's
-        // power-of-two scale.  Rows past the chunk end are zero in both.
+        // V-tile rows (tokens) handled by this thread.  The mask work of TMEM
+        // lane quadrant q grows with q (its rows have q + 1 column blocks)
+        // and runs on the same SM sub-partition as state warp q, so the
+        // V-tile rows are dealt out unevenly: 48, 40, 24 and 16 rows to
+        // state warps 0..3 (rows [0,48), [48,88), [88,112), [112,128)).
+        const int vbase = w4 == 0 ? 0 : (w4 == 1 ? 48 : (w4 == 2 ? 88 : 112));
+        const int vcount = w4 == 0 ? 48 : (w4 == 1 ? 40 : (w4 == 2 ? 24 : 16));
+        const int nvrows = (lane < vcount - 32) ? 2 : (lane < vcount ? 1 : 0);
+        const int vrow0 = vbase + lane;
+        // Chunk i's V tile: Vhat = Lambda_K V as a hi/lo bf16 pair, and V
+        // itself converted in place to fp16 with the chunk's power-of-two
+        // scale.  Rows past the chunk end are zero in both.
         auto make_vhat = [&](int i) -> bool {
             const int st = i & 1;
             if (!warp_wait(bar(cs.full_v[st]), (i >> 1) & 1, abort_flag)) return false;
             const int Lc = min(BC, L - i * BC);
-            const bool live = r < Lc;
-            const float g = live ? cs.pw[Lc - 1 - r] : 0.f;
-            const uint32_t row = vslot(st) + r * 128;
-            uint4 x[8];
-            float m = 0.f;
+            uint32_t mbits = 0;  // max |v| as packed bf16 magnitudes
+            for (int k = 0; k < nvrows; ++k) {
+                const int vr = vrow0 + 32 * k;
+                if (vr >= Lc) continue;
+                const uint32_t row = vslot(st) + vr * 128;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                x[c] = ld_shared_v4(row + (uint32_t)((c + r) & 7) * 16);  // rotated: no conflicts
-                const uint32_t w[4] = {x[c].x, x[c].y, x[c].z, x[c].w};
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float2 f = unpack_bf16(w[q]);
-                    m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 x = ld_shared_v4(row + (uint32_t)((c + vr) & 7) * 16);  // rotated
+                    mbits = __vmaxu2(mbits, x.x & 0x7fff7fffu);
+                    mbits = __vmaxu2(mbits, x.y & 0x7fff7fffu);
+                    mbits = __vmaxu2(mbits, x.z & 0x7fff7fffu);
+                    mbits = __vmaxu2(mbits, x.w & 0x7fff7fffu);
                 }
             }
-            if (!live) m = 0.f;
+            float m = fmaxf(__uint_as_float(mbits << 16), __uint_as_float(mbits & 0xffff0000u));
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-            if (lane == 0) cs.vmax[i & 1][w4] = m;
+            if (lane == 0) st_shared_f32(vmax_s + 4u * (uint32_t)((i & 1) * 4 + w4), m);
             mbar_arrive(bar(cs.vmax_ready[i & 1]));
             if (!warp_wait(bar(cs.vmax_ready[i & 1]), (i >> 1) & 1, abort_flag)) return false;
-            const float mt = fmaxf(fmaxf(cs.vmax[i & 1][0], cs.vmax[i & 1][1]),
-                                   fmaxf(cs.vmax[i & 1][2], cs.vmax[i & 1][3]));
-            const int f = fp16_scale_exp(mt);
-            const float inv = live ? exp2i(-f) : 0.f;
+            const uint32_t vm = vmax_s + 16u * (uint32_t)(i & 1);
+            const float mt = fmaxf(fmaxf(ld_shared_f32(vm), ld_shared_f32(vm + 4)),
+                                   fmaxf(ld_shared_f32(vm + 8), ld_shared_f32(vm + 12)));
+            // fp16 scale: none when the tile is comfortably inside fp16's
+            // normal range, else 2^-f with max |v| 2^-f in [2^14, 2^15).
+            const int f = (mt <= 1024.f && mt >= 0.0625f) ? 0 : fp16_scale_exp(mt, 14);
+            const float inv = exp2i(-f);
             if (i & 1)
                 vscale1 = exp2i(f);
             else
                 vscale0 = exp2i(f);
+            for (int k = 0; k < nvrows; ++k) {
+                const int vr = vrow0 + 32 * k;
+                const uint32_t row = vslot(st) + vr * 128;
+                // lambda^(Lc-1-l) split as g_hi + g_lo (bf16 each) so that the
+                // packed bf16 FMAs below give hi + lo = v g to ~16 bits.
+                const float g = vr < Lc ? pw(Lc - 1 - vr) : 0.f;
+                const __nv_bfloat16 ghb = __float2bfloat16_rn(g);
+                const __nv_bfloat16 glb = __float2bfloat16_rn(g - __bfloat162float(ghb));
+                const __nv_bfloat162 gh = __halves2bfloat162(ghb, ghb);
+                const __nv_bfloat162 gl = __halves2bfloat162(glb, glb);
+                const float sc = vr < Lc ? inv : 0.f;
+                const bool unscaled = f == 0 && vr < Lc;
+#pragma unroll 2
+                for (int c = 0; c < 8; ++c) {
+                    const uint32_t ch = (uint32_t)((c + vr) & 7) * 16;
+                    const uint4 x = ld_shared_v4(row + ch);
+                    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+                    uint32_t hi[4], lo[4], hv[4];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const uint32_t ch = (uint32_t)((c + r) & 7) * 16;
-                const uint32_t w[4] = {x[c].x, x[c].y, x[c].z, x[c].w};
-                uint32_t hi[4], lo[4], hv[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float2 f2 = unpack_bf16(w[q]);
-                    split_bf16(f2.x * g, f2.y * g, hi[q], lo[q]);
-                    hv[q] = pack_f16(f2.x * inv, f2.y * inv);
+                    for (int q = 0; q < 4; ++q) {
+                        const __nv_bfloat162 v2 = *reinterpret_cast<const __nv_bfloat162 *>(&w[q]);
+                        const __nv_bfloat162 h2 = __hmul2(v2, gh);
+                        // exact residual of the rounded product, plus the g_lo term
+                        __nv_bfloat162 l2 = __hfma2(v2, gh, __hneg2(h2));
+                        l2 = __hfma2(v2, gl, l2);
+                        hi[q] = *reinterpret_cast<const uint32_t *>(&h2);
+                        lo[q] = *reinterpret_cast<const uint32_t *>(&l2);
+                        hv[q] = unscaled ? pack_f16(__uint_as_float(w[q] << 16),
+                                                    __uint_as_float(w[q] & 0xffff0000u))
+                                         : pack_f16(__uint_as_float(w[q] << 16) * sc,
+                                                    __uint_as_float(w[q] & 0xffff0000u) * sc);
+                    }
+                    st_shared_v4(vha + vr * 128 + ch, hi[0], hi[1], hi[2], hi[3]);
+                    st_shared_v4(vha + kHalf + vr * 128 + ch, lo[0], lo[1], lo[2], lo[3]);
+                    st_shared_v4(row + ch, hv[0], hv[1], hv[2], hv[3]);
                 }
-                st_shared_v4(vha + r * 128 + ch, hi[0], hi[1], hi[2], hi[3]);
-                st_shared_v4(vha + kHalf + r * 128 + ch, lo[0], lo[1], lo[2], lo[3]);
-                st_shared_v4(row + ch, hv[0], hv[1], hv[2], hv[3]);
             }
             fence_proxy_async_smem();
             mbar_arrive(bar(cs.vhat_full));
@@ -487,7 +535,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             // ---- KV_i = lambda^{Lc} KV_{i-1} + dKV_hi + dKV_lo ----
             if (!warp_wait(bar(cs.dkv_full), ph, abort_flag)) break;
             tc_fence_after();
-            const float dec = cs.pw[Lc];
+            const float dec = pw(Lc);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 float a[16], b[16];
@@ -507,8 +555,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
                 const uint32_t phys = (uint32_t)(c ^ (r & 7));
                 uint32_t hi[4], lo[4];
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    split_bf16(kv[8 * c + 2 * q], kv[8 * c + 2 * q + 1], hi[q], lo[q]);
+                for (int q = 0; q < 4; ++q) {
+                    // hi = x with the low 16 bits cleared (a bf16, exact);
+                    // lo = x - hi (exact in fp32), also truncated to bf16:
+                    // hi + lo = x to about 2^-14 relative
+                    const uint32_t ua = __float_as_uint(kv[8 * c + 2 * q]);
+                    const uint32_t ub = __float_as_uint(kv[8 * c + 2 * q + 1]);
+                    hi[q] = __byte_perm(ua, ub, 0x7632);
+                    const float la = __uint_as_float(ua) - __uint_as_float(ua & 0xffff0000u);
+                    const float lb = __uint_as_float(ub) - __uint_as_float(ub & 0xffff0000u);
+                    lo[q] = __byte_perm(__float_as_uint(la), __float_as_uint(lb), 0x7632);
+                }
                 st_shared_v4(kvb + r * 128 + phys * 16, hi[0], hi[1], hi[2], hi[3]);
                 st_shared_v4(kvb + kHalf + r * 128 + phys * 16, lo[0], lo[1], lo[2], lo[3]);
             }
@@ -520,37 +577,33 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             if (!warp_wait(bar(cs.o_full), ph, abort_flag)) break;
             if (!warp_wait(bar(cs.p_full[st]), sph, abort_flag)) break;  // orders rowscale
             tc_fence_after();
-            const float s1 = cs.rowscale[st][r] * ((i & 1) ? vscale1 : vscale0);
-            const float qf = cs.pw[r + 1];
-            const bool full = Lc == BC;
-            const uint32_t stage = vslot(st) + r * 128;
+            const float s1 = ld_shared_f32(rowscale_s + 4u * (uint32_t)(st * BC + r)) *
+                             ((i & 1) ? vscale1 : vscale0);
+            const float qf = pw(r + 1);
             __nv_bfloat16 *orow = out + ((long)(t0 + i * BC + r) * H + h) * D + vs * DV;
-#pragma unroll
+#pragma unroll 1
             for (int q = 0; q < 4; ++q) {
                 float a[16], b[16], c2[16];
                 tmem_ld16(tmem + lane_off + st * 128 + 64 + q * 16, a);
                 tmem_ld16(tmem + lane_off + kColO2 + q * 16, b);
                 tmem_ld16(tmem + lane_off + kColO2 + 64 + q * 16, c2);
                 tmem_wait_ld();
+                if (q == 3) {  // all TMEM reads of this chunk are done
+                    tc_fence_before();
+                    mbar_arrive(bar(cs.o2_free));
+                    mbar_arrive(bar(cs.s_free[st]));
+                }
                 uint32_t w[8];
 #pragma unroll
                 for (int m = 0; m < 8; ++m)
                     w[m] = pack_bf16(fmaf(qf, b[2 * m] + c2[2 * m], s1 * a[2 * m]),
                                      fmaf(qf, b[2 * m + 1] + c2[2 * m + 1], s1 * a[2 * m + 1]));
-                if (full) {
-                    st_shared_v4(stage + (uint32_t)((2 * q) ^ (r & 7)) * 16, w[0], w[1], w[2], w[3]);
-                    st_shared_v4(stage + (uint32_t)((2 * q + 1) ^ (r & 7)) * 16, w[4], w[5], w[6], w[7]);
-                } else if (r < Lc) {
+                if (r < Lc) {
                     uint4 *dst = reinterpret_cast<uint4 *>(orow + q * 16);
                     dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
                     dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
                 }
             }
-            tc_fence_before();
-            mbar_arrive(bar(cs.o2_free));
-            mbar_arrive(bar(cs.s_free[st]));
-            if (full) fence_proxy_async_smem();
-            mbar_arrive(bar(cs.out_staged[st]));
         }
         if (final_state && !*abort_flag) {
             float4 *dst = reinterpret_cast<float4 *>(final_state + (((long)s * H + h) * D + r) * D +

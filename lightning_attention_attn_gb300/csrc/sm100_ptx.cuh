@@ -50,18 +50,35 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// As mbar_try_wait, but a thread whose phase is not complete is suspended
+// (without taking issue slots) until the phase completes or about
+// suspend_ns nanoseconds have passed.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity,
+                                                    uint32_t suspend_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(suspend_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete.  Gives up (returns
 // false) when *abort becomes non-zero or after timeout_ns; on a timeout it
 // sets *abort so the other roles of the CTA stop too.
+// Waiting threads sleep in try_wait (woken when the phase completes), so a
+// waiting warp does not take issue slots from working warps of its SM
+// sub-partition; they wake at least every 0.2 ms to check the deadline.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
                                           uint64_t timeout_ns) {
-#pragma unroll 1
-    for (int it = 0; it < 256; ++it)
-        if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
 #pragma unroll 1
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, 200000u)) return true;
         if (*abort) return false;
         if (globaltimer_ns() - t0 > timeout_ns) {
             *abort = 1;

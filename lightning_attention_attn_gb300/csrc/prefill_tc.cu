@@ -438,15 +438,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         fence_proxy_async_smem();
         mbar_arrive(bar(cs.kv_full));
 
-        // V-tile rows (tokens) handled by this thread.  The mask work of TMEM
-        // lane quadrant q grows with q (its rows have q + 1 column blocks)
-        // and runs on the same SM sub-partition as state warp q, so the
-        // V-tile rows are dealt out unevenly: 48, 40, 24 and 16 rows to
-        // state warps 0..3 (rows [0,48), [48,88), [88,112), [112,128)).
-        const int vbase = w4 == 0 ? 0 : (w4 == 1 ? 48 : (w4 == 2 ? 88 : 112));
-        const int vcount = w4 == 0 ? 48 : (w4 == 1 ? 40 : (w4 == 2 ? 24 : 16));
-        const int nvrows = (lane < vcount - 32) ? 2 : (lane < vcount ? 1 : 0);
-        const int vrow0 = vbase + lane;
+        // V-tile row (token) handled by this thread: one each, so the tile
+        // conversion, which the next dKV MMA waits for, takes one row's time.
+        const int vrow0 = r;
         // Chunk i's V tile: Vhat = Lambda_K V as a hi/lo bf16 pair, and V
         // itself converted in place to fp16 with the chunk's power-of-two
         // scale.  Rows past the chunk end are zero in both.
@@ -454,11 +448,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             const int st = i & 1;
             if (!warp_wait(bar(cs.full_v[st]), (i >> 1) & 1, abort_flag)) return false;
             const int Lc = min(BC, L - i * BC);
+            const int vr = vrow0;
+            const bool live = vr < Lc;
+            const uint32_t row = vslot(st) + vr * 128;
             uint32_t mbits = 0;  // max |v| as packed bf16 magnitudes
-            for (int k = 0; k < nvrows; ++k) {
-                const int vr = vrow0 + 32 * k;
-                if (vr >= Lc) continue;
-                const uint32_t row = vslot(st) + vr * 128;
+            if (live) {
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     const uint4 x = ld_shared_v4(row + (uint32_t)((c + vr) & 7) * 16);  // rotated
@@ -485,42 +479,38 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
                 vscale1 = exp2i(f);
             else
                 vscale0 = exp2i(f);
-            for (int k = 0; k < nvrows; ++k) {
-                const int vr = vrow0 + 32 * k;
-                const uint32_t row = vslot(st) + vr * 128;
-                // lambda^(Lc-1-l) split as g_hi + g_lo (bf16 each) so that the
-                // packed bf16 FMAs below give hi + lo = v g to ~16 bits.
-                const float g = vr < Lc ? pw(Lc - 1 - vr) : 0.f;
-                const __nv_bfloat16 ghb = __float2bfloat16_rn(g);
-                const __nv_bfloat16 glb = __float2bfloat16_rn(g - __bfloat162float(ghb));
-                const __nv_bfloat162 gh = __halves2bfloat162(ghb, ghb);
-                const __nv_bfloat162 gl = __halves2bfloat162(glb, glb);
-                const float sc = vr < Lc ? inv : 0.f;
-                const bool unscaled = f == 0 && vr < Lc;
+            // lambda^(Lc-1-l) split as g_hi + g_lo (bf16 each) so that the
+            // packed bf16 FMAs below give hi + lo = v g to ~16 bits.
+            const float g = live ? pw(Lc - 1 - vr) : 0.f;
+            const __nv_bfloat16 ghb = __float2bfloat16_rn(g);
+            const __nv_bfloat16 glb = __float2bfloat16_rn(g - __bfloat162float(ghb));
+            const __nv_bfloat162 gh = __halves2bfloat162(ghb, ghb);
+            const __nv_bfloat162 gl = __halves2bfloat162(glb, glb);
+            const float sc = live ? inv : 0.f;
+            const bool unscaled = f == 0 && live;
 #pragma unroll 2
-                for (int c = 0; c < 8; ++c) {
-                    const uint32_t ch = (uint32_t)((c + vr) & 7) * 16;
-                    const uint4 x = ld_shared_v4(row + ch);
-                    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-                    uint32_t hi[4], lo[4], hv[4];
+            for (int c = 0; c < 8; ++c) {
+                const uint32_t ch = (uint32_t)((c + vr) & 7) * 16;
+                const uint4 x = ld_shared_v4(row + ch);
+                const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+                uint32_t hi[4], lo[4], hv[4];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const __nv_bfloat162 v2 = *reinterpret_cast<const __nv_bfloat162 *>(&w[q]);
-                        const __nv_bfloat162 h2 = __hmul2(v2, gh);
-                        // exact residual of the rounded product, plus the g_lo term
-                        __nv_bfloat162 l2 = __hfma2(v2, gh, __hneg2(h2));
-                        l2 = __hfma2(v2, gl, l2);
-                        hi[q] = *reinterpret_cast<const uint32_t *>(&h2);
-                        lo[q] = *reinterpret_cast<const uint32_t *>(&l2);
-                        hv[q] = unscaled ? pack_f16(__uint_as_float(w[q] << 16),
-                                                    __uint_as_float(w[q] & 0xffff0000u))
-                                         : pack_f16(__uint_as_float(w[q] << 16) * sc,
-                                                    __uint_as_float(w[q] & 0xffff0000u) * sc);
-                    }
-                    st_shared_v4(vha + vr * 128 + ch, hi[0], hi[1], hi[2], hi[3]);
-                    st_shared_v4(vha + kHalf + vr * 128 + ch, lo[0], lo[1], lo[2], lo[3]);
-                    st_shared_v4(row + ch, hv[0], hv[1], hv[2], hv[3]);
+                for (int q = 0; q < 4; ++q) {
+                    const __nv_bfloat162 v2 = *reinterpret_cast<const __nv_bfloat162 *>(&w[q]);
+                    const __nv_bfloat162 h2 = __hmul2(v2, gh);
+                    // exact residual of the rounded product, plus the g_lo term
+                    __nv_bfloat162 l2 = __hfma2(v2, gh, __hneg2(h2));
+                    l2 = __hfma2(v2, gl, l2);
+                    hi[q] = *reinterpret_cast<const uint32_t *>(&h2);
+                    lo[q] = *reinterpret_cast<const uint32_t *>(&l2);
+                    hv[q] = unscaled ? pack_f16(__uint_as_float(w[q] << 16),
+                                                __uint_as_float(w[q] & 0xffff0000u))
+                                     : pack_f16(__uint_as_float(w[q] << 16) * sc,
+                                                __uint_as_float(w[q] & 0xffff0000u) * sc);
                 }
+                st_shared_v4(vha + vr * 128 + ch, hi[0], hi[1], hi[2], hi[3]);
+                st_shared_v4(vha + kHalf + vr * 128 + ch, lo[0], lo[1], lo[2], lo[3]);
+                st_shared_v4(row + ch, hv[0], hv[1], hv[2], hv[3]);
             }
             fence_proxy_async_smem();
             mbar_arrive(bar(cs.vhat_full));
@@ -548,6 +538,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             }
             tc_fence_before();
             mbar_arrive(bar(cs.dkv_free));
+            // ---- next chunk's Vhat (its buffer is free: dKV_i is done), so
+            // the dKV MMA of chunk i+1 can follow S_{i+1} without a gap ----
+            if (i + 1 < nch && !(ok = make_vhat(i + 1))) break;
             // ---- hi/lo copy of KV_i for the next chunk's Q KV (after O2_i read KV_{i-1}) ----
             if (!warp_wait(bar(cs.kv_free), ph, abort_flag)) break;
 #pragma unroll
@@ -571,8 +564,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             }
             fence_proxy_async_smem();
             mbar_arrive(bar(cs.kv_full));
-            // ---- next chunk's Vhat, so its dKV MMA can start early ----
-            if (i + 1 < nch && !(ok = make_vhat(i + 1))) break;
             // ---- output: o_j = 2^(e_j + f) O1_j + lambda^(j+1) (O2hi_j + O2lo_j) ----
             if (!warp_wait(bar(cs.o_full), ph, abort_flag)) break;
             if (!warp_wait(bar(cs.p_full[st]), sph, abort_flag)) break;  // orders rowscale

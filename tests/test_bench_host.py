@@ -1,0 +1,88 @@
+"""Host-side logic of bench.py that needs no GPU: the multi-rank timing
+aggregation (max over ranks, tokens summed over ranks) on two gloo ranks, the
+algorithmic byte/flop model, and the reference arm's JSON line."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+def _worker(rank, ws, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(ws), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=ws)
+    try:
+        bench.barrier(ws)
+        t = bench.max_over_ranks(10.0 + rank, ws)         # rank 1 is slower
+        tok = bench.sum_over_ranks(8192.0 * 3, ws)        # 3 steps per rank
+        q.put((rank, t, tok))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_aggregate_like_the_bench():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    res = sorted(q.get(timeout=10) for _ in range(2))
+    for rank, t, tok in res:
+        assert t == 11.0                 # max over ranks
+        assert tok == 2 * 8192.0 * 3     # whole-job tokens
+
+
+def test_single_rank_helpers_are_identity():
+    assert bench.max_over_ranks(3.5, 1) == 3.5
+    assert bench.sum_over_ranks(7.0, 1) == 7.0
+
+
+def test_algorithmic_model_matches_survey_numbers():
+    byts, flops = bench.prefill_alg(8192, 64, 128, 128, 1)
+    assert byts == 541_065_216                     # 8d per token-head + H d^2 4
+    assert flops == 8192 * 64 * (4 * 128 * 128 + 2 * 129 * 128)
+    assert bench.decode_alg(128, 64, 128) == 1_082_130_432
+
+
+def test_reference_arm_prints_one_json_line(tmp_path):
+    env = dict(os.environ, WORLD_SIZE="1", RANK="0")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "0"], capture_output=True, text=True,
+                       env=env, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    j = json.loads(lines[0])
+    assert j["impl"] == "reference" and j["value"] > 0 and j["unit"] == "tokens/s"
+    assert j["cpu_baseline"]["kind"] == "oracle" and j["cpu_baseline"]["cores"] >= 1
+    assert j["e2e"]["h2d_bytes_per_step"] == 0 and j["gpu_launches"] == 0
+
+
+def test_reference_arm_other_ranks_exit_quietly():
+    env = dict(os.environ, WORLD_SIZE="2", RANK="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "0"], capture_output=True, text=True,
+                       env=env, timeout=120, cwd=ROOT)
+    assert r.returncode == 0 and r.stdout.strip() == ""

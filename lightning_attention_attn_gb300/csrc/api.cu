@@ -8,7 +8,7 @@
 
 #include <cuda_runtime.h>
 
-#include "../../include/lightning_attn.h"
+#include "lightning_attn.h"
 #include "la_internal.h"
 
 namespace {

@@ -69,10 +69,11 @@ constexpr int D = 128;       // head dim (d_k = d_v)
 constexpr int DV = 64;       // value columns per CTA
 constexpr int NVS = D / DV;  // value slices per head
 constexpr int BC = 128;      // chunk (block) size
-constexpr int kThreads = 320;
+constexpr int kThreads = 512;      // 16 warps: 4 per SM sub-partition, 128 registers
 constexpr int kStateWarp0 = 4;
-constexpr int kTmaWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kVWarp0 = 8;
+constexpr int kTmaWarp = 12;
+constexpr int kMmaWarp = 13;
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
 
 // Shared memory (offsets from a 1024-byte aligned base).  Operand tiles are
@@ -88,7 +89,7 @@ constexpr uint32_t kOffCtrl = kOffKVb + 2 * kHalf;
 
 struct Ctrl {
     uint64_t full_q[2], full_k[2], full_v[2], empty_q[2], empty_k[2], empty_v[2];
-    uint64_t s_full[2], s_free[2], p_full[2], vmax_ready[2];
+    uint64_t s_full[2], s_free[2], p_full[2], vmax_ready[2], vconv_full[2];
     uint64_t o_full, o2_free, dkv_full, dkv_free, vhat_full, kv_full, kv_free, mma_done;
     uint32_t tmem_base;
     int abort;
@@ -97,6 +98,7 @@ struct Ctrl {
     float pw[BC + 4];         // pw[e] = lambda^e, e = 0..BC
     float rowscale[2][BC];    // 2^e_j of P's rows, per S buffer
     float vmax[2][4];         // per-warp max |v| of a chunk, double buffered
+    float vscale[4];          // 2^f of V's fp16 scale, ring indexed by chunk & 3
 };
 constexpr uint32_t kSmemBytes = kOffCtrl + sizeof(Ctrl) + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -213,6 +215,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             mbar_init(bar(cs.s_free[i]), 128);
             mbar_init(bar(cs.p_full[i]), 128);
             mbar_init(bar(cs.vmax_ready[i]), 128);
+            mbar_init(bar(cs.vconv_full[i]), 128);
         }
         mbar_init(bar(cs.o_full), 1);
         mbar_init(bar(cs.o2_free), 128);
@@ -276,55 +279,55 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         __syncwarp();
     } else if (warp == kMmaWarp) {
         // ================= MMA issuer =================
+        // Per chunk i: dKV_i, O2_i, then the next chunk's S_{i+1}, then P_i V_i.
+        // S_{i+1} goes before P_i V_i so that the mask warpgroup turns
+        // S_{i+1} into P_{i+1} while the tensor core runs P_i V_i, dKV_{i+1}
+        // and O2_{i+1}.
         if (lane == 0) {
             const uint32_t vha = sb + kOffVhat, kvb = sb + kOffKVb;
-            for (int i = 0; i < nch; ++i) {
+            auto issue_s = [&](int i) -> bool {  // S_i = Q_i K_i^T
+                const int st = i & 1;
+                const uint32_t sph = (i >> 1) & 1;
+                // buffer st is free once chunk i-2's P V and epilogue are done
+                if (!mbar_wait(bar(cs.full_q[st]), sph, abort_flag, kTimeoutNs)) return false;
+                if (!mbar_wait(bar(cs.full_k[st]), sph, abort_flag, kTimeoutNs)) return false;
+                if (!mbar_wait(bar(cs.s_free[st]), sph ^ 1, abort_flag, kTimeoutNs)) return false;
+                tc_fence_after();
+                mma8_k_k(tmem + st * 128, sdesc_sw128(qslot(st), 16, 1024),
+                         sdesc_sw128(kslot(st), 16, 1024), kIdescS);
+                mma_commit(bar(cs.s_full[st]));
+                return true;
+            };
+            bool ok = nch > 0 ? issue_s(0) : true;
+            for (int i = 0; ok && i < nch; ++i) {
                 const int st = i & 1;
                 const uint32_t sph = (i >> 1) & 1, ph = i & 1;
                 const uint32_t qa = qslot(st), ka = kslot(st), va = vslot(st);
                 const uint32_t colS = st * 128;
-                // S_i = Q_i K_i^T (buffer free once the epilogue of chunk i-2 read O1)
-                if (!mbar_wait(bar(cs.full_q[st]), sph, abort_flag, kTimeoutNs)) break;
-                if (!mbar_wait(bar(cs.full_k[st]), sph, abort_flag, kTimeoutNs)) break;
-                if (!mbar_wait(bar(cs.s_free[st]), sph ^ 1, abort_flag, kTimeoutNs)) break;
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-                    mma_bf16(tmem + colS, sdesc_sw128(qa + off, 16, 1024),
-                             sdesc_sw128(ka + off, 16, 1024), kIdescS, kk > 0);
-                }
-                mma_commit(bar(cs.s_full[st]));
                 // dKV_i = K_i^T [Vhat_hi | Vhat_lo]
                 if (!mbar_wait(bar(cs.vhat_full), ph, abort_flag, kTimeoutNs)) break;
                 if (!mbar_wait(bar(cs.dkv_free), ph ^ 1, abort_flag, kTimeoutNs)) break;
                 tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < BC / 16; ++kk)
-                    mma_bf16(tmem + kColDKV, sdesc_sw128(ka + kk * 2048, kHalf, 1024),
-                             sdesc_sw128(vha + kk * 2048, kHalf, 1024), kIdescKV, kk > 0);
+                mma8_mn_mn(tmem + kColDKV, sdesc_sw128(ka, kHalf, 1024),
+                           sdesc_sw128(vha, kHalf, 1024), kIdescKV);
                 mma_commit(bar(cs.dkv_full));
                 mma_commit(bar(cs.empty_k[st]));
                 // O2_i = Q_i [KV_hi | KV_lo] (the state after chunk i-1)
                 if (!mbar_wait(bar(cs.kv_full), ph, abort_flag, kTimeoutNs)) break;
                 if (!mbar_wait(bar(cs.o2_free), ph ^ 1, abort_flag, kTimeoutNs)) break;
                 tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-                    mma_bf16(tmem + kColO2, sdesc_sw128(qa + off, 16, 1024),
-                             sdesc_sw128(kvb + kk * 2048, kHalf, 1024), kIdescO2, kk > 0);
-                }
+                mma8_k_mn(tmem + kColO2, sdesc_sw128(qa, 16, 1024),
+                          sdesc_sw128(kvb, kHalf, 1024), kIdescO2);
                 mma_commit(bar(cs.kv_free));
                 mma_commit(bar(cs.empty_q[st]));
+                // S_{i+1}
+                if (i + 1 < nch && !(ok = issue_s(i + 1))) break;
                 // O1_i = P_i V_i (fp16; P in the first half of the S buffer,
                 // O1 into its second half)
                 if (!mbar_wait(bar(cs.p_full[st]), sph, abort_flag, kTimeoutNs)) break;
+                if (!mbar_wait(bar(cs.vconv_full[st]), sph, abort_flag, kTimeoutNs)) break;
                 tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < BC / 16; ++kk)
-                    mma_bf16_tmem_a(tmem + colS + 64, tmem + colS + kk * 8,
-                                    sdesc_sw128(va + kk * 2048, kHalf, 1024), kIdescPV, kk > 0);
+                mma8_t_mn(tmem + colS + 64, tmem + colS, sdesc_sw128(va, kHalf, 1024), kIdescPV);
                 mma_commit(bar(cs.o_full));
                 mma_commit(bar(cs.empty_v[st]));
             }
@@ -419,16 +422,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             tc_fence_before();
             mbar_arrive(bar(cs.p_full[st]));
         }
-    } else {
+    } else if (warp < kVWarp0) {
         // ================= state warpgroup =================
         const int w4 = warp - kStateWarp0;
         const int r = w4 * 32 + lane;  // TMEM lane: d_k row / token row
         const uint32_t lane_off = (uint32_t)(w4 * 32) << 16;
-        const uint32_t vha = sb + kOffVhat, kvb = sb + kOffKVb;
+        const uint32_t kvb = sb + kOffKVb;
+        const uint32_t vscale_s = smem_u32(&cs.vscale[0]);
         float kv[DV];
 #pragma unroll
         for (int c = 0; c < DV; ++c) kv[c] = 0.f;
-        float vscale0 = 1.f, vscale1 = 1.f;  // 2^f of the chunks with even / odd index
         // KV_{-1} = 0
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
@@ -438,87 +441,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         fence_proxy_async_smem();
         mbar_arrive(bar(cs.kv_full));
 
-        // V-tile row (token) handled by this thread: one each, so the tile
-        // conversion, which the next dKV MMA waits for, takes one row's time.
-        const int vrow0 = r;
-        // Chunk i's V tile: Vhat = Lambda_K V as a hi/lo bf16 pair, and V
-        // itself converted in place to fp16 with the chunk's power-of-two
-        // scale.  Rows past the chunk end are zero in both.
-        auto make_vhat = [&](int i) -> bool {
-            const int st = i & 1;
-            if (!warp_wait(bar(cs.full_v[st]), (i >> 1) & 1, abort_flag)) return false;
-            const int Lc = min(BC, L - i * BC);
-            const int vr = vrow0;
-            const bool live = vr < Lc;
-            const uint32_t row = vslot(st) + vr * 128;
-            uint32_t mbits = 0;  // max |v| as packed bf16 magnitudes
-            if (live) {
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const uint4 x = ld_shared_v4(row + (uint32_t)((c + vr) & 7) * 16);  // rotated
-                    mbits = __vmaxu2(mbits, x.x & 0x7fff7fffu);
-                    mbits = __vmaxu2(mbits, x.y & 0x7fff7fffu);
-                    mbits = __vmaxu2(mbits, x.z & 0x7fff7fffu);
-                    mbits = __vmaxu2(mbits, x.w & 0x7fff7fffu);
-                }
-            }
-            float m = fmaxf(__uint_as_float(mbits << 16), __uint_as_float(mbits & 0xffff0000u));
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-            if (lane == 0) st_shared_f32(vmax_s + 4u * (uint32_t)((i & 1) * 4 + w4), m);
-            mbar_arrive(bar(cs.vmax_ready[i & 1]));
-            if (!warp_wait(bar(cs.vmax_ready[i & 1]), (i >> 1) & 1, abort_flag)) return false;
-            const uint32_t vm = vmax_s + 16u * (uint32_t)(i & 1);
-            const float mt = fmaxf(fmaxf(ld_shared_f32(vm), ld_shared_f32(vm + 4)),
-                                   fmaxf(ld_shared_f32(vm + 8), ld_shared_f32(vm + 12)));
-            // fp16 scale: none when the tile is comfortably inside fp16's
-            // normal range, else 2^-f with max |v| 2^-f in [2^14, 2^15).
-            const int f = (mt <= 1024.f && mt >= 0.0625f) ? 0 : fp16_scale_exp(mt, 14);
-            const float inv = exp2i(-f);
-            if (i & 1)
-                vscale1 = exp2i(f);
-            else
-                vscale0 = exp2i(f);
-            // lambda^(Lc-1-l) split as g_hi + g_lo (bf16 each) so that the
-            // packed bf16 FMAs below give hi + lo = v g to ~16 bits.
-            const float g = live ? pw(Lc - 1 - vr) : 0.f;
-            const __nv_bfloat16 ghb = __float2bfloat16_rn(g);
-            const __nv_bfloat16 glb = __float2bfloat16_rn(g - __bfloat162float(ghb));
-            const __nv_bfloat162 gh = __halves2bfloat162(ghb, ghb);
-            const __nv_bfloat162 gl = __halves2bfloat162(glb, glb);
-            const float sc = live ? inv : 0.f;
-            const bool unscaled = f == 0 && live;
-#pragma unroll 2
-            for (int c = 0; c < 8; ++c) {
-                const uint32_t ch = (uint32_t)((c + vr) & 7) * 16;
-                const uint4 x = ld_shared_v4(row + ch);
-                const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-                uint32_t hi[4], lo[4], hv[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const __nv_bfloat162 v2 = *reinterpret_cast<const __nv_bfloat162 *>(&w[q]);
-                    const __nv_bfloat162 h2 = __hmul2(v2, gh);
-                    // exact residual of the rounded product, plus the g_lo term
-                    __nv_bfloat162 l2 = __hfma2(v2, gh, __hneg2(h2));
-                    l2 = __hfma2(v2, gl, l2);
-                    hi[q] = *reinterpret_cast<const uint32_t *>(&h2);
-                    lo[q] = *reinterpret_cast<const uint32_t *>(&l2);
-                    hv[q] = unscaled ? pack_f16(__uint_as_float(w[q] << 16),
-                                                __uint_as_float(w[q] & 0xffff0000u))
-                                     : pack_f16(__uint_as_float(w[q] << 16) * sc,
-                                                __uint_as_float(w[q] & 0xffff0000u) * sc);
-                }
-                st_shared_v4(vha + vr * 128 + ch, hi[0], hi[1], hi[2], hi[3]);
-                st_shared_v4(vha + kHalf + vr * 128 + ch, lo[0], lo[1], lo[2], lo[3]);
-                st_shared_v4(row + ch, hv[0], hv[1], hv[2], hv[3]);
-            }
-            fence_proxy_async_smem();
-            mbar_arrive(bar(cs.vhat_full));
-            return true;
-        };
-
-        bool ok = nch > 0 ? make_vhat(0) : true;
-        for (int i = 0; ok && i < nch; ++i) {
+        for (int i = 0; i < nch; ++i) {
             const int st = i & 1;
             const uint32_t sph = (i >> 1) & 1, ph = i & 1;
             const int Lc = min(BC, L - i * BC);
@@ -538,9 +461,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             }
             tc_fence_before();
             mbar_arrive(bar(cs.dkv_free));
-            // ---- next chunk's Vhat (its buffer is free: dKV_i is done), so
-            // the dKV MMA of chunk i+1 can follow S_{i+1} without a gap ----
-            if (i + 1 < nch && !(ok = make_vhat(i + 1))) break;
             // ---- hi/lo copy of KV_i for the next chunk's Q KV (after O2_i read KV_{i-1}) ----
             if (!warp_wait(bar(cs.kv_free), ph, abort_flag)) break;
 #pragma unroll
@@ -569,31 +489,28 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             if (!warp_wait(bar(cs.p_full[st]), sph, abort_flag)) break;  // orders rowscale
             tc_fence_after();
             const float s1 = ld_shared_f32(rowscale_s + 4u * (uint32_t)(st * BC + r)) *
-                             ((i & 1) ? vscale1 : vscale0);
+                             ld_shared_f32(vscale_s + 4u * (uint32_t)(i & 3));
             const float qf = pw(r + 1);
-            __nv_bfloat16 *orow = out + ((long)(t0 + i * BC + r) * H + h) * D + vs * DV;
+            uint4 *orow = reinterpret_cast<uint4 *>(out + ((long)(t0 + i * BC + r) * H + h) * D +
+                                                    vs * DV);
 #pragma unroll 1
-            for (int q = 0; q < 4; ++q) {
-                float a[16], b[16], c2[16];
-                tmem_ld16(tmem + lane_off + st * 128 + 64 + q * 16, a);
-                tmem_ld16(tmem + lane_off + kColO2 + q * 16, b);
-                tmem_ld16(tmem + lane_off + kColO2 + 64 + q * 16, c2);
+            for (int g = 0; g < 8; ++g) {
+                float a[8], b[8], c2[8];
+                tmem_ld8(tmem + lane_off + st * 128 + 64 + g * 8, a);
+                tmem_ld8(tmem + lane_off + kColO2 + g * 8, b);
+                tmem_ld8(tmem + lane_off + kColO2 + 64 + g * 8, c2);
                 tmem_wait_ld();
-                if (q == 3) {  // all TMEM reads of this chunk are done
+                if (g == 7) {  // all TMEM reads of this chunk are done
                     tc_fence_before();
                     mbar_arrive(bar(cs.o2_free));
                     mbar_arrive(bar(cs.s_free[st]));
                 }
-                uint32_t w[8];
+                uint32_t w[4];
 #pragma unroll
-                for (int m = 0; m < 8; ++m)
+                for (int m = 0; m < 4; ++m)
                     w[m] = pack_bf16(fmaf(qf, b[2 * m] + c2[2 * m], s1 * a[2 * m]),
                                      fmaf(qf, b[2 * m + 1] + c2[2 * m + 1], s1 * a[2 * m + 1]));
-                if (r < Lc) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + q * 16);
-                    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-                }
+                if (r < Lc) orow[g] = make_uint4(w[0], w[1], w[2], w[3]);
             }
         }
         if (final_state && !*abort_flag) {
@@ -603,7 +520,102 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             for (int c = 0; c < DV / 4; ++c)
                 dst[c] = make_float4(kv[4 * c], kv[4 * c + 1], kv[4 * c + 2], kv[4 * c + 3]);
         }
+    } else if (warp < kVWarp0 + 4) {
+        // ================= V-tile warpgroup =================
+        // Chunk i's V tile, one row (token) per thread, in two steps:
+        //  1. Vhat = Lambda_K V as a hi/lo bf16 pair for the dKV MMA (Vhat_i
+        //     may be written once dKV_{i-1} has read Vhat_{i-1});
+        //  2. V itself, converted in place to fp16 with the chunk's
+        //     power-of-two scale (a max over the tile) for the P V MMA.
+        // Rows past the chunk end are zero in both.
+        const int w4 = warp - kVWarp0;
+        const int vr = w4 * 32 + lane;
+        const uint32_t vha = sb + kOffVhat;
+        const uint32_t vscale_s = smem_u32(&cs.vscale[0]);
+        for (int i = 0; i < nch; ++i) {
+            const int st = i & 1;
+            if (i > 0 && !warp_wait(bar(cs.dkv_full), (i - 1) & 1, abort_flag)) break;
+            if (!warp_wait(bar(cs.full_v[st]), (i >> 1) & 1, abort_flag)) break;
+            const int Lc = min(BC, L - i * BC);
+            const bool live = vr < Lc;
+            const uint32_t row = vslot(st) + vr * 128;
+            uint4 x[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) x[c] = ld_shared_v4(row + (uint32_t)((c + vr) & 7) * 16);
+            // ---- 1: Vhat.  lambda^(Lc-1-l) split as g_hi + g_lo (bf16
+            // each) so that the packed bf16 FMAs give hi + lo = v g to ~16 bits.
+            {
+                const float g = live ? pw(Lc - 1 - vr) : 0.f;
+                const __nv_bfloat16 ghb = __float2bfloat16_rn(g);
+                const __nv_bfloat16 glb = __float2bfloat16_rn(g - __bfloat162float(ghb));
+                const __nv_bfloat162 gh = __halves2bfloat162(ghb, ghb);
+                const __nv_bfloat162 gl = __halves2bfloat162(glb, glb);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint32_t ch = (uint32_t)((c + vr) & 7) * 16;
+                    const uint32_t w[4] = {x[c].x, x[c].y, x[c].z, x[c].w};
+                    uint32_t hi[4], lo[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const __nv_bfloat162 v2 = *reinterpret_cast<const __nv_bfloat162 *>(&w[q]);
+                        const __nv_bfloat162 h2 = __hmul2(v2, gh);
+                        // exact residual of the rounded product, plus the g_lo term
+                        __nv_bfloat162 l2 = __hfma2(v2, gh, __hneg2(h2));
+                        l2 = __hfma2(v2, gl, l2);
+                        hi[q] = *reinterpret_cast<const uint32_t *>(&h2);
+                        lo[q] = *reinterpret_cast<const uint32_t *>(&l2);
+                    }
+                    st_shared_v4(vha + vr * 128 + ch, hi[0], hi[1], hi[2], hi[3]);
+                    st_shared_v4(vha + kHalf + vr * 128 + ch, lo[0], lo[1], lo[2], lo[3]);
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(bar(cs.vhat_full));
+            }
+            // ---- 2: fp16 V for P V
+            uint32_t mbits = 0;  // max |v| as packed bf16 magnitudes
+            if (live) {
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    mbits = __vmaxu2(mbits, x[c].x & 0x7fff7fffu);
+                    mbits = __vmaxu2(mbits, x[c].y & 0x7fff7fffu);
+                    mbits = __vmaxu2(mbits, x[c].z & 0x7fff7fffu);
+                    mbits = __vmaxu2(mbits, x[c].w & 0x7fff7fffu);
+                }
+            }
+            float m = fmaxf(__uint_as_float(mbits << 16), __uint_as_float(mbits & 0xffff0000u));
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            if (lane == 0) st_shared_f32(vmax_s + 4u * (uint32_t)((i & 1) * 4 + w4), m);
+            mbar_arrive(bar(cs.vmax_ready[i & 1]));
+            if (!warp_wait(bar(cs.vmax_ready[i & 1]), (i >> 1) & 1, abort_flag)) break;
+            const uint32_t vm = vmax_s + 16u * (uint32_t)(i & 1);
+            const float mt = fmaxf(fmaxf(ld_shared_f32(vm), ld_shared_f32(vm + 4)),
+                                   fmaxf(ld_shared_f32(vm + 8), ld_shared_f32(vm + 12)));
+            // no scale when the tile is comfortably inside fp16's normal
+            // range, else 2^-f with max |v| 2^-f in [2^14, 2^15)
+            const int f = (mt <= 1024.f && mt >= 0.0625f) ? 0 : fp16_scale_exp(mt, 14);
+            if (threadIdx.x == kVWarp0 * 32)
+                st_shared_f32(vscale_s + 4u * (uint32_t)(i & 3), exp2i(f));
+            const float sc = live ? exp2i(-f) : 0.f;
+            const bool unscaled = f == 0 && live;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const uint32_t ch = (uint32_t)((c + vr) & 7) * 16;
+                const uint32_t w[4] = {x[c].x, x[c].y, x[c].z, x[c].w};
+                uint32_t hv[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    hv[q] = unscaled ? pack_f16(__uint_as_float(w[q] << 16),
+                                                __uint_as_float(w[q] & 0xffff0000u))
+                                     : pack_f16(__uint_as_float(w[q] << 16) * sc,
+                                                __uint_as_float(w[q] & 0xffff0000u) * sc);
+                st_shared_v4(row + ch, hv[0], hv[1], hv[2], hv[3]);
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(bar(cs.vconv_full[st]));
+        }
     }
+    // warps 14 and 15 have no role
 
     // ---- teardown ----
     tc_fence_before();

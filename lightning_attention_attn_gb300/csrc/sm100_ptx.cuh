@@ -179,6 +179,80 @@ __device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem
         : "memory");
 }
 
+// Eight MMAs accumulating into one TMEM tile (D = sum_k A_k B_k + D when
+// acc != 0, else the first one overwrites D), from one inline-asm block so the issuing thread spends
+// two adds per instruction.  Operand k starts at the base descriptor plus a
+// fixed offset in 16-byte units: for a K-major 128-byte-swizzled operand of
+// 128 K values in two 64-wide halves (16 KB apart) the offsets are
+// 0, 2, 4, 6 (32 bytes into the swizzle row) then 1024 + the same; for an
+// MN-major operand, 16 K rows of 128 bytes = 128 units per step.
+#define LA_MMA8_BODY(A1, A2, A3, A4, A5, A6, A7, B1, B2, B3, B4, B5, B6, B7)                   \
+    "{\n\t.reg .pred pf, pt;\n\t.reg .b64 da, db;\n\t"                                      \
+    "setp.ne.b32 pf, %4, 0;\n\tsetp.eq.b32 pt, 0, 0;\n\t"                                    \
+    "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, pf;\n\t"                            \
+    "add.s64 da, %1, " A1 ";\n\tadd.s64 db, %2, " B1 ";\n\t"                                  \
+    "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, pt;\n\t"                            \
+    "add.s64 da, %1, " A2 ";\n\tadd.s64 db, %2, " B2 ";\n\t"                                  \
+    "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, pt;\n\t"                            \
+    "add.s64 da, %1, " A3 ";\n\tadd.s64 db, %2, " B3 ";\n\t"                                  \
+    "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, pt;\n\t"                            \
+    "add.s64 da, %1, " A4 ";\n\tadd.s64 db, %2, " B4 ";\n\t"                                  \
+    "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, pt;\n\t"                            \
+    "add.s64 da, %1, " A5 ";\n\tadd.s64 db, %2, " B5 ";\n\t"                                  \
+    "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, pt;\n\t"                            \
+    "add.s64 da, %1, " A6 ";\n\tadd.s64 db, %2, " B6 ";\n\t"                                  \
+    "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, pt;\n\t"                            \
+    "add.s64 da, %1, " A7 ";\n\tadd.s64 db, %2, " B7 ";\n\t"                                  \
+    "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, pt;\n\t}"
+
+// A K-major, B K-major (Q K^T)
+__device__ __forceinline__ void mma8_k_k(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                          uint32_t acc = 0) {
+    asm volatile(LA_MMA8_BODY("2", "4", "6", "1024", "1026", "1028", "1030",
+                              "2", "4", "6", "1024", "1026", "1028", "1030")
+                 ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc)
+                 : "memory");
+}
+// A K-major, B MN-major (Q [KV_hi | KV_lo])
+__device__ __forceinline__ void mma8_k_mn(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                          uint32_t acc = 0) {
+    asm volatile(LA_MMA8_BODY("2", "4", "6", "1024", "1026", "1028", "1030",
+                              "128", "256", "384", "512", "640", "768", "896")
+                 ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc)
+                 : "memory");
+}
+// A MN-major, B MN-major (K^T [Vhat_hi | Vhat_lo])
+__device__ __forceinline__ void mma8_mn_mn(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                          uint32_t acc = 0) {
+    asm volatile(LA_MMA8_BODY("128", "256", "384", "512", "640", "768", "896",
+                              "128", "256", "384", "512", "640", "768", "896")
+                 ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc)
+                 : "memory");
+}
+// A from TMEM (8 columns per step), B MN-major (P V)
+__device__ __forceinline__ void mma8_t_mn(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc) {
+    asm volatile(
+        "{\n\t.reg .pred pf, pt;\n\t.reg .b32 ta;\n\t.reg .b64 db;\n\t"
+        "setp.ne.b32 pf, 0, 0;\n\tsetp.eq.b32 pt, 0, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, pf;\n\t"
+        "add.u32 ta, %1, 8;\n\tadd.s64 db, %2, 128;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %3, pt;\n\t"
+        "add.u32 ta, %1, 16;\n\tadd.s64 db, %2, 256;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %3, pt;\n\t"
+        "add.u32 ta, %1, 24;\n\tadd.s64 db, %2, 384;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %3, pt;\n\t"
+        "add.u32 ta, %1, 32;\n\tadd.s64 db, %2, 512;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %3, pt;\n\t"
+        "add.u32 ta, %1, 40;\n\tadd.s64 db, %2, 640;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %3, pt;\n\t"
+        "add.u32 ta, %1, 48;\n\tadd.s64 db, %2, 768;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %3, pt;\n\t"
+        "add.u32 ta, %1, 56;\n\tadd.s64 db, %2, 896;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %3, pt;\n\t}"
+        ::"r"(d), "r"(a_tmem), "l"(b), "r"(idesc)
+        : "memory");
+}
+
 // The mbarrier completes one arrival when every tcgen05 operation this
 // thread issued before it has finished.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -215,6 +289,15 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&r)[16]) {
           "=r"(u[13]), "=r"(u[14]), "=r"(u[15])
         : "r"(taddr)
         : "memory");
+}
+// 32 lanes x 8 consecutive fp32 columns (see tmem_ld32).
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&r)[8]) {
+    uint32_t *u = reinterpret_cast<uint32_t *>(r);
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]),
+                   "=r"(u[6]), "=r"(u[7])
+                 : "r"(taddr)
+                 : "memory");
 }
 // 32 lanes x 16 consecutive 32-bit columns: thread t writes row
 // (lane base + t), columns [col, col + 16).

@@ -29,19 +29,28 @@
 // the tensor core as fp16 (11 significant bits), each with an exact
 // power-of-two scale chosen so the values sit at the top of the fp16 range
 // (P per row, V per chunk): no overflow, no subnormal loss, and the scale is
-// undone in fp32 in the epilogue.  The fp32 state itself lives in registers
-// of the state warpgroup for the whole sequence.  Nothing but q, k, v (read
-// once per CTA) and out / final state (written once) touches HBM.
+// undone in fp32 in the epilogue.  The fp32 state itself lives in TMEM for
+// the whole sequence, as the sum of the two halves of the dKV accumulator:
+// the state warpgroup writes lambda^{B_{i+1}} KV_i back into it and the next
+// dKV MMA accumulates onto that.  Nothing but q, k, v (read once per CTA)
+// and out / final state (written once) touches HBM.
 //
 // TMEM (512 columns): S buffer b = columns [128b, 128b + 128): S (fp32), then
 // P (fp16 pairs) over its first 64 columns and O1 (fp32) in its last 64;
-// O2 = [256, 384); dKV = [384, 512).
+// O2 = [256, 384); dKV / state = [384, 512).
 //
-// Warp roles (320 threads):
-//   warps 0-3  mask warpgroup: S -> P = fp16(2^-e_j S (.) M) into TMEM
-//   warps 4-7  state warpgroup: Vhat / fp16 V, KV update, KV copy, output
-//   warp  8    TMA producer: Q, K, V two-slot rings
-//   warp  9    MMA issuer (one thread)
+// Warp roles (512 threads, 128 registers each):
+//   warps 0-3    mask: S -> P = fp16(2^-e_j S (.) M) into TMEM, one lane
+//                quadrant each, helped by warps 14 and 15 on the two
+//                quadrants with the most blocks below the diagonal
+//   warps 4-7    state: KV fold + write-back, KV copy, output; its thread 0
+//                also issues the TMA loads of the Q, K, V two-slot rings
+//   warps 8-11   V-tile: Vhat hi/lo, fp16 V
+//   warp  12     MMA stream A (one thread): S and P V
+//   warp  13     MMA stream B (one thread): dKV and Q KV
+// Two issuing threads keep the tensor pipe fed while either one waits: the
+// tcgen05 instruction queue is short, so a wait between two groups of MMAs
+// from a single issuer leaves the pipe idle.
 // Every wait is bounded and warp-uniform: a wait that gives up sets a CTA-wide
 // abort flag, all roles leave their loops, in-flight TMA copies and MMAs are
 // drained, TMEM is freed, and a device error word is raised for
@@ -69,11 +78,13 @@ constexpr int D = 128;       // head dim (d_k = d_v)
 constexpr int DV = 64;       // value columns per CTA
 constexpr int NVS = D / DV;  // value slices per head
 constexpr int BC = 128;      // chunk (block) size
-constexpr int kThreads = 512;      // 16 warps: 4 per SM sub-partition, 128 registers
-constexpr int kStateWarp0 = 4;
+constexpr int kThreads = 512;  // 16 warps: 4 per SM sub-partition, 128 registers
+constexpr int kStateWarp0 = 4; // thread 0 of this warp also issues the TMA loads
 constexpr int kVWarp0 = 8;
-constexpr int kTmaWarp = 12;
-constexpr int kMmaWarp = 13;
+constexpr int kMmaWarpA = 12;  // S and P V
+constexpr int kMmaWarpB = 13;  // dKV and Q KV
+constexpr int kMaskHelp2 = 14; // helps mask warp 2 (TMEM lanes 64-95)
+constexpr int kMaskHelp3 = 15; // helps mask warp 3 (TMEM lanes 96-127)
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
 
 // Shared memory (offsets from a 1024-byte aligned base).  Operand tiles are
@@ -88,17 +99,19 @@ constexpr uint32_t kOffKVb = kOffVhat + 2 * kHalf; // hi, lo: 128 d_k x 64
 constexpr uint32_t kOffCtrl = kOffKVb + 2 * kHalf;
 
 struct Ctrl {
+    alignas(16) float pw[BC + 4];  // pw[e] = lambda^e, e = 0..BC
     uint64_t full_q[2], full_k[2], full_v[2], empty_q[2], empty_k[2], empty_v[2];
-    uint64_t s_full[2], s_free[2], p_full[2], vmax_ready[2], vconv_full[2];
-    uint64_t o_full, o2_free, dkv_full, dkv_free, vhat_full, kv_full, kv_free, mma_done;
+    uint64_t s_full[2], s_free[2], pv_ready[2], vmax_ready[2], pair[2], o_full[2];
+    uint64_t o2_full, o2_ready, dkv_full, dkv_ready, done_a, done_b;
     uint32_t tmem_base;
     int abort;
     int seq_slot;
     int pad;
-    float pw[BC + 4];         // pw[e] = lambda^e, e = 0..BC
-    float rowscale[2][BC];    // 2^e_j of P's rows, per S buffer
-    float vmax[2][4];         // per-warp max |v| of a chunk, double buffered
-    float vscale[4];          // 2^f of V's fp16 scale, ring indexed by chunk & 3
+    float vmax[2][4];              // per-warp max |v| of a chunk, double buffered
+    float vscale[4];               // 2^f of V's fp16 scale, ring indexed by chunk & 3
+    signed char rowe[2][BC];       // e_j of P's rows (scale 2^-e_j), per S buffer
+    uint16_t mpart[2][2][2][32];   // [pair][chunk & 1][owner, helper][lane]: partial
+                                   // row bounds, top 16 bits of the float
 };
 constexpr uint32_t kSmemBytes = kOffCtrl + sizeof(Ctrl) + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -118,16 +131,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
     __half2 v = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
-}
-__device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
-    __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162 *>(&u);
-    return __bfloat1622float2(v);
-}
-// hi = bf16(x), lo = bf16(x - hi), packed in pairs
-__device__ __forceinline__ void split_bf16(float a, float b, uint32_t &hi, uint32_t &lo) {
-    const __nv_bfloat16 ha = __float2bfloat16_rn(a), hb = __float2bfloat16_rn(b);
-    hi = (uint32_t)__bfloat16_as_ushort(ha) | ((uint32_t)__bfloat16_as_ushort(hb) << 16);
-    lo = pack_bf16(a - __bfloat162float(ha), b - __bfloat162float(hb));
 }
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
@@ -195,8 +198,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
 
     auto bar = [&](const uint64_t &b) { return smem_u32(&b); };
     const uint32_t pw_s = smem_u32(&cs.pw[0]);          // lambda^e at pw_s + 4 e
-    const uint32_t rowscale_s = smem_u32(&cs.rowscale[0][0]);
+    const uint32_t rowe_s = smem_u32(&cs.rowe[0][0]);
     const uint32_t vmax_s = smem_u32(&cs.vmax[0][0]);
+    const uint32_t vscale_s = smem_u32(&cs.vscale[0]);
     auto pw = [&](int e) { return ld_shared_f32(pw_s + 4u * (uint32_t)e); };
     auto qslot = [&](int st) { return sb + kOffQ + st * 2 * kHalf; };
     auto kslot = [&](int st) { return sb + kOffK + st * 2 * kHalf; };
@@ -208,23 +212,24 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             mbar_init(bar(cs.full_q[i]), 1);
             mbar_init(bar(cs.full_k[i]), 1);
             mbar_init(bar(cs.full_v[i]), 1);
-            mbar_init(bar(cs.empty_q[i]), 1);
-            mbar_init(bar(cs.empty_k[i]), 1);
+            mbar_init(bar(cs.empty_q[i]), 2);  // S_i (stream A) and Q_i KV (stream B)
+            mbar_init(bar(cs.empty_k[i]), 2);  // S_i (stream A) and dKV_i (stream B)
             mbar_init(bar(cs.empty_v[i]), 1);
             mbar_init(bar(cs.s_full[i]), 1);
             mbar_init(bar(cs.s_free[i]), 128);
-            mbar_init(bar(cs.p_full[i]), 128);
+            mbar_init(bar(cs.pv_ready[i]), 6 * 32 + 128);  // mask warps + V-tile warpgroup
             mbar_init(bar(cs.vmax_ready[i]), 128);
-            mbar_init(bar(cs.vconv_full[i]), 128);
+            mbar_init(bar(cs.pair[i]), 64);
+            // by chunk parity: near the end of a sequence stream A may finish
+            // two P V groups before the state warps wait for the first
+            mbar_init(bar(cs.o_full[i]), 1);
         }
-        mbar_init(bar(cs.o_full), 1);
-        mbar_init(bar(cs.o2_free), 128);
+        mbar_init(bar(cs.o2_full), 1);
+        mbar_init(bar(cs.o2_ready), 128);
         mbar_init(bar(cs.dkv_full), 1);
-        mbar_init(bar(cs.dkv_free), 128);
-        mbar_init(bar(cs.vhat_full), 128);
-        mbar_init(bar(cs.kv_full), 128);
-        mbar_init(bar(cs.kv_free), 1);
-        mbar_init(bar(cs.mma_done), 1);
+        mbar_init(bar(cs.dkv_ready), 256);  // V-tile (Vhat) + state (write-back)
+        mbar_init(bar(cs.done_a), 1);
+        mbar_init(bar(cs.done_b), 1);
         cs.abort = 0;
         fence_mbar_init();
     }
@@ -236,124 +241,167 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = cs.tmem_base;
+    // broadcast so that the compiler sees a warp-uniform TMEM address
+    const uint32_t tmem = __shfl_sync(0xffffffffu, cs.tmem_base, 0);
     volatile int *abort_flag = &cs.abort;
 
-    if (warp == kTmaWarp) {
-        // ================= TMA producer =================
-        if (lane == 0) {
-            tma_prefetch_desc(&tmQ);
-            tma_prefetch_desc(&tmK);
-            tma_prefetch_desc(&tmV);
-            tma_prefetch_desc(&tmO);
-            int nq = 0, nk = 0, nv = 0;
-            bool ok = true;
-            for (int i = 0; i < nch && ok; ++i) {
-                const int st = i & 1;
-                const uint32_t sph = (i >> 1) & 1;
-                const int y = t0 + i * BC;
-                if (!(ok = mbar_wait(bar(cs.empty_q[st]), sph ^ 1, abort_flag, kTimeoutNs))) break;
-                mbar_arrive_expect_tx(bar(cs.full_q[st]), 2 * kHalf);
-                tma_load_2d(qslot(st), &tmQ, bar(cs.full_q[st]), h * D, y);
-                tma_load_2d(qslot(st) + kHalf, &tmQ, bar(cs.full_q[st]), h * D + 64, y);
-                ++nq;
-                if (!(ok = mbar_wait(bar(cs.empty_k[st]), sph ^ 1, abort_flag, kTimeoutNs))) break;
-                mbar_arrive_expect_tx(bar(cs.full_k[st]), 2 * kHalf);
-                tma_load_2d(kslot(st), &tmK, bar(cs.full_k[st]), h * D, y);
-                tma_load_2d(kslot(st) + kHalf, &tmK, bar(cs.full_k[st]), h * D + 64, y);
-                ++nk;
-                if (!(ok = mbar_wait(bar(cs.empty_v[st]), sph ^ 1, abort_flag, kTimeoutNs))) break;
-                mbar_arrive_expect_tx(bar(cs.full_v[st]), kHalf);
-                tma_load_2d(vslot(st), &tmV, bar(cs.full_v[st]), h * D + vs * DV, y);
-                ++nv;
-            }
-            // Never leave with a load still landing in shared memory.
-            int no_abort = 0;
-            for (int c = max(0, nq - 2); c < nq; ++c)
-                mbar_wait(bar(cs.full_q[c & 1]), (c >> 1) & 1, &no_abort, kTimeoutNs);
-            for (int c = max(0, nk - 2); c < nk; ++c)
-                mbar_wait(bar(cs.full_k[c & 1]), (c >> 1) & 1, &no_abort, kTimeoutNs);
-            for (int c = max(0, nv - 2); c < nv; ++c)
-                mbar_wait(bar(cs.full_v[c & 1]), (c >> 1) & 1, &no_abort, kTimeoutNs);
-        }
-        __syncwarp();
-    } else if (warp == kMmaWarp) {
-        // ================= MMA issuer =================
-        // Per chunk i: dKV_i, O2_i, then the next chunk's S_{i+1}, then P_i V_i.
-        // S_{i+1} goes before P_i V_i so that the mask warpgroup turns
-        // S_{i+1} into P_{i+1} while the tensor core runs P_i V_i, dKV_{i+1}
-        // and O2_{i+1}.
-        if (lane == 0) {
-            const uint32_t vha = sb + kOffVhat, kvb = sb + kOffKVb;
-            auto issue_s = [&](int i) -> bool {  // S_i = Q_i K_i^T
-                const int st = i & 1;
-                const uint32_t sph = (i >> 1) & 1;
-                // buffer st is free once chunk i-2's P V and epilogue are done
-                if (!mbar_wait(bar(cs.full_q[st]), sph, abort_flag, kTimeoutNs)) return false;
-                if (!mbar_wait(bar(cs.full_k[st]), sph, abort_flag, kTimeoutNs)) return false;
-                if (!mbar_wait(bar(cs.s_free[st]), sph ^ 1, abort_flag, kTimeoutNs)) return false;
-                tc_fence_after();
-                mma8_k_k(tmem + st * 128, sdesc_sw128(qslot(st), 16, 1024),
-                         sdesc_sw128(kslot(st), 16, 1024), kIdescS);
+    if (warp == kMmaWarpA) {
+        // ================= MMA stream A: S and P V =================
+        // Per chunk i: S_{i+1}, then P_i V_i, so that the mask warps turn
+        // S_{i+1} into P_{i+1} while the tensor core runs P_i V_i and stream
+        // B's dKV / Q KV.  The whole warp waits; lane 0 issues.
+        auto issue_s = [&](int i) -> bool {  // S_i = Q_i K_i^T
+            const int st = i & 1;
+            const uint32_t sph = (i >> 1) & 1;
+            if (!warp_wait(bar(cs.full_q[st]), sph, abort_flag)) return false;
+            if (!warp_wait(bar(cs.full_k[st]), sph, abort_flag)) return false;
+            // buffer st is free once chunk i-2's output has read its O1
+            if (!warp_wait(bar(cs.s_free[st]), sph ^ 1, abort_flag)) return false;
+            tc_fence_after();
+            if (lane == 0) {
+                mma_group_ss(tmem + st * 128, sdesc_sw128(qslot(st), 16, 1024), kKMajorS1,
+                             kKMajorS2, sdesc_sw128(kslot(st), 16, 1024), kKMajorS1, kKMajorS2,
+                             kIdescS, 0u);
                 mma_commit(bar(cs.s_full[st]));
-                return true;
-            };
-            bool ok = nch > 0 ? issue_s(0) : true;
-            for (int i = 0; ok && i < nch; ++i) {
-                const int st = i & 1;
-                const uint32_t sph = (i >> 1) & 1, ph = i & 1;
-                const uint32_t qa = qslot(st), ka = kslot(st), va = vslot(st);
-                const uint32_t colS = st * 128;
-                // dKV_i = K_i^T [Vhat_hi | Vhat_lo]
-                if (!mbar_wait(bar(cs.vhat_full), ph, abort_flag, kTimeoutNs)) break;
-                if (!mbar_wait(bar(cs.dkv_free), ph ^ 1, abort_flag, kTimeoutNs)) break;
-                tc_fence_after();
-                mma8_mn_mn(tmem + kColDKV, sdesc_sw128(ka, kHalf, 1024),
-                           sdesc_sw128(vha, kHalf, 1024), kIdescKV);
-                mma_commit(bar(cs.dkv_full));
-                mma_commit(bar(cs.empty_k[st]));
-                // O2_i = Q_i [KV_hi | KV_lo] (the state after chunk i-1)
-                if (!mbar_wait(bar(cs.kv_full), ph, abort_flag, kTimeoutNs)) break;
-                if (!mbar_wait(bar(cs.o2_free), ph ^ 1, abort_flag, kTimeoutNs)) break;
-                tc_fence_after();
-                mma8_k_mn(tmem + kColO2, sdesc_sw128(qa, 16, 1024),
-                          sdesc_sw128(kvb, kHalf, 1024), kIdescO2);
-                mma_commit(bar(cs.kv_free));
                 mma_commit(bar(cs.empty_q[st]));
-                // S_{i+1}
-                if (i + 1 < nch && !(ok = issue_s(i + 1))) break;
-                // O1_i = P_i V_i (fp16; P in the first half of the S buffer,
-                // O1 into its second half)
-                if (!mbar_wait(bar(cs.p_full[st]), sph, abort_flag, kTimeoutNs)) break;
-                if (!mbar_wait(bar(cs.vconv_full[st]), sph, abort_flag, kTimeoutNs)) break;
-                tc_fence_after();
-                mma8_t_mn(tmem + colS + 64, tmem + colS, sdesc_sw128(va, kHalf, 1024), kIdescPV);
-                mma_commit(bar(cs.o_full));
+                mma_commit(bar(cs.empty_k[st]));
+            }
+            __syncwarp();
+            return true;
+        };
+        for (int i = -1; i < nch; ++i) {
+            if (i + 1 < nch && !issue_s(i + 1)) break;
+            if (i < 0) continue;
+            const int st = i & 1;
+            const uint32_t sph = (i >> 1) & 1;
+            // O1_i = P_i V_i (fp16; P in the first half of the S buffer, O1
+            // into its second half)
+            if (!warp_wait(bar(cs.pv_ready[st]), sph, abort_flag)) break;
+            tc_fence_after();
+            if (lane == 0) {
+                mma_group_ts(tmem + st * 128 + 64, tmem + st * 128,
+                             sdesc_sw128(vslot(st), kHalf, 1024), kIdescPV, 0u);
+                mma_commit(bar(cs.o_full[st]));
                 mma_commit(bar(cs.empty_v[st]));
             }
-            // All MMAs must be finished before TMEM is released.
-            mma_commit(bar(cs.mma_done));
-            int no_abort = 0;
-            mbar_wait(bar(cs.mma_done), 0, &no_abort, kTimeoutNs);
+            __syncwarp();
         }
+        // All MMAs must be finished before TMEM is released.
+        if (lane == 0) mma_commit(bar(cs.done_a));
         __syncwarp();
-    } else if (warp < kStateWarp0) {
-        // ================= mask warpgroup: S -> P =================
-        // Thread j owns row j of the chunk (TMEM lane j).  p_jl = S_jl
-        // lambda^(j-l) for l <= j, l < Lc, else 0.  P goes to TMEM as fp16
-        // scaled by 2^-e_j, a power of two chosen from an upper bound of the
-        // row's |p| (pass 1: max |S| of each column block times the block's
-        // largest decay factor) so the row's values sit below 2^12: no
+        int no_abort = 0;
+        warp_wait(bar(cs.done_a), 0, &no_abort);
+    } else if (warp == kMmaWarpB) {
+        // ================= MMA stream B: dKV and Q KV =================
+        const uint32_t vha = sb + kOffVhat, kvb = sb + kOffKVb;
+        for (int i = 0; i < nch; ++i) {
+            const int st = i & 1;
+            const uint32_t sph = (i >> 1) & 1, ph = i & 1;
+            // dKV += K_i^T [Vhat_hi | Vhat_lo]: the accumulator holds
+            // lambda^{B_i} KV_{i-1}, written back by the state warpgroup
+            if (!warp_wait(bar(cs.full_k[st]), sph, abort_flag)) break;
+            if (!warp_wait(bar(cs.dkv_ready), ph, abort_flag)) break;
+            tc_fence_after();
+            if (lane == 0) {
+                mma_group_ss(tmem + kColDKV, sdesc_sw128(kslot(st), kHalf, 1024), kMNMajorS1,
+                             kMNMajorS2, sdesc_sw128(vha, kHalf, 1024), kMNMajorS1, kMNMajorS2,
+                             kIdescKV, i > 0 ? 1u : 0u);
+                mma_commit(bar(cs.dkv_full));
+                mma_commit(bar(cs.empty_k[st]));
+            }
+            __syncwarp();
+            // O2_i = Q_i [KV_hi | KV_lo] (the state after chunk i-1)
+            if (!warp_wait(bar(cs.full_q[st]), sph, abort_flag)) break;
+            if (!warp_wait(bar(cs.o2_ready), ph, abort_flag)) break;
+            tc_fence_after();
+            if (lane == 0) {
+                mma_group_ss(tmem + kColO2, sdesc_sw128(qslot(st), 16, 1024), kKMajorS1,
+                             kKMajorS2, sdesc_sw128(kvb, kHalf, 1024), kMNMajorS1, kMNMajorS2,
+                             kIdescO2, 0u);
+                mma_commit(bar(cs.o2_full));
+                mma_commit(bar(cs.empty_q[st]));
+            }
+            __syncwarp();
+        }
+        if (lane == 0) mma_commit(bar(cs.done_b));
+        __syncwarp();
+        int no_abort = 0;
+        warp_wait(bar(cs.done_b), 0, &no_abort);
+    } else if (warp < kStateWarp0 || warp == kMaskHelp2 || warp == kMaskHelp3) {
+        // ================= mask warps: S -> P =================
+        // Row j of the chunk is TMEM lane j; the warps of lane quadrant q
+        // (rows 32q .. 32q + 31) hold that quadrant's 32-column S blocks
+        // cb <= q in registers, two at most per warp (quadrants 2 and 3 are
+        // split between an owner warp, which has the diagonal block, and a
+        // helper warp).  p_jl = S_jl lambda^(j-l) for l <= j, l < Lc, else 0.
+        // P goes to TMEM as fp16 scaled by 2^-e_j, a power of two chosen from
+        // an upper bound of the row's |p| (max |S| of each block times the
+        // block's largest decay factor; the two warps of a split quadrant
+        // exchange their partial bounds) so that the row sits below 2^12: no
         // overflow, and 11 significant bits for everything within 2^25 of
-        // the bound.  Pass 2 masks, scales and packs one 32-column block at a
-        // time into TMEM columns [16 cb, 16 cb + 16) of the S buffer: blocks
-        // are visited in increasing cb, so block cb overwrites S columns of
-        // block cb / 2 <= cb, already read.
-        const int j = warp * 32 + lane;
-        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-        float colf[32];  // lambda^(31-c): off the diagonal block,
-#pragma unroll           // lambda^(j-l) = lambda^(j-(32cb+31)) lambda^(31-c)
-        for (int c = 0; c < 32; ++c) colf[c] = pw(31 - c);
+        // the bound.  P block cb lands in TMEM columns [16 cb, 16 cb + 16) of
+        // the S buffer; it is written after every S block of the quadrant
+        // has been read (the exchange orders the two warps of a pair).
+        const int q = warp & 3;
+        const bool owner = warp < kStateWarp0;
+        const int j = q * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        const int cb0 = owner ? (q < 2 ? 0 : q - 1) : 0;
+        const int nb = owner ? (q == 0 ? 1 : 2) : (q == 2 ? 1 : 2);
+        const int pr = q - 2;  // pair index of a split quadrant
+        // Upper bound of |p| over the valid columns of one block.
+        auto block_bound = [&](const float(&sv)[32], int cb, int Lc) -> float {
+            const bool diag = cb == q;
+            const int lim = min(diag ? lane : 31, Lc - 1 - cb * 32);  // last valid column
+            float t[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+                t[k] = fmaxf(2 * k <= lim ? fabsf(sv[2 * k]) : 0.f,
+                             2 * k + 1 <= lim ? fabsf(sv[2 * k + 1]) : 0.f);
+#pragma unroll
+            for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+                for (int k = 0; k < w; ++k) t[k] = fmaxf(t[k], t[k + w]);
+            return diag ? t[0] : t[0] * pw(j - cb * 32 - 31);
+        };
+        // Masks, decays, scales and packs one block into TMEM.
+        auto write_block = [&](const float(&sv)[32], int cb, int Lc, float inv, uint32_t scol) {
+            uint32_t pk[16];
+            if (cb == q) {  // diagonal block: lambda^(lane - c) for c <= lane
+                const int lim = min(lane, Lc - 1 - cb * 32);
+                const float2 inv2 = make_float2(inv, inv);
+#pragma unroll
+                for (int m = 0; m < 16; ++m) {
+                    const int c = 2 * m;
+                    const float2 f = f2_mul(make_float2(pw(max(lane - c, 0)), pw(max(lane - c - 1, 0))),
+                                            inv2);
+                    const float2 x = f2_mul(make_float2(sv[c], sv[c + 1]), f);
+                    pk[m] = pack_f16(c <= lim ? x.x : 0.f, c + 1 <= lim ? x.y : 0.f);
+                }
+            } else {  // below the diagonal: lambda^(j - 32 cb - 31) lambda^(31 - c)
+                const float rowf = pw(j - cb * 32 - 31) * inv;
+                const float2 rf = make_float2(rowf, rowf);
+                const int lim = min(31, Lc - 1 - cb * 32);
+#pragma unroll
+                for (int g = 0; g < 8; ++g) {
+                    // lambda^(31 - c) for c = 4g .. 4g + 3: pw[28 - 4g .. 31 - 4g] reversed
+                    const uint4 cu4 = ld_shared_v4(pw_s + 16u * (uint32_t)(7 - g));
+                    const float2 f0 = f2_mul(rf, make_float2(__uint_as_float(cu4.w), __uint_as_float(cu4.z)));
+                    const float2 f1 = f2_mul(rf, make_float2(__uint_as_float(cu4.y), __uint_as_float(cu4.x)));
+                    float2 x0 = f2_mul(make_float2(sv[4 * g], sv[4 * g + 1]), f0);
+                    float2 x1 = f2_mul(make_float2(sv[4 * g + 2], sv[4 * g + 3]), f1);
+                    if (lim < 31) {  // ragged last chunk
+                        x0.x = 4 * g <= lim ? x0.x : 0.f;
+                        x0.y = 4 * g + 1 <= lim ? x0.y : 0.f;
+                        x1.x = 4 * g + 2 <= lim ? x1.x : 0.f;
+                        x1.y = 4 * g + 3 <= lim ? x1.y : 0.f;
+                    }
+                    pk[2 * g] = pack_f16(x0.x, x0.y);
+                    pk[2 * g + 1] = pack_f16(x1.x, x1.y);
+                }
+            }
+            tmem_st16(scol + cb * 16, pk);
+        };
         uint32_t zero[16];
 #pragma unroll
         for (int m = 0; m < 16; ++m) zero[m] = 0u;
@@ -364,74 +412,100 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             const uint32_t scol = tmem + lane_off + st * 128;
             if (!warp_wait(bar(cs.s_full[st]), sph, abort_flag)) break;
             tc_fence_after();
-            // pass 1: bound of max |p| over the row
-            float bound = 0.f;
-#pragma unroll 1
-            for (int cb = 0; cb <= warp; ++cb) {
-                float sv[32];
-                tmem_ld32(scol + cb * 32, sv);
-                tmem_wait_ld();
-                const int lim = min(cb == warp ? lane : 31, Lc - 1 - cb * 32);  // last valid c
-                float m = 0.f;
-#pragma unroll
-                for (int c = 0; c < 32; ++c)
-                    if (c <= lim) m = fmaxf(m, fabsf(sv[c]));
-                bound = fmaxf(bound, cb == warp ? m : m * pw(j - cb * 32 - 31));
+            float sa[32], sb2[32];
+            tmem_ld32(scol + cb0 * 32, sa);
+            if (nb == 2) tmem_ld32(scol + (cb0 + 1) * 32, sb2);
+            tmem_wait_ld();
+            float bound = block_bound(sa, cb0, Lc);
+            if (nb == 2) bound = fmaxf(bound, block_bound(sb2, cb0 + 1, Lc));
+            if (q >= 2) {  // exchange with the other warp of the quadrant
+                // Only the exponent of the bound matters: pass its top 16 bits
+                // (a nonzero bound stays nonzero), so both warps pick the same e.
+                const uint32_t ub = __float_as_uint(bound);
+                const uint16_t mine = (uint16_t)((ub >> 16) | ((ub >> 16) == 0u && ub != 0u ? 1u : 0u));
+                cs.mpart[pr][i & 1][owner ? 0 : 1][lane] = mine;
+                mbar_arrive(bar(cs.pair[pr]));
+                if (!warp_wait(bar(cs.pair[pr]), (uint32_t)(i & 1), abort_flag)) break;
+                const uint32_t theirs = *reinterpret_cast<volatile uint16_t *>(
+                    &cs.mpart[pr][i & 1][owner ? 1 : 0][lane]);
+                bound = fmaxf(__uint_as_float((uint32_t)mine << 16), __uint_as_float(theirs << 16));
             }
             const int e = fp16_scale_exp(bound, 11);
             const float inv = exp2i(-e);
-            // pass 2: the blocks below the diagonal in increasing order, then
-            // the diagonal block (P block cb lands in S block cb / 2 <= cb,
-            // which has been read by then)
+            // one copy of the block code for both held blocks (the
+            // instruction cache is shared by the roles of a sub-partition)
 #pragma unroll 1
-            for (int cb = 0; cb < warp; ++cb) {
-                float sv[32];
-                tmem_ld32(scol + cb * 32, sv);
-                tmem_wait_ld();
-                const float rowf = pw(j - cb * 32 - 31) * inv;
-                const int lim = Lc - 1 - cb * 32;
-                uint32_t pk[16];
+            for (int k = 0; k < nb; ++k) {
+                write_block(sa, cb0 + k, Lc, inv, scol);
 #pragma unroll
-                for (int m = 0; m < 16; ++m) {
-                    const int c = 2 * m;
-                    const float a = (c <= lim) ? sv[c] * (rowf * colf[c]) : 0.f;
-                    const float b = (c + 1 <= lim) ? sv[c + 1] * (rowf * colf[c + 1]) : 0.f;
-                    pk[m] = pack_f16(a, b);
-                }
-                tmem_st16(scol + cb * 16, pk);
+                for (int c = 0; c < 32; ++c) sa[c] = sb2[c];
             }
-            {
-                float sv[32];
-                tmem_ld32(scol + warp * 32, sv);
-                tmem_wait_ld();
-                const int lim = min(lane, Lc - 1 - warp * 32);
-                uint32_t pk[16];
-#pragma unroll
-                for (int m = 0; m < 16; ++m) {
-                    const int c = 2 * m;
-                    const float a = (c <= lim) ? sv[c] * (pw(max(lane - c, 0)) * inv) : 0.f;
-                    const float b = (c + 1 <= lim) ? sv[c + 1] * (pw(max(lane - c - 1, 0)) * inv) : 0.f;
-                    pk[m] = pack_f16(a, b);
-                }
-                tmem_st16(scol + warp * 16, pk);
-            }
+            if (owner) {
 #pragma unroll 1
-            for (int cb = warp + 1; cb < 4; ++cb) tmem_st16(scol + cb * 16, zero);
-            st_shared_f32(rowscale_s + 4u * (uint32_t)(st * BC + j), exp2i(e));
+                for (int cb = q + 1; cb < 4; ++cb) tmem_st16(scol + cb * 16, zero);
+                cs.rowe[st][j] = (signed char)e;
+            }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bar(cs.p_full[st]));
+            mbar_arrive(bar(cs.pv_ready[st]));
         }
     } else if (warp < kVWarp0) {
         // ================= state warpgroup =================
+        // Thread r owns TMEM lane r: row r of the d_k x 64 state and token r
+        // of the chunk.  The fp32 state lives in the dKV accumulator as the
+        // sum of its two 64-column halves.  Per chunk:
+        //   fold: KV_i = sum of the halves; lambda^{B_{i+1}} KV_i / 2 is
+        //         written back into both halves for dKV_{i+1} to accumulate
+        //         onto (dKV_{i+1} may start right after);
+        //   copy: once Q_i KV_{i-1} has finished, a hi/lo bf16 copy of KV_i
+        //         for Q_{i+1} KV_i;
+        //   O2:   Q_i KV_{i-1} (hi + lo) into registers, freeing its columns;
+        //   out:  once P_i V_i has finished, o = 2^(e + f) O1 + lambda^(r+1) O2.
         const int w4 = warp - kStateWarp0;
-        const int r = w4 * 32 + lane;  // TMEM lane: d_k row / token row
+        const int r = w4 * 32 + lane;
         const uint32_t lane_off = (uint32_t)(w4 * 32) << 16;
         const uint32_t kvb = sb + kOffKVb;
-        const uint32_t vscale_s = smem_u32(&cs.vscale[0]);
-        float kv[DV];
-#pragma unroll
-        for (int c = 0; c < DV; ++c) kv[c] = 0.f;
+        const uint32_t tkv = tmem + lane_off + kColDKV;
+        const uint32_t to2 = tmem + lane_off + kColO2;
+        // TMA loads (thread 0 of the warpgroup).  Slot c & 1 of a ring is
+        // reloaded for chunk c once chunk c - 2 has released it: Q and K when
+        // Q KV and dKV of chunk c - 2 have finished (seen here at the copy
+        // step), V when its P V has finished (seen at the output step).
+        const bool loader = threadIdx.x == kStateWarp0 * 32;
+        int nq = 0, nk = 0, nv = 0;
+        auto load_qk = [&](int c) -> bool {
+            const int st = c & 1;
+            const uint32_t sph = (c >> 1) & 1;
+            const int y = t0 + c * BC;
+            if (!mbar_wait(bar(cs.empty_q[st]), sph ^ 1, abort_flag, kTimeoutNs)) return false;
+            mbar_arrive_expect_tx(bar(cs.full_q[st]), 2 * kHalf);
+            tma_load_2d(qslot(st), &tmQ, bar(cs.full_q[st]), h * D, y);
+            tma_load_2d(qslot(st) + kHalf, &tmQ, bar(cs.full_q[st]), h * D + 64, y);
+            ++nq;
+            if (!mbar_wait(bar(cs.empty_k[st]), sph ^ 1, abort_flag, kTimeoutNs)) return false;
+            mbar_arrive_expect_tx(bar(cs.full_k[st]), 2 * kHalf);
+            tma_load_2d(kslot(st), &tmK, bar(cs.full_k[st]), h * D, y);
+            tma_load_2d(kslot(st) + kHalf, &tmK, bar(cs.full_k[st]), h * D + 64, y);
+            ++nk;
+            return true;
+        };
+        auto load_v = [&](int c) -> bool {
+            const int st = c & 1;
+            const uint32_t sph = (c >> 1) & 1;
+            if (!mbar_wait(bar(cs.empty_v[st]), sph ^ 1, abort_flag, kTimeoutNs)) return false;
+            mbar_arrive_expect_tx(bar(cs.full_v[st]), kHalf);
+            tma_load_2d(vslot(st), &tmV, bar(cs.full_v[st]), h * D + vs * DV, t0 + c * BC);
+            ++nv;
+            return true;
+        };
+        if (loader) {
+            tma_prefetch_desc(&tmQ);
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
+            for (int c = 0; c < min(nch, 2); ++c)
+                if (!load_qk(c) || !load_v(c)) break;
+        }
+        __syncwarp();
         // KV_{-1} = 0
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
@@ -439,86 +513,159 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             st_shared_v4(kvb + kHalf + r * 128 + c * 16, 0u, 0u, 0u, 0u);
         }
         fence_proxy_async_smem();
-        mbar_arrive(bar(cs.kv_full));
+        mbar_arrive(bar(cs.o2_ready));   // Q_0 KV_{-1} may go
+        mbar_arrive(bar(cs.dkv_ready));  // dKV_0 overwrites the accumulator
 
         for (int i = 0; i < nch; ++i) {
             const int st = i & 1;
             const uint32_t sph = (i >> 1) & 1, ph = i & 1;
             const int Lc = min(BC, L - i * BC);
-            // ---- KV_i = lambda^{Lc} KV_{i-1} + dKV_hi + dKV_lo ----
+            const bool last = i + 1 == nch;
+            // ---- fold ----
             if (!warp_wait(bar(cs.dkv_full), ph, abort_flag)) break;
             tc_fence_after();
-            const float dec = pw(Lc);
+            float kv[DV];
+            tmem_ld32(tkv, *reinterpret_cast<float(*)[32]>(&kv[0]));
+            tmem_ld32(tkv + 32, *reinterpret_cast<float(*)[32]>(&kv[32]));
+            tmem_wait_ld();
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                float a[16], b[16];
-                tmem_ld16(tmem + lane_off + kColDKV + q * 16, a);
-                tmem_ld16(tmem + lane_off + kColDKV + 64 + q * 16, b);
+            for (int hh = 0; hh < 4; ++hh) {
+                float b[16];
+                tmem_ld16(tkv + 64 + 16 * hh, b);
                 tmem_wait_ld();
 #pragma unroll
-                for (int c = 0; c < 16; ++c)
-                    kv[q * 16 + c] = fmaf(dec, kv[q * 16 + c], a[c] + b[c]);
+                for (int c = 0; c < 8; ++c) {
+                    const float2 x = f2_add(make_float2(kv[16 * hh + 2 * c], kv[16 * hh + 2 * c + 1]),
+                                            make_float2(b[2 * c], b[2 * c + 1]));
+                    kv[16 * hh + 2 * c] = x.x;
+                    kv[16 * hh + 2 * c + 1] = x.y;
+                }
+            }
+            if (!last) {
+                const float dh = 0.5f * pw(min(BC, L - (i + 1) * BC));
+                const float2 d2 = make_float2(dh, dh);
+#pragma unroll
+                for (int hh = 0; hh < 4; ++hh) {
+                    uint32_t w[16];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const float2 x =
+                            f2_mul(make_float2(kv[16 * hh + 2 * c], kv[16 * hh + 2 * c + 1]), d2);
+                        w[2 * c] = __float_as_uint(x.x);
+                        w[2 * c + 1] = __float_as_uint(x.y);
+                    }
+                    tmem_st16(tkv + 16 * hh, w);
+                    tmem_st16(tkv + 64 + 16 * hh, w);
+                }
+                tmem_wait_st();
+            } else if (final_state) {
+                float4 *dst = reinterpret_cast<float4 *>(
+                    final_state + (((long)s * H + h) * D + r) * D + vs * DV);
+#pragma unroll
+                for (int c = 0; c < DV / 4; ++c)
+                    dst[c] = make_float4(kv[4 * c], kv[4 * c + 1], kv[4 * c + 2], kv[4 * c + 3]);
             }
             tc_fence_before();
-            mbar_arrive(bar(cs.dkv_free));
-            // ---- hi/lo copy of KV_i for the next chunk's Q KV (after O2_i read KV_{i-1}) ----
-            if (!warp_wait(bar(cs.kv_free), ph, abort_flag)) break;
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const uint32_t phys = (uint32_t)(c ^ (r & 7));
-                uint32_t hi[4], lo[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    // hi = x with the low 16 bits cleared (a bf16, exact);
-                    // lo = x - hi (exact in fp32), also truncated to bf16:
-                    // hi + lo = x to about 2^-14 relative
-                    const uint32_t ua = __float_as_uint(kv[8 * c + 2 * q]);
-                    const uint32_t ub = __float_as_uint(kv[8 * c + 2 * q + 1]);
-                    hi[q] = __byte_perm(ua, ub, 0x7632);
-                    const float la = __uint_as_float(ua) - __uint_as_float(ua & 0xffff0000u);
-                    const float lb = __uint_as_float(ub) - __uint_as_float(ub & 0xffff0000u);
-                    lo[q] = __byte_perm(__float_as_uint(la), __float_as_uint(lb), 0x7632);
-                }
-                st_shared_v4(kvb + r * 128 + phys * 16, hi[0], hi[1], hi[2], hi[3]);
-                st_shared_v4(kvb + kHalf + r * 128 + phys * 16, lo[0], lo[1], lo[2], lo[3]);
-            }
-            fence_proxy_async_smem();
-            mbar_arrive(bar(cs.kv_full));
-            // ---- output: o_j = 2^(e_j + f) O1_j + lambda^(j+1) (O2hi_j + O2lo_j) ----
-            if (!warp_wait(bar(cs.o_full), ph, abort_flag)) break;
-            if (!warp_wait(bar(cs.p_full[st]), sph, abort_flag)) break;  // orders rowscale
+            mbar_arrive(bar(cs.dkv_ready));
+            // ---- copy ----
+            if (!warp_wait(bar(cs.o2_full), ph, abort_flag)) break;
             tc_fence_after();
-            const float s1 = ld_shared_f32(rowscale_s + 4u * (uint32_t)(st * BC + r)) *
+            if (!last) {
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    // hi = x with the low 16 bits cleared (a bf16, exact);
+                    // lo = x - hi (exact in fp32), also truncated:
+                    // hi + lo = x to about 2^-14 relative
+                    const uint32_t phys = (uint32_t)(c ^ (r & 7));
+                    uint32_t hi[4], lo[4];
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        const uint32_t ua = __float_as_uint(kv[8 * c + 2 * m]);
+                        const uint32_t ub = __float_as_uint(kv[8 * c + 2 * m + 1]);
+                        hi[m] = __byte_perm(ua, ub, 0x7632);
+                        const float2 l2 =
+                            f2_sub(make_float2(__uint_as_float(ua), __uint_as_float(ub)),
+                                   make_float2(__uint_as_float(ua & 0xffff0000u),
+                                               __uint_as_float(ub & 0xffff0000u)));
+                        lo[m] = __byte_perm(__float_as_uint(l2.x), __float_as_uint(l2.y), 0x7632);
+                    }
+                    st_shared_v4(kvb + r * 128 + phys * 16, hi[0], hi[1], hi[2], hi[3]);
+                    st_shared_v4(kvb + kHalf + r * 128 + phys * 16, lo[0], lo[1], lo[2], lo[3]);
+                }
+                fence_proxy_async_smem();
+            }
+            if (loader && i + 2 < nch) load_qk(i + 2);
+            __syncwarp();
+            // ---- O2 ----
+            float o2[DV];
+            tmem_ld32(to2, *reinterpret_cast<float(*)[32]>(&o2[0]));
+            tmem_ld32(to2 + 32, *reinterpret_cast<float(*)[32]>(&o2[32]));
+            tmem_wait_ld();
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                float b[32];
+                tmem_ld32(to2 + 64 + 32 * hh, b);
+                tmem_wait_ld();
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    const float2 x = f2_add(make_float2(o2[32 * hh + 2 * c], o2[32 * hh + 2 * c + 1]),
+                                            make_float2(b[2 * c], b[2 * c + 1]));
+                    o2[32 * hh + 2 * c] = x.x;
+                    o2[32 * hh + 2 * c + 1] = x.y;
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(bar(cs.o2_ready));
+            // ---- out: o_r = 2^(e_r + f) O1_r + lambda^(r+1) O2_r ----
+            if (!warp_wait(bar(cs.o_full[st]), sph, abort_flag)) break;
+            if (!warp_wait(bar(cs.pv_ready[st]), sph, abort_flag)) break;  // orders the scales
+            tc_fence_after();
+            if (loader && i + 2 < nch) load_v(i + 2);
+            __syncwarp();
+            const float s1 = exp2i((int)*reinterpret_cast<volatile signed char *>(&cs.rowe[st][r])) *
                              ld_shared_f32(vscale_s + 4u * (uint32_t)(i & 3));
             const float qf = pw(r + 1);
+            const float2 s12 = make_float2(s1, s1), qf2 = make_float2(qf, qf);
             uint4 *orow = reinterpret_cast<uint4 *>(out + ((long)(t0 + i * BC + r) * H + h) * D +
                                                     vs * DV);
-#pragma unroll 1
-            for (int g = 0; g < 8; ++g) {
-                float a[8], b[8], c2[8];
-                tmem_ld8(tmem + lane_off + st * 128 + 64 + g * 8, a);
-                tmem_ld8(tmem + lane_off + kColO2 + g * 8, b);
-                tmem_ld8(tmem + lane_off + kColO2 + 64 + g * 8, c2);
+#pragma unroll
+            for (int hh = 0; hh < 4; ++hh) {
+                float a[16];
+                tmem_ld16(tmem + lane_off + st * 128 + 64 + 16 * hh, a);
                 tmem_wait_ld();
-                if (g == 7) {  // all TMEM reads of this chunk are done
+                if (hh == 3) {  // all TMEM reads of this chunk are done
                     tc_fence_before();
-                    mbar_arrive(bar(cs.o2_free));
                     mbar_arrive(bar(cs.s_free[st]));
                 }
-                uint32_t w[4];
+                uint32_t w[8];
 #pragma unroll
-                for (int m = 0; m < 4; ++m)
-                    w[m] = pack_bf16(fmaf(qf, b[2 * m] + c2[2 * m], s1 * a[2 * m]),
-                                     fmaf(qf, b[2 * m + 1] + c2[2 * m + 1], s1 * a[2 * m + 1]));
-                if (r < Lc) orow[g] = make_uint4(w[0], w[1], w[2], w[3]);
+                for (int m = 0; m < 8; ++m) {
+                    const float2 y = f2_fma(
+                        qf2, make_float2(o2[16 * hh + 2 * m], o2[16 * hh + 2 * m + 1]),
+                        f2_mul(s12, make_float2(a[2 * m], a[2 * m + 1])));
+                    w[m] = pack_bf16(y.x, y.y);
+                }
+                if (r < Lc) {
+                    orow[2 * hh] = make_uint4(w[0], w[1], w[2], w[3]);
+                    orow[2 * hh + 1] = make_uint4(w[4], w[5], w[6], w[7]);
+                }
             }
         }
-        if (final_state && !*abort_flag) {
+        if (loader) {  // never leave with a load still landing in shared memory
+            int no_abort = 0;
+            for (int c = max(0, nq - 2); c < nq; ++c)
+                mbar_wait(bar(cs.full_q[c & 1]), (c >> 1) & 1, &no_abort, kTimeoutNs);
+            for (int c = max(0, nk - 2); c < nk; ++c)
+                mbar_wait(bar(cs.full_k[c & 1]), (c >> 1) & 1, &no_abort, kTimeoutNs);
+            for (int c = max(0, nv - 2); c < nv; ++c)
+                mbar_wait(bar(cs.full_v[c & 1]), (c >> 1) & 1, &no_abort, kTimeoutNs);
+        }
+        __syncwarp();
+        if (nch == 0 && final_state) {  // empty sequence: the state stays zero
             float4 *dst = reinterpret_cast<float4 *>(final_state + (((long)s * H + h) * D + r) * D +
                                                      vs * DV);
 #pragma unroll
-            for (int c = 0; c < DV / 4; ++c)
-                dst[c] = make_float4(kv[4 * c], kv[4 * c + 1], kv[4 * c + 2], kv[4 * c + 3]);
+            for (int c = 0; c < DV / 4; ++c) dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
     } else if (warp < kVWarp0 + 4) {
         // ================= V-tile warpgroup =================
@@ -531,7 +678,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         const int w4 = warp - kVWarp0;
         const int vr = w4 * 32 + lane;
         const uint32_t vha = sb + kOffVhat;
-        const uint32_t vscale_s = smem_u32(&cs.vscale[0]);
         for (int i = 0; i < nch; ++i) {
             const int st = i & 1;
             if (i > 0 && !warp_wait(bar(cs.dkv_full), (i - 1) & 1, abort_flag)) break;
@@ -539,24 +685,26 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             const int Lc = min(BC, L - i * BC);
             const bool live = vr < Lc;
             const uint32_t row = vslot(st) + vr * 128;
-            uint4 x[8];
-#pragma unroll
-            for (int c = 0; c < 8; ++c) x[c] = ld_shared_v4(row + (uint32_t)((c + vr) & 7) * 16);
-            // ---- 1: Vhat.  lambda^(Lc-1-l) split as g_hi + g_lo (bf16
-            // each) so that the packed bf16 FMAs give hi + lo = v g to ~16 bits.
+            // ---- 1: Vhat (and max |v| of the row).  lambda^(Lc-1-l) split as
+            // g_hi + g_lo (bf16 each) so that the packed bf16 FMAs give
+            // hi + lo = v g to ~16 bits.  The loops stay rolled: the three
+            // roles of an SM sub-partition share its instruction cache.
+            uint32_t mbits = 0;  // max |v| as packed bf16 magnitudes
             {
                 const float g = live ? pw(Lc - 1 - vr) : 0.f;
                 const __nv_bfloat16 ghb = __float2bfloat16_rn(g);
                 const __nv_bfloat16 glb = __float2bfloat16_rn(g - __bfloat162float(ghb));
                 const __nv_bfloat162 gh = __halves2bfloat162(ghb, ghb);
                 const __nv_bfloat162 gl = __halves2bfloat162(glb, glb);
-#pragma unroll
+#pragma unroll 1
                 for (int c = 0; c < 8; ++c) {
                     const uint32_t ch = (uint32_t)((c + vr) & 7) * 16;
-                    const uint32_t w[4] = {x[c].x, x[c].y, x[c].z, x[c].w};
+                    const uint4 x = ld_shared_v4(row + ch);
+                    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
                     uint32_t hi[4], lo[4];
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
+                        mbits = __vmaxu2(mbits, w[q] & 0x7fff7fffu);
                         const __nv_bfloat162 v2 = *reinterpret_cast<const __nv_bfloat162 *>(&w[q]);
                         const __nv_bfloat162 h2 = __hmul2(v2, gh);
                         // exact residual of the rounded product, plus the g_lo term
@@ -569,19 +717,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
                     st_shared_v4(vha + kHalf + vr * 128 + ch, lo[0], lo[1], lo[2], lo[3]);
                 }
                 fence_proxy_async_smem();
-                mbar_arrive(bar(cs.vhat_full));
+                mbar_arrive(bar(cs.dkv_ready));
             }
             // ---- 2: fp16 V for P V
-            uint32_t mbits = 0;  // max |v| as packed bf16 magnitudes
-            if (live) {
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    mbits = __vmaxu2(mbits, x[c].x & 0x7fff7fffu);
-                    mbits = __vmaxu2(mbits, x[c].y & 0x7fff7fffu);
-                    mbits = __vmaxu2(mbits, x[c].z & 0x7fff7fffu);
-                    mbits = __vmaxu2(mbits, x[c].w & 0x7fff7fffu);
-                }
-            }
+            if (!live) mbits = 0;
             float m = fmaxf(__uint_as_float(mbits << 16), __uint_as_float(mbits & 0xffff0000u));
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -592,30 +731,32 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             const float mt = fmaxf(fmaxf(ld_shared_f32(vm), ld_shared_f32(vm + 4)),
                                    fmaxf(ld_shared_f32(vm + 8), ld_shared_f32(vm + 12)));
             // no scale when the tile is comfortably inside fp16's normal
-            // range, else 2^-f with max |v| 2^-f in [2^14, 2^15)
+            // range, else 2^-f with max |v| 2^-f in [2^14, 2^15); rows past
+            // the chunk end become zero
             const int f = (mt <= 1024.f && mt >= 0.0625f) ? 0 : fp16_scale_exp(mt, 14);
             if (threadIdx.x == kVWarp0 * 32)
                 st_shared_f32(vscale_s + 4u * (uint32_t)(i & 3), exp2i(f));
             const float sc = live ? exp2i(-f) : 0.f;
-            const bool unscaled = f == 0 && live;
-#pragma unroll
+            const float2 sc2 = make_float2(sc, sc);
+#pragma unroll 1
             for (int c = 0; c < 8; ++c) {
                 const uint32_t ch = (uint32_t)((c + vr) & 7) * 16;
-                const uint32_t w[4] = {x[c].x, x[c].y, x[c].z, x[c].w};
+                const uint4 x = ld_shared_v4(row + ch);
+                const uint32_t w[4] = {x.x, x.y, x.z, x.w};
                 uint32_t hv[4];
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    hv[q] = unscaled ? pack_f16(__uint_as_float(w[q] << 16),
-                                                __uint_as_float(w[q] & 0xffff0000u))
-                                     : pack_f16(__uint_as_float(w[q] << 16) * sc,
-                                                __uint_as_float(w[q] & 0xffff0000u) * sc);
+                for (int q = 0; q < 4; ++q) {
+                    const float2 y = f2_mul(make_float2(__uint_as_float(w[q] << 16),
+                                                        __uint_as_float(w[q] & 0xffff0000u)),
+                                            sc2);
+                    hv[q] = pack_f16(y.x, y.y);
+                }
                 st_shared_v4(row + ch, hv[0], hv[1], hv[2], hv[3]);
             }
             fence_proxy_async_smem();
-            mbar_arrive(bar(cs.vconv_full[st]));
+            mbar_arrive(bar(cs.pv_ready[st]));
         }
     }
-    // warps 14 and 15 have no role
 
     // ---- teardown ----
     tc_fence_before();

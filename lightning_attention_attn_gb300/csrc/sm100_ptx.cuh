@@ -87,6 +87,43 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// ------------------------------------------------------- packed fp32 pairs
+// One instruction for two IEEE fp32 operations (round to nearest even, the
+// same results as the scalar forms), sm_100 and later.
+__device__ __forceinline__ float2 f2_add(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+__device__ __forceinline__ float2 f2_sub(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+__device__ __forceinline__ float2 f2_mul(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+// a * b + c
+__device__ __forceinline__ float2 f2_fma(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mov.b64 rc, {%6, %7};\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_prefetch_desc(const void *tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
@@ -179,78 +216,34 @@ __device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem
         : "memory");
 }
 
-// Eight MMAs accumulating into one TMEM tile (D = sum_k A_k B_k + D when
-// acc != 0, else the first one overwrites D), from one inline-asm block so the issuing thread spends
-// two adds per instruction.  Operand k starts at the base descriptor plus a
-// fixed offset in 16-byte units: for a K-major 128-byte-swizzled operand of
-// 128 K values in two 64-wide halves (16 KB apart) the offsets are
-// 0, 2, 4, 6 (32 bytes into the swizzle row) then 1024 + the same; for an
-// MN-major operand, 16 K rows of 128 bytes = 128 units per step.
-#define LA_MMA8_BODY(A1, A2, A3, A4, A5, A6, A7, B1, B2, B3, B4, B5, B6, B7)                   \
-    "{\n\t.reg .pred pf, pt;\n\t.reg .b64 da, db;\n\t"                                      \
-    "setp.ne.b32 pf, %4, 0;\n\tsetp.eq.b32 pt, 0, 0;\n\t"                                    \
-    "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, pf;\n\t"                            \
-    "add.s64 da, %1, " A1 ";\n\tadd.s64 db, %2, " B1 ";\n\t"                                  \
-    "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, pt;\n\t"                            \
-    "add.s64 da, %1, " A2 ";\n\tadd.s64 db, %2, " B2 ";\n\t"                                  \
-    "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, pt;\n\t"                            \
-    "add.s64 da, %1, " A3 ";\n\tadd.s64 db, %2, " B3 ";\n\t"                                  \
-    "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, pt;\n\t"                            \
-    "add.s64 da, %1, " A4 ";\n\tadd.s64 db, %2, " B4 ";\n\t"                                  \
-    "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, pt;\n\t"                            \
-    "add.s64 da, %1, " A5 ";\n\tadd.s64 db, %2, " B5 ";\n\t"                                  \
-    "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, pt;\n\t"                            \
-    "add.s64 da, %1, " A6 ";\n\tadd.s64 db, %2, " B6 ";\n\t"                                  \
-    "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, pt;\n\t"                            \
-    "add.s64 da, %1, " A7 ";\n\tadd.s64 db, %2, " B7 ";\n\t"                                  \
-    "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, pt;\n\t}"
-
-// A K-major, B K-major (Q K^T)
-__device__ __forceinline__ void mma8_k_k(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
-                                          uint32_t acc = 0) {
-    asm volatile(LA_MMA8_BODY("2", "4", "6", "1024", "1026", "1028", "1030",
-                              "2", "4", "6", "1024", "1026", "1028", "1030")
-                 ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc)
-                 : "memory");
+// A group of eight MMAs over K = 128 into one TMEM tile: D = sum_k A_k B_k
+// (plus the old D when acc != 0).  Each tcgen05.mma site compiles to a loop
+// over the issuing lanes that moves their operands into uniform registers,
+// so the K steps run in a rolled loop around a single site: short code for
+// an instruction cache shared by every role of an SM sub-partition.
+// K step k starts at the base descriptor plus (k & 3) * s1 + (k >> 2) * s2
+// (16-byte units): a K-major 128-byte-swizzled operand of 128 K values in
+// two 64-wide halves 16 KB apart has s1 = 2 (32 bytes into the swizzle row),
+// s2 = 1024; an MN-major operand (16 K rows of 128 bytes per step) has
+// s1 = 128, s2 = 512.
+__device__ __forceinline__ void mma_group_ss(uint32_t d, uint64_t a, uint32_t as1, uint32_t as2,
+                                             uint64_t b, uint32_t bs1, uint32_t bs2,
+                                             uint32_t idesc, uint32_t acc) {
+#pragma unroll 1
+    for (uint32_t k = 0; k < 8; ++k) {
+        const uint64_t da = a + (uint64_t)((k & 3u) * as1 + (k >> 2) * as2);
+        const uint64_t db = b + (uint64_t)((k & 3u) * bs1 + (k >> 2) * bs2);
+        mma_bf16(d, da, db, idesc, acc | k);
+    }
 }
-// A K-major, B MN-major (Q [KV_hi | KV_lo])
-__device__ __forceinline__ void mma8_k_mn(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
-                                          uint32_t acc = 0) {
-    asm volatile(LA_MMA8_BODY("2", "4", "6", "1024", "1026", "1028", "1030",
-                              "128", "256", "384", "512", "640", "768", "896")
-                 ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc)
-                 : "memory");
-}
-// A MN-major, B MN-major (K^T [Vhat_hi | Vhat_lo])
-__device__ __forceinline__ void mma8_mn_mn(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
-                                          uint32_t acc = 0) {
-    asm volatile(LA_MMA8_BODY("128", "256", "384", "512", "640", "768", "896",
-                              "128", "256", "384", "512", "640", "768", "896")
-                 ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc)
-                 : "memory");
-}
-// A from TMEM (8 columns per step), B MN-major (P V)
-__device__ __forceinline__ void mma8_t_mn(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc) {
-    asm volatile(
-        "{\n\t.reg .pred pf, pt;\n\t.reg .b32 ta;\n\t.reg .b64 db;\n\t"
-        "setp.ne.b32 pf, 0, 0;\n\tsetp.eq.b32 pt, 0, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, pf;\n\t"
-        "add.u32 ta, %1, 8;\n\tadd.s64 db, %2, 128;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %3, pt;\n\t"
-        "add.u32 ta, %1, 16;\n\tadd.s64 db, %2, 256;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %3, pt;\n\t"
-        "add.u32 ta, %1, 24;\n\tadd.s64 db, %2, 384;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %3, pt;\n\t"
-        "add.u32 ta, %1, 32;\n\tadd.s64 db, %2, 512;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %3, pt;\n\t"
-        "add.u32 ta, %1, 40;\n\tadd.s64 db, %2, 640;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %3, pt;\n\t"
-        "add.u32 ta, %1, 48;\n\tadd.s64 db, %2, 768;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %3, pt;\n\t"
-        "add.u32 ta, %1, 56;\n\tadd.s64 db, %2, 896;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %3, pt;\n\t}"
-        ::"r"(d), "r"(a_tmem), "l"(b), "r"(idesc)
-        : "memory");
+constexpr uint32_t kKMajorS1 = 2, kKMajorS2 = 1024, kMNMajorS1 = 128, kMNMajorS2 = 512;
+// The same with A read from TMEM (8 columns per K step of 16 16-bit values)
+// and B MN-major.
+__device__ __forceinline__ void mma_group_ts(uint32_t d, uint32_t a_tmem, uint64_t b,
+                                             uint32_t idesc, uint32_t acc) {
+#pragma unroll 1
+    for (uint32_t k = 0; k < 8; ++k)
+        mma_bf16_tmem_a(d, a_tmem + 8u * k, b + (uint64_t)(128u * k), idesc, acc | k);
 }
 
 // The mbarrier completes one arrival when every tcgen05 operation this
@@ -308,6 +301,20 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&u)[16
         "r"(u[0]), "r"(u[1]), "r"(u[2]), "r"(u[3]), "r"(u[4]), "r"(u[5]), "r"(u[6]), "r"(u[7]),
         "r"(u[8]), "r"(u[9]), "r"(u[10]), "r"(u[11]), "r"(u[12]), "r"(u[13]), "r"(u[14]),
         "r"(u[15])
+        : "memory");
+}
+// 32 lanes x 32 consecutive 32-bit columns from registers.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&u)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(
+            taddr),
+        "r"(u[0]), "r"(u[1]), "r"(u[2]), "r"(u[3]), "r"(u[4]), "r"(u[5]), "r"(u[6]), "r"(u[7]),
+        "r"(u[8]), "r"(u[9]), "r"(u[10]), "r"(u[11]), "r"(u[12]), "r"(u[13]), "r"(u[14]),
+        "r"(u[15]), "r"(u[16]), "r"(u[17]), "r"(u[18]), "r"(u[19]), "r"(u[20]), "r"(u[21]),
+        "r"(u[22]), "r"(u[23]), "r"(u[24]), "r"(u[25]), "r"(u[26]), "r"(u[27]), "r"(u[28]),
+        "r"(u[29]), "r"(u[30]), "r"(u[31])
         : "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() {

@@ -241,11 +241,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // broadcast so that the compiler sees a warp-uniform TMEM address
+    // An allocation of all 512 columns can only start at lane 0, column 0.
+    // The MMA issuers use that constant (their operands must be provably
+    // warp-uniform to issue quickly); the TMEM loads and stores use the
+    // allocated address.
+    constexpr uint32_t tmem_mma = 0;
     const uint32_t tmem = __shfl_sync(0xffffffffu, cs.tmem_base, 0);
     volatile int *abort_flag = &cs.abort;
+    const bool tmem_ok = tmem == tmem_mma;  // never expected to fail
 
-    if (warp == kMmaWarpA) {
+    if (!tmem_ok) {
+        // leave TMEM alone; the error word is raised below
+    } else if (warp == kMmaWarpA) {
         // ================= MMA stream A: S and P V =================
         // Per chunk i: S_{i+1}, then P_i V_i, so that the mask warps turn
         // S_{i+1} into P_{i+1} while the tensor core runs P_i V_i and stream
@@ -258,10 +265,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             // buffer st is free once chunk i-2's output has read its O1
             if (!warp_wait(bar(cs.s_free[st]), sph ^ 1, abort_flag)) return false;
             tc_fence_after();
-            if (lane == 0) {
-                mma_group_ss(tmem + st * 128, sdesc_sw128(qslot(st), 16, 1024), kKMajorS1,
-                             kKMajorS2, sdesc_sw128(kslot(st), 16, 1024), kKMajorS1, kKMajorS2,
-                             kIdescS, 0u);
+            const uint64_t dq = sdesc_sw128(qslot(st), 16, 1024);
+            const uint64_t dk = sdesc_sw128(kslot(st), 16, 1024);
+            if (elect_one()) {
+                mma_group_ss<kKMajorS1, kKMajorS2, kKMajorS1, kKMajorS2>(tmem_mma + st * 128, dq, dk,
+                                                                         kIdescS, 0u);
                 mma_commit(bar(cs.s_full[st]));
                 mma_commit(bar(cs.empty_q[st]));
                 mma_commit(bar(cs.empty_k[st]));
@@ -278,16 +286,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             // into its second half)
             if (!warp_wait(bar(cs.pv_ready[st]), sph, abort_flag)) break;
             tc_fence_after();
-            if (lane == 0) {
-                mma_group_ts(tmem + st * 128 + 64, tmem + st * 128,
-                             sdesc_sw128(vslot(st), kHalf, 1024), kIdescPV, 0u);
+            const uint64_t dv = sdesc_sw128(vslot(st), kHalf, 1024);
+            if (elect_one()) {
+                mma_group_ts(tmem_mma + st * 128 + 64, tmem_mma + st * 128, dv, kIdescPV, 0u);
                 mma_commit(bar(cs.o_full[st]));
                 mma_commit(bar(cs.empty_v[st]));
             }
             __syncwarp();
         }
         // All MMAs must be finished before TMEM is released.
-        if (lane == 0) mma_commit(bar(cs.done_a));
+        if (elect_one()) mma_commit(bar(cs.done_a));
         __syncwarp();
         int no_abort = 0;
         warp_wait(bar(cs.done_a), 0, &no_abort);
@@ -302,10 +310,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             if (!warp_wait(bar(cs.full_k[st]), sph, abort_flag)) break;
             if (!warp_wait(bar(cs.dkv_ready), ph, abort_flag)) break;
             tc_fence_after();
-            if (lane == 0) {
-                mma_group_ss(tmem + kColDKV, sdesc_sw128(kslot(st), kHalf, 1024), kMNMajorS1,
-                             kMNMajorS2, sdesc_sw128(vha, kHalf, 1024), kMNMajorS1, kMNMajorS2,
-                             kIdescKV, i > 0 ? 1u : 0u);
+            const uint64_t dk = sdesc_sw128(kslot(st), kHalf, 1024);
+            const uint64_t dvh = sdesc_sw128(vha, kHalf, 1024);
+            if (elect_one()) {
+                mma_group_ss<kMNMajorS1, kMNMajorS2, kMNMajorS1, kMNMajorS2>(
+                    tmem_mma + kColDKV, dk, dvh, kIdescKV, i > 0 ? 1u : 0u);
                 mma_commit(bar(cs.dkv_full));
                 mma_commit(bar(cs.empty_k[st]));
             }
@@ -314,16 +323,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             if (!warp_wait(bar(cs.full_q[st]), sph, abort_flag)) break;
             if (!warp_wait(bar(cs.o2_ready), ph, abort_flag)) break;
             tc_fence_after();
-            if (lane == 0) {
-                mma_group_ss(tmem + kColO2, sdesc_sw128(qslot(st), 16, 1024), kKMajorS1,
-                             kKMajorS2, sdesc_sw128(kvb, kHalf, 1024), kMNMajorS1, kMNMajorS2,
-                             kIdescO2, 0u);
+            const uint64_t dq = sdesc_sw128(qslot(st), 16, 1024);
+            const uint64_t dkv = sdesc_sw128(kvb, kHalf, 1024);
+            if (elect_one()) {
+                mma_group_ss<kKMajorS1, kKMajorS2, kMNMajorS1, kMNMajorS2>(tmem_mma + kColO2, dq, dkv,
+                                                                           kIdescO2, 0u);
                 mma_commit(bar(cs.o2_full));
                 mma_commit(bar(cs.empty_q[st]));
             }
             __syncwarp();
         }
-        if (lane == 0) mma_commit(bar(cs.done_b));
+        if (elect_one()) mma_commit(bar(cs.done_b));
         __syncwarp();
         int no_abort = 0;
         warp_wait(bar(cs.done_b), 0, &no_abort);
@@ -765,7 +775,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
-    if (threadIdx.x == 0 && cs.abort) atomicOr(&g_tc_error, 1u);
+    if (threadIdx.x == 0 && (cs.abort || !tmem_ok)) atomicOr(&g_tc_error, 1u);
 }
 
 // ------------------------------------------------------------ host side

@@ -216,34 +216,43 @@ __device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem
         : "memory");
 }
 
-// A group of eight MMAs over K = 128 into one TMEM tile: D = sum_k A_k B_k
-// (plus the old D when acc != 0).  Each tcgen05.mma site compiles to a loop
-// over the issuing lanes that moves their operands into uniform registers,
-// so the K steps run in a rolled loop around a single site: short code for
-// an instruction cache shared by every role of an SM sub-partition.
-// K step k starts at the base descriptor plus (k & 3) * s1 + (k >> 2) * s2
-// (16-byte units): a K-major 128-byte-swizzled operand of 128 K values in
-// two 64-wide halves 16 KB apart has s1 = 2 (32 bytes into the swizzle row),
-// s2 = 1024; an MN-major operand (16 K rows of 128 bytes per step) has
-// s1 = 128, s2 = 512.
-__device__ __forceinline__ void mma_group_ss(uint32_t d, uint64_t a, uint32_t as1, uint32_t as2,
-                                             uint64_t b, uint32_t bs1, uint32_t bs2,
-                                             uint32_t idesc, uint32_t acc) {
-#pragma unroll 1
-    for (uint32_t k = 0; k < 8; ++k) {
-        const uint64_t da = a + (uint64_t)((k & 3u) * as1 + (k >> 2) * as2);
-        const uint64_t db = b + (uint64_t)((k & 3u) * bs1 + (k >> 2) * bs2);
-        mma_bf16(d, da, db, idesc, acc | k);
-    }
+// One lane of a converged warp (the whole warp calls this; the lanes agree
+// on every operand).
+__device__ __forceinline__ bool elect_one() {
+    uint32_t p;
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\tselp.u32 %0, 1, 0, e;\n\t}"
+        : "=r"(p));
+    return p != 0;
 }
+
+// A group of eight MMAs over K = 128 into one TMEM tile: D = sum_k A_k B_k
+// (plus the old D when acc != 0).  Call it from the elected lane with
+// operands the whole warp computed: tcgen05.mma has per-thread semantics, so
+// every site compiles to a loop over the issuing lanes, which stays short
+// (and the issue rate keeps up with the tensor pipe) only when the operands
+// are warp-uniform values.
+// K step k starts at the base descriptor plus (k & 3) * S1 + (k >> 2) * S2
+// (16-byte units): a K-major 128-byte-swizzled operand of 128 K values in
+// two 64-wide halves 16 KB apart has S1 = 2 (32 bytes into the swizzle row),
+// S2 = 1024; an MN-major operand (16 K rows of 128 bytes per step) has
+// S1 = 128, S2 = 512.
 constexpr uint32_t kKMajorS1 = 2, kKMajorS2 = 1024, kMNMajorS1 = 128, kMNMajorS2 = 512;
+template <uint32_t AS1, uint32_t AS2, uint32_t BS1, uint32_t BS2>
+__device__ __forceinline__ void mma_group_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                             uint32_t acc) {
+#pragma unroll
+    for (uint32_t k = 0; k < 8; ++k)
+        mma_bf16(d, a + (uint64_t)((k & 3u) * AS1 + (k >> 2) * AS2),
+                 b + (uint64_t)((k & 3u) * BS1 + (k >> 2) * BS2), idesc, k ? 1u : acc);
+}
 // The same with A read from TMEM (8 columns per K step of 16 16-bit values)
 // and B MN-major.
 __device__ __forceinline__ void mma_group_ts(uint32_t d, uint32_t a_tmem, uint64_t b,
                                              uint32_t idesc, uint32_t acc) {
-#pragma unroll 1
+#pragma unroll
     for (uint32_t k = 0; k < 8; ++k)
-        mma_bf16_tmem_a(d, a_tmem + 8u * k, b + (uint64_t)(128u * k), idesc, acc | k);
+        mma_bf16_tmem_a(d, a_tmem + 8u * k, b + (uint64_t)(128u * k), idesc, k ? 1u : acc);
 }
 
 // The mbarrier completes one arrival when every tcgen05 operation this

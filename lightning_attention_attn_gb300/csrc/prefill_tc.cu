@@ -100,6 +100,7 @@ constexpr uint32_t kOffCtrl = kOffKVb + 2 * kHalf;
 
 struct Ctrl {
     alignas(16) float pw[BC + 4];  // pw[e] = lambda^e, e = 0..BC
+    float pwt[64];                 // pwt[32 + d] = lambda^d for d >= 0, 0 for d < 0
     uint64_t full_q[2], full_k[2], full_v[2], empty_q[2], empty_k[2], empty_v[2];
     uint64_t s_full[2], s_free[2], pv_ready[2], vmax_ready[2], pair[2], o_full[2];
     uint64_t o2_full, o2_ready, dkv_full, dkv_ready, done_a, done_b;
@@ -234,6 +235,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         fence_mbar_init();
     }
     for (int e = threadIdx.x; e <= BC; e += kThreads) cs.pw[e] = powf(lam, (float)e);
+    if (threadIdx.x < 64) cs.pwt[threadIdx.x] = threadIdx.x < 32 ? 0.f : powf(lam, (float)(threadIdx.x - 32));
     if (warp == 0) {
         tmem_alloc(smem_u32(&cs.tmem_base), kTmemCols);
         tmem_relinquish();
@@ -343,72 +345,91 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         // (rows 32q .. 32q + 31) hold that quadrant's 32-column S blocks
         // cb <= q in registers, two at most per warp (quadrants 2 and 3 are
         // split between an owner warp, which has the diagonal block, and a
-        // helper warp).  p_jl = S_jl lambda^(j-l) for l <= j, l < Lc, else 0.
-        // P goes to TMEM as fp16 scaled by 2^-e_j, a power of two chosen from
-        // an upper bound of the row's |p| (max |S| of each block times the
-        // block's largest decay factor; the two warps of a split quadrant
-        // exchange their partial bounds) so that the row sits below 2^12: no
-        // overflow, and 11 significant bits for everything within 2^25 of
-        // the bound.  P block cb lands in TMEM columns [16 cb, 16 cb + 16) of
-        // the S buffer; it is written after every S block of the quadrant
-        // has been read (the exchange orders the two warps of a pair).
+        // helper warp).  p_jl = S_jl lambda^(j-l) for l <= j, l < Lc, else 0,
+        // goes to TMEM as fp16 scaled by 2^-e_j, a power of two chosen from
+        // the row's max |p| (the two warps of a split quadrant exchange their
+        // partial maxima) so that the row sits below 2^12: no overflow, and
+        // 11 significant bits for everything within 2^25 of the maximum.
+        //   pass 1: the decay goes into the held registers, p' = S f, with
+        //     f = lambda^(lane - c) (masked) on the diagonal block and
+        //     f = lambda^(32 (q - cb) - 1 - c) below it, where the rest of
+        //     lambda^(j-l), lambda^(lane+1), is a row constant; max |p|;
+        //   pass 2: p = p' 2^-e_j (times lambda^(lane+1) below the diagonal)
+        //     to fp16.
+        // P block cb lands in TMEM columns [16 cb, 16 cb + 16) of the S
+        // buffer, written after every S block of the quadrant has been read
+        // (the exchange orders the two warps of a pair).
         const int q = warp & 3;
         const bool owner = warp < kStateWarp0;
         const int j = q * 32 + lane;
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-        const int cb0 = owner ? (q < 2 ? 0 : q - 1) : 0;
-        const int nb = owner ? (q == 0 ? 1 : 2) : (q == 2 ? 1 : 2);
+        // Blocks: register set A holds a block below the diagonal (none for
+        // the quadrant-0 owner); set B holds the owner's diagonal block, or
+        // the quadrant-3 helper's second block.
+        const bool has_a = !(owner && q == 0);
+        const int cba = owner ? q - 1 : 0;
+        const bool has_b = owner || q == 3;
+        const int cbb = owner ? q : 1;
         const int pr = q - 2;  // pair index of a split quadrant
-        // Upper bound of |p| over the valid columns of one block.
-        auto block_bound = [&](const float(&sv)[32], int cb, int Lc) -> float {
-            const bool diag = cb == q;
-            const int lim = min(diag ? lane : 31, Lc - 1 - cb * 32);  // last valid column
-            float t[16];
+        const uint32_t pwt_s = smem_u32(&cs.pwt[32]);  // masked table: lambda^d at pwt_s + 4 d
+        const float rowlam = pw(lane + 1);
+        // p' = S lambda^(32 (q - cb) - 1 - c) for a block below the diagonal;
+        // returns max |p'| over the valid columns.
+        auto decay_below = [&](float(&sv)[32], int cb, int Lc) -> float {
+            const uint32_t tab = pw_s + 4u * (uint32_t)(32 * (q - cb) - 32);
+            float m = 0.f;
 #pragma unroll
-            for (int k = 0; k < 16; ++k)
-                t[k] = fmaxf(2 * k <= lim ? fabsf(sv[2 * k]) : 0.f,
-                             2 * k + 1 <= lim ? fabsf(sv[2 * k + 1]) : 0.f);
+            for (int g = 0; g < 8; ++g) {
+                // lambda^(32 (q - cb) - 1 - c), c = 4g .. 4g + 3: the four
+                // table entries from 32 (q - cb) - 4 - 4g, reversed
+                const uint4 f4 = ld_shared_v4(tab + 16u * (uint32_t)(7 - g));
+                const float2 x0 = f2_mul(make_float2(sv[4 * g], sv[4 * g + 1]),
+                                         make_float2(__uint_as_float(f4.w), __uint_as_float(f4.z)));
+                const float2 x1 = f2_mul(make_float2(sv[4 * g + 2], sv[4 * g + 3]),
+                                         make_float2(__uint_as_float(f4.y), __uint_as_float(f4.x)));
+                sv[4 * g] = x0.x;
+                sv[4 * g + 1] = x0.y;
+                sv[4 * g + 2] = x1.x;
+                sv[4 * g + 3] = x1.y;
+            }
+            const int lim = Lc - 1 - cb * 32;  // last valid column
+            if (lim < 31) {  // ragged last chunk
 #pragma unroll
-            for (int w = 8; w > 0; w >>= 1)
+                for (int c = 0; c < 32; ++c) sv[c] = c <= lim ? sv[c] : 0.f;
+            }
 #pragma unroll
-                for (int k = 0; k < w; ++k) t[k] = fmaxf(t[k], t[k + w]);
-            return diag ? t[0] : t[0] * pw(j - cb * 32 - 31);
+            for (int c = 0; c < 32; ++c) m = fmaxf(m, fabsf(sv[c]));
+            return m;
         };
-        // Masks, decays, scales and packs one block into TMEM.
-        auto write_block = [&](const float(&sv)[32], int cb, int Lc, float inv, uint32_t scol) {
+        // p' = S lambda^(lane - c) for c <= lane (0 above the diagonal).
+        auto decay_diag = [&](float(&sv)[32], int cb, int Lc) -> float {
+            const uint32_t tab = pwt_s + 4u * (uint32_t)lane;
+            float m = 0.f;
+#pragma unroll
+            for (int c = 0; c < 32; c += 2) {
+                const float2 x = f2_mul(make_float2(sv[c], sv[c + 1]),
+                                        make_float2(ld_shared_f32(tab - 4u * c),
+                                                    ld_shared_f32(tab - 4u * (c + 1))));
+                sv[c] = x.x;
+                sv[c + 1] = x.y;
+            }
+            const int lim = Lc - 1 - cb * 32;
+            if (lim < 31) {
+#pragma unroll
+                for (int c = 0; c < 32; ++c) sv[c] = c <= lim ? sv[c] : 0.f;
+            }
+#pragma unroll
+            for (int c = 0; c < 32; ++c) m = fmaxf(m, fabsf(sv[c]));
+            return m;
+        };
+        // p = p' * scale to fp16, into TMEM columns [16 cb, 16 cb + 16)
+        auto store_block = [&](const float(&sv)[32], int cb, float scale, uint32_t scol) {
+            const float2 s2 = make_float2(scale, scale);
             uint32_t pk[16];
-            if (cb == q) {  // diagonal block: lambda^(lane - c) for c <= lane
-                const int lim = min(lane, Lc - 1 - cb * 32);
-                const float2 inv2 = make_float2(inv, inv);
 #pragma unroll
-                for (int m = 0; m < 16; ++m) {
-                    const int c = 2 * m;
-                    const float2 f = f2_mul(make_float2(pw(max(lane - c, 0)), pw(max(lane - c - 1, 0))),
-                                            inv2);
-                    const float2 x = f2_mul(make_float2(sv[c], sv[c + 1]), f);
-                    pk[m] = pack_f16(c <= lim ? x.x : 0.f, c + 1 <= lim ? x.y : 0.f);
-                }
-            } else {  // below the diagonal: lambda^(j - 32 cb - 31) lambda^(31 - c)
-                const float rowf = pw(j - cb * 32 - 31) * inv;
-                const float2 rf = make_float2(rowf, rowf);
-                const int lim = min(31, Lc - 1 - cb * 32);
-#pragma unroll
-                for (int g = 0; g < 8; ++g) {
-                    // lambda^(31 - c) for c = 4g .. 4g + 3: pw[28 - 4g .. 31 - 4g] reversed
-                    const uint4 cu4 = ld_shared_v4(pw_s + 16u * (uint32_t)(7 - g));
-                    const float2 f0 = f2_mul(rf, make_float2(__uint_as_float(cu4.w), __uint_as_float(cu4.z)));
-                    const float2 f1 = f2_mul(rf, make_float2(__uint_as_float(cu4.y), __uint_as_float(cu4.x)));
-                    float2 x0 = f2_mul(make_float2(sv[4 * g], sv[4 * g + 1]), f0);
-                    float2 x1 = f2_mul(make_float2(sv[4 * g + 2], sv[4 * g + 3]), f1);
-                    if (lim < 31) {  // ragged last chunk
-                        x0.x = 4 * g <= lim ? x0.x : 0.f;
-                        x0.y = 4 * g + 1 <= lim ? x0.y : 0.f;
-                        x1.x = 4 * g + 2 <= lim ? x1.x : 0.f;
-                        x1.y = 4 * g + 3 <= lim ? x1.y : 0.f;
-                    }
-                    pk[2 * g] = pack_f16(x0.x, x0.y);
-                    pk[2 * g + 1] = pack_f16(x1.x, x1.y);
-                }
+            for (int m = 0; m < 16; ++m) {
+                const float2 x = f2_mul(make_float2(sv[2 * m], sv[2 * m + 1]), s2);
+                pk[m] = pack_f16(x.x, x.y);
             }
             tmem_st16(scol + cb * 16, pk);
         };
@@ -423,11 +444,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             if (!warp_wait(bar(cs.s_full[st]), sph, abort_flag)) break;
             tc_fence_after();
             float sa[32], sb2[32];
-            tmem_ld32(scol + cb0 * 32, sa);
-            if (nb == 2) tmem_ld32(scol + (cb0 + 1) * 32, sb2);
+            if (has_a) tmem_ld32(scol + cba * 32, sa);
+            if (has_b) tmem_ld32(scol + cbb * 32, sb2);
             tmem_wait_ld();
-            float bound = block_bound(sa, cb0, Lc);
-            if (nb == 2) bound = fmaxf(bound, block_bound(sb2, cb0 + 1, Lc));
+            // pass 1
+            float mb = 0.f, md = 0.f;  // max |p'| below the diagonal, on it
+            if (has_a) mb = decay_below(sa, cba, Lc);
+            if (owner) md = decay_diag(sb2, cbb, Lc);
+            else if (has_b) mb = fmaxf(mb, decay_below(sb2, cbb, Lc));
+            float bound = fmaxf(mb * rowlam, md);
             if (q >= 2) {  // exchange with the other warp of the quadrant
                 // Only the exponent of the bound matters: pass its top 16 bits
                 // (a nonzero bound stays nonzero), so both warps pick the same e.
@@ -442,14 +467,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             }
             const int e = fp16_scale_exp(bound, 11);
             const float inv = exp2i(-e);
-            // one copy of the block code for both held blocks (the
-            // instruction cache is shared by the roles of a sub-partition)
-#pragma unroll 1
-            for (int k = 0; k < nb; ++k) {
-                write_block(sa, cb0 + k, Lc, inv, scol);
-#pragma unroll
-                for (int c = 0; c < 32; ++c) sa[c] = sb2[c];
-            }
+            // pass 2
+            if (has_a) store_block(sa, cba, rowlam * inv, scol);
+            if (has_b) store_block(sb2, cbb, owner ? inv : rowlam * inv, scol);
             if (owner) {
 #pragma unroll 1
                 for (int cb = q + 1; cb < 4; ++cb) tmem_st16(scol + cb * 16, zero);

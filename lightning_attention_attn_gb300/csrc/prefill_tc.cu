@@ -44,10 +44,13 @@
 //                quadrant each, helped by warps 14 and 15 on the two
 //                quadrants with the most blocks below the diagonal
 //   warps 4-7    state: KV fold + write-back, KV copy, output; its thread 0
-//                also issues the TMA loads of the Q, K, V two-slot rings
+//                also issues the TMA loads of the Q ring
 //   warps 8-11   V-tile: Vhat hi/lo, fp16 V
-//   warp  12     MMA stream A (one thread): S and P V
-//   warp  13     MMA stream B (one thread): dKV and Q KV
+//   warp  12     MMA stream A (one thread): S and P V; TMA loads of the V ring
+//   warp  13     MMA stream B (one thread): dKV and Q KV; TMA loads of the K
+//                ring
+// Each ring slot is reloaded, by a role that waits for that event anyway, as
+// soon as the last MMA reading it has finished.
 // Two issuing threads keep the tensor pipe fed while either one waits: the
 // tcgen05 instruction queue is short, so a wait between two groups of MMAs
 // from a single issuer leaves the pipe idle.
@@ -79,7 +82,7 @@ constexpr int DV = 64;       // value columns per CTA
 constexpr int NVS = D / DV;  // value slices per head
 constexpr int BC = 128;      // chunk (block) size
 constexpr int kThreads = 512;  // 16 warps: 4 per SM sub-partition, 128 registers
-constexpr int kStateWarp0 = 4; // thread 0 of this warp also issues the TMA loads
+constexpr int kStateWarp0 = 4;
 constexpr int kVWarp0 = 8;
 constexpr int kMmaWarpA = 12;  // S and P V
 constexpr int kMmaWarpB = 13;  // dKV and Q KV
@@ -259,6 +262,23 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         // Per chunk i: S_{i+1}, then P_i V_i, so that the mask warps turn
         // S_{i+1} into P_{i+1} while the tensor core runs P_i V_i and stream
         // B's dKV / Q KV.  The whole warp waits; lane 0 issues.
+        // V ring: slot c & 1 is reloaded for chunk c as soon as P_{c-2} V_{c-2}
+        // has finished reading it.
+        int nv = 0;
+        auto load_v = [&](int c) -> bool {
+            const int st = c & 1;
+            if (!warp_wait(bar(cs.empty_v[st]), ((c >> 1) & 1) ^ 1, abort_flag)) return false;
+            if (elect_one()) {
+                mbar_arrive_expect_tx(bar(cs.full_v[st]), kHalf);
+                tma_load_2d(vslot(st), &tmV, bar(cs.full_v[st]), h * D + vs * DV, t0 + c * BC);
+            }
+            __syncwarp();
+            ++nv;
+            return true;
+        };
+        if (elect_one()) tma_prefetch_desc(&tmV);
+        __syncwarp();
+        for (int c = 0; c < min(nch, 2); ++c) load_v(c);
         auto issue_s = [&](int i) -> bool {  // S_i = Q_i K_i^T
             const int st = i & 1;
             const uint32_t sph = (i >> 1) & 1;
@@ -295,15 +315,38 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
                 mma_commit(bar(cs.empty_v[st]));
             }
             __syncwarp();
+            if (i + 2 < nch && !load_v(i + 2)) break;
         }
-        // All MMAs must be finished before TMEM is released.
+        // All MMAs must be finished before TMEM is released, and no load
+        // may still be landing in shared memory when the CTA exits.
         if (elect_one()) mma_commit(bar(cs.done_a));
         __syncwarp();
         int no_abort = 0;
         warp_wait(bar(cs.done_a), 0, &no_abort);
+        for (int c = max(0, nv - 2); c < nv; ++c)
+            warp_wait(bar(cs.full_v[c & 1]), (c >> 1) & 1, &no_abort);
     } else if (warp == kMmaWarpB) {
         // ================= MMA stream B: dKV and Q KV =================
         const uint32_t vha = sb + kOffVhat, kvb = sb + kOffKVb;
+        // K ring: slot c & 1 is reloaded for chunk c once S and dKV of chunk
+        // c - 2 have finished; K_{i+2} is loaded right after Q_i KV is issued
+        // (the wait is for dKV_i, which the next dKV needs anyway).
+        int nk = 0;
+        auto load_k = [&](int c) -> bool {
+            const int st = c & 1;
+            if (!warp_wait(bar(cs.empty_k[st]), ((c >> 1) & 1) ^ 1, abort_flag)) return false;
+            if (elect_one()) {
+                mbar_arrive_expect_tx(bar(cs.full_k[st]), 2 * kHalf);
+                tma_load_2d(kslot(st), &tmK, bar(cs.full_k[st]), h * D, t0 + c * BC);
+                tma_load_2d(kslot(st) + kHalf, &tmK, bar(cs.full_k[st]), h * D + 64, t0 + c * BC);
+            }
+            __syncwarp();
+            ++nk;
+            return true;
+        };
+        if (elect_one()) tma_prefetch_desc(&tmK);
+        __syncwarp();
+        for (int c = 0; c < min(nch, 2); ++c) load_k(c);
         for (int i = 0; i < nch; ++i) {
             const int st = i & 1;
             const uint32_t sph = (i >> 1) & 1, ph = i & 1;
@@ -334,11 +377,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
                 mma_commit(bar(cs.empty_q[st]));
             }
             __syncwarp();
+            if (i + 2 < nch && !load_k(i + 2)) break;
         }
         if (elect_one()) mma_commit(bar(cs.done_b));
         __syncwarp();
         int no_abort = 0;
         warp_wait(bar(cs.done_b), 0, &no_abort);
+        for (int c = max(0, nk - 2); c < nk; ++c)
+            warp_wait(bar(cs.full_k[c & 1]), (c >> 1) & 1, &no_abort);
     } else if (warp < kStateWarp0 || warp == kMaskHelp2 || warp == kMaskHelp3) {
         // ================= mask warps: S -> P =================
         // Row j of the chunk is TMEM lane j; the warps of lane quadrant q
@@ -497,43 +543,24 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         const uint32_t kvb = sb + kOffKVb;
         const uint32_t tkv = tmem + lane_off + kColDKV;
         const uint32_t to2 = tmem + lane_off + kColO2;
-        // TMA loads (thread 0 of the warpgroup).  Slot c & 1 of a ring is
-        // reloaded for chunk c once chunk c - 2 has released it: Q and K when
-        // Q KV and dKV of chunk c - 2 have finished (seen here at the copy
-        // step), V when its P V has finished (seen at the output step).
-        const bool loader = threadIdx.x == kStateWarp0 * 32;
-        int nq = 0, nk = 0, nv = 0;
-        auto load_qk = [&](int c) -> bool {
+        // Q ring (thread 0 of the warpgroup): slot c & 1 is reloaded for
+        // chunk c once S and Q KV of chunk c - 2 have finished; the copy step
+        // of chunk c - 2 waits for that Q KV anyway.
+        const bool qloader = threadIdx.x == kStateWarp0 * 32;
+        int nq = 0;
+        auto load_q = [&](int c) -> bool {
             const int st = c & 1;
-            const uint32_t sph = (c >> 1) & 1;
-            const int y = t0 + c * BC;
-            if (!mbar_wait(bar(cs.empty_q[st]), sph ^ 1, abort_flag, kTimeoutNs)) return false;
+            if (!mbar_wait(bar(cs.empty_q[st]), ((c >> 1) & 1) ^ 1, abort_flag, kTimeoutNs))
+                return false;
             mbar_arrive_expect_tx(bar(cs.full_q[st]), 2 * kHalf);
-            tma_load_2d(qslot(st), &tmQ, bar(cs.full_q[st]), h * D, y);
-            tma_load_2d(qslot(st) + kHalf, &tmQ, bar(cs.full_q[st]), h * D + 64, y);
+            tma_load_2d(qslot(st), &tmQ, bar(cs.full_q[st]), h * D, t0 + c * BC);
+            tma_load_2d(qslot(st) + kHalf, &tmQ, bar(cs.full_q[st]), h * D + 64, t0 + c * BC);
             ++nq;
-            if (!mbar_wait(bar(cs.empty_k[st]), sph ^ 1, abort_flag, kTimeoutNs)) return false;
-            mbar_arrive_expect_tx(bar(cs.full_k[st]), 2 * kHalf);
-            tma_load_2d(kslot(st), &tmK, bar(cs.full_k[st]), h * D, y);
-            tma_load_2d(kslot(st) + kHalf, &tmK, bar(cs.full_k[st]), h * D + 64, y);
-            ++nk;
             return true;
         };
-        auto load_v = [&](int c) -> bool {
-            const int st = c & 1;
-            const uint32_t sph = (c >> 1) & 1;
-            if (!mbar_wait(bar(cs.empty_v[st]), sph ^ 1, abort_flag, kTimeoutNs)) return false;
-            mbar_arrive_expect_tx(bar(cs.full_v[st]), kHalf);
-            tma_load_2d(vslot(st), &tmV, bar(cs.full_v[st]), h * D + vs * DV, t0 + c * BC);
-            ++nv;
-            return true;
-        };
-        if (loader) {
+        if (qloader) {
             tma_prefetch_desc(&tmQ);
-            tma_prefetch_desc(&tmK);
-            tma_prefetch_desc(&tmV);
-            for (int c = 0; c < min(nch, 2); ++c)
-                if (!load_qk(c) || !load_v(c)) break;
+            for (int c = 0; c < min(nch, 2); ++c) load_q(c);
         }
         __syncwarp();
         // KV_{-1} = 0
@@ -624,7 +651,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
                 }
                 fence_proxy_async_smem();
             }
-            if (loader && i + 2 < nch) load_qk(i + 2);
+            if (qloader && i + 2 < nch) load_q(i + 2);
             __syncwarp();
             // ---- O2 ----
             float o2[DV];
@@ -650,8 +677,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             if (!warp_wait(bar(cs.o_full[st]), sph, abort_flag)) break;
             if (!warp_wait(bar(cs.pv_ready[st]), sph, abort_flag)) break;  // orders the scales
             tc_fence_after();
-            if (loader && i + 2 < nch) load_v(i + 2);
-            __syncwarp();
             const float s1 = exp2i((int)*reinterpret_cast<volatile signed char *>(&cs.rowe[st][r])) *
                              ld_shared_f32(vscale_s + 4u * (uint32_t)(i & 3));
             const float qf = pw(r + 1);
@@ -681,14 +706,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
                 }
             }
         }
-        if (loader) {  // never leave with a load still landing in shared memory
+        if (qloader) {  // never leave with a load still landing in shared memory
             int no_abort = 0;
             for (int c = max(0, nq - 2); c < nq; ++c)
                 mbar_wait(bar(cs.full_q[c & 1]), (c >> 1) & 1, &no_abort, kTimeoutNs);
-            for (int c = max(0, nk - 2); c < nk; ++c)
-                mbar_wait(bar(cs.full_k[c & 1]), (c >> 1) & 1, &no_abort, kTimeoutNs);
-            for (int c = max(0, nv - 2); c < nv; ++c)
-                mbar_wait(bar(cs.full_v[c & 1]), (c >> 1) & 1, &no_abort, kTimeoutNs);
         }
         __syncwarp();
         if (nch == 0 && final_state) {  // empty sequence: the state stays zero
@@ -699,34 +720,51 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         }
     } else if (warp < kVWarp0 + 4) {
         // ================= V-tile warpgroup =================
-        // Chunk i's V tile, one row (token) per thread, in two steps:
+        // Chunk i's V tile, one row (token) per thread, in three steps:
+        //  0. max |v| over the tile (exchanged among the four warps while
+        //     step 1 runs), as soon as the tile has landed;
         //  1. Vhat = Lambda_K V as a hi/lo bf16 pair for the dKV MMA (Vhat_i
         //     may be written once dKV_{i-1} has read Vhat_{i-1});
         //  2. V itself, converted in place to fp16 with the chunk's
-        //     power-of-two scale (a max over the tile) for the P V MMA.
+        //     power-of-two scale for the P V MMA.
         // Rows past the chunk end are zero in both.
         const int w4 = warp - kVWarp0;
         const int vr = w4 * 32 + lane;
         const uint32_t vha = sb + kOffVhat;
         for (int i = 0; i < nch; ++i) {
             const int st = i & 1;
-            if (i > 0 && !warp_wait(bar(cs.dkv_full), (i - 1) & 1, abort_flag)) break;
             if (!warp_wait(bar(cs.full_v[st]), (i >> 1) & 1, abort_flag)) break;
             const int Lc = min(BC, L - i * BC);
             const bool live = vr < Lc;
             const uint32_t row = vslot(st) + vr * 128;
-            // ---- 1: Vhat (and max |v| of the row).  lambda^(Lc-1-l) split as
-            // g_hi + g_lo (bf16 each) so that the packed bf16 FMAs give
-            // hi + lo = v g to ~16 bits.  The loops stay rolled: the three
-            // roles of an SM sub-partition share its instruction cache.
-            uint32_t mbits = 0;  // max |v| as packed bf16 magnitudes
+            // ---- 0: max |v| (bf16 magnitudes, packed)
+            {
+                uint32_t mbits = 0;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 x = ld_shared_v4(row + (uint32_t)((c + vr) & 7) * 16);
+                    mbits = __vmaxu2(__vmaxu2(mbits, x.x & 0x7fff7fffu), x.y & 0x7fff7fffu);
+                    mbits = __vmaxu2(__vmaxu2(mbits, x.z & 0x7fff7fffu), x.w & 0x7fff7fffu);
+                }
+                if (!live) mbits = 0;
+                float m = fmaxf(__uint_as_float(mbits << 16), __uint_as_float(mbits & 0xffff0000u));
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                if (lane == 0) st_shared_f32(vmax_s + 4u * (uint32_t)((i & 1) * 4 + w4), m);
+                mbar_arrive(bar(cs.vmax_ready[i & 1]));
+            }
+            // ---- 1: Vhat.  lambda^(Lc-1-l) split as g_hi + g_lo (bf16
+            // each) so that the packed bf16 FMAs give hi + lo = v g to ~16
+            // bits.  The loops stay rolled: the three roles of an SM
+            // sub-partition share its instruction cache.
+            if (i > 0 && !warp_wait(bar(cs.dkv_full), (i - 1) & 1, abort_flag)) break;
             {
                 const float g = live ? pw(Lc - 1 - vr) : 0.f;
                 const __nv_bfloat16 ghb = __float2bfloat16_rn(g);
                 const __nv_bfloat16 glb = __float2bfloat16_rn(g - __bfloat162float(ghb));
                 const __nv_bfloat162 gh = __halves2bfloat162(ghb, ghb);
                 const __nv_bfloat162 gl = __halves2bfloat162(glb, glb);
-#pragma unroll 1
+#pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     const uint32_t ch = (uint32_t)((c + vr) & 7) * 16;
                     const uint4 x = ld_shared_v4(row + ch);
@@ -734,7 +772,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
                     uint32_t hi[4], lo[4];
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        mbits = __vmaxu2(mbits, w[q] & 0x7fff7fffu);
                         const __nv_bfloat162 v2 = *reinterpret_cast<const __nv_bfloat162 *>(&w[q]);
                         const __nv_bfloat162 h2 = __hmul2(v2, gh);
                         // exact residual of the rounded product, plus the g_lo term
@@ -750,12 +787,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
                 mbar_arrive(bar(cs.dkv_ready));
             }
             // ---- 2: fp16 V for P V
-            if (!live) mbits = 0;
-            float m = fmaxf(__uint_as_float(mbits << 16), __uint_as_float(mbits & 0xffff0000u));
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-            if (lane == 0) st_shared_f32(vmax_s + 4u * (uint32_t)((i & 1) * 4 + w4), m);
-            mbar_arrive(bar(cs.vmax_ready[i & 1]));
             if (!warp_wait(bar(cs.vmax_ready[i & 1]), (i >> 1) & 1, abort_flag)) break;
             const uint32_t vm = vmax_s + 16u * (uint32_t)(i & 1);
             const float mt = fmaxf(fmaxf(ld_shared_f32(vm), ld_shared_f32(vm + 4)),
@@ -768,7 +799,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
                 st_shared_f32(vscale_s + 4u * (uint32_t)(i & 3), exp2i(f));
             const float sc = live ? exp2i(-f) : 0.f;
             const float2 sc2 = make_float2(sc, sc);
-#pragma unroll 1
+#pragma unroll
             for (int c = 0; c < 8; ++c) {
                 const uint32_t ch = (uint32_t)((c + vr) & 7) * 16;
                 const uint4 x = ld_shared_v4(row + ch);

@@ -44,11 +44,10 @@
 //                quadrant each, helped by warps 14 and 15 on the two
 //                quadrants with the most blocks below the diagonal
 //   warps 4-7    state: KV fold + write-back, KV copy, output; its thread 0
-//                also issues the TMA loads of the Q ring
+//                also issues the TMA loads of the Q and K rings
 //   warps 8-11   V-tile: Vhat hi/lo, fp16 V
 //   warp  12     MMA stream A (one thread): S and P V; TMA loads of the V ring
-//   warp  13     MMA stream B (one thread): dKV and Q KV; TMA loads of the K
-//                ring
+//   warp  13     MMA stream B (one thread): dKV and Q KV
 // Each ring slot is reloaded, by a role that waits for that event anyway, as
 // soon as the last MMA reading it has finished.
 // Two issuing threads keep the tensor pipe fed while either one waits: the
@@ -328,25 +327,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     } else if (warp == kMmaWarpB) {
         // ================= MMA stream B: dKV and Q KV =================
         const uint32_t vha = sb + kOffVhat, kvb = sb + kOffKVb;
-        // K ring: slot c & 1 is reloaded for chunk c once S and dKV of chunk
-        // c - 2 have finished; K_{i+2} is loaded right after Q_i KV is issued
-        // (the wait is for dKV_i, which the next dKV needs anyway).
-        int nk = 0;
-        auto load_k = [&](int c) -> bool {
-            const int st = c & 1;
-            if (!warp_wait(bar(cs.empty_k[st]), ((c >> 1) & 1) ^ 1, abort_flag)) return false;
-            if (elect_one()) {
-                mbar_arrive_expect_tx(bar(cs.full_k[st]), 2 * kHalf);
-                tma_load_2d(kslot(st), &tmK, bar(cs.full_k[st]), h * D, t0 + c * BC);
-                tma_load_2d(kslot(st) + kHalf, &tmK, bar(cs.full_k[st]), h * D + 64, t0 + c * BC);
-            }
-            __syncwarp();
-            ++nk;
-            return true;
-        };
-        if (elect_one()) tma_prefetch_desc(&tmK);
-        __syncwarp();
-        for (int c = 0; c < min(nch, 2); ++c) load_k(c);
         for (int i = 0; i < nch; ++i) {
             const int st = i & 1;
             const uint32_t sph = (i >> 1) & 1, ph = i & 1;
@@ -377,14 +357,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
                 mma_commit(bar(cs.empty_q[st]));
             }
             __syncwarp();
-            if (i + 2 < nch && !load_k(i + 2)) break;
         }
         if (elect_one()) mma_commit(bar(cs.done_b));
         __syncwarp();
         int no_abort = 0;
         warp_wait(bar(cs.done_b), 0, &no_abort);
-        for (int c = max(0, nk - 2); c < nk; ++c)
-            warp_wait(bar(cs.full_k[c & 1]), (c >> 1) & 1, &no_abort);
     } else if (warp < kStateWarp0 || warp == kMaskHelp2 || warp == kMaskHelp3) {
         // ================= mask warps: S -> P =================
         // Row j of the chunk is TMEM lane j; the warps of lane quadrant q
@@ -543,11 +520,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         const uint32_t kvb = sb + kOffKVb;
         const uint32_t tkv = tmem + lane_off + kColDKV;
         const uint32_t to2 = tmem + lane_off + kColO2;
-        // Q ring (thread 0 of the warpgroup): slot c & 1 is reloaded for
-        // chunk c once S and Q KV of chunk c - 2 have finished; the copy step
-        // of chunk c - 2 waits for that Q KV anyway.
-        const bool qloader = threadIdx.x == kStateWarp0 * 32;
-        int nq = 0;
+        // Q and K rings (thread 0 of the warpgroup): slot c & 1 is reloaded
+        // for chunk c once S and dKV (K) or S and Q KV (Q) of chunk c - 2
+        // have finished; the fold and copy steps of chunk c - 2 wait for dKV
+        // and Q KV anyway, and S was issued before.
+        const bool loader = threadIdx.x == kStateWarp0 * 32;
+        int nq = 0, nk = 0;
         auto load_q = [&](int c) -> bool {
             const int st = c & 1;
             if (!mbar_wait(bar(cs.empty_q[st]), ((c >> 1) & 1) ^ 1, abort_flag, kTimeoutNs))
@@ -558,9 +536,21 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             ++nq;
             return true;
         };
-        if (qloader) {
+        auto load_k = [&](int c) -> bool {
+            const int st = c & 1;
+            if (!mbar_wait(bar(cs.empty_k[st]), ((c >> 1) & 1) ^ 1, abort_flag, kTimeoutNs))
+                return false;
+            mbar_arrive_expect_tx(bar(cs.full_k[st]), 2 * kHalf);
+            tma_load_2d(kslot(st), &tmK, bar(cs.full_k[st]), h * D, t0 + c * BC);
+            tma_load_2d(kslot(st) + kHalf, &tmK, bar(cs.full_k[st]), h * D + 64, t0 + c * BC);
+            ++nk;
+            return true;
+        };
+        if (loader) {
             tma_prefetch_desc(&tmQ);
-            for (int c = 0; c < min(nch, 2); ++c) load_q(c);
+            tma_prefetch_desc(&tmK);
+            for (int c = 0; c < min(nch, 2); ++c)
+                if (!load_k(c) || !load_q(c)) break;
         }
         __syncwarp();
         // KV_{-1} = 0
@@ -624,6 +614,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             }
             tc_fence_before();
             mbar_arrive(bar(cs.dkv_ready));
+            if (loader && i + 2 < nch) load_k(i + 2);
+            __syncwarp();
             // ---- copy ----
             if (!warp_wait(bar(cs.o2_full), ph, abort_flag)) break;
             tc_fence_after();
@@ -651,7 +643,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
                 }
                 fence_proxy_async_smem();
             }
-            if (qloader && i + 2 < nch) load_q(i + 2);
+            if (loader && i + 2 < nch) load_q(i + 2);
             __syncwarp();
             // ---- O2 ----
             float o2[DV];
@@ -706,10 +698,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
                 }
             }
         }
-        if (qloader) {  // never leave with a load still landing in shared memory
+        if (loader) {  // never leave with a load still landing in shared memory
             int no_abort = 0;
             for (int c = max(0, nq - 2); c < nq; ++c)
                 mbar_wait(bar(cs.full_q[c & 1]), (c >> 1) & 1, &no_abort, kTimeoutNs);
+            for (int c = max(0, nk - 2); c < nk; ++c)
+                mbar_wait(bar(cs.full_k[c & 1]), (c >> 1) & 1, &no_abort, kTimeoutNs);
         }
         __syncwarp();
         if (nch == 0 && final_state) {  // empty sequence: the state stays zero

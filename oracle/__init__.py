@@ -11,6 +11,7 @@ Sources followed (MiniMax-01 technical report, CSDN full translation):
   * §2.2.1, eq. 5 -- right-product recursion kv_t = kv_{t-1} + k_t^T v_t
   * Fig. 12 caption -- the diagonal decay matrix: weight lambda_h^(t-u)
   * §3.2 "data packing" -- packed sequences are independent
+  * §3.3.1 prefix KV cache -- a sequence may continue from a cached state
 Parity pins: tests/test_oracle.py (golden hand examples, closed forms,
 two-form agreement, exact rational brute force, invariants).
 """
@@ -53,10 +54,10 @@ def _needs_build() -> bool:
 
 def _declare(lib):
     lib.la_oracle_quadratic.argtypes = [_dp, _dp, _dp, _dp, _ip, ctypes.c_int,
-                                        ctypes.c_int, ctypes.c_int, _up, _dp,
+                                        ctypes.c_int, ctypes.c_int, _up, _dp, _dp,
                                         ctypes.c_int]
     lib.la_oracle_recurrent.argtypes = [_dp, _dp, _dp, _dp, _ip, ctypes.c_int,
-                                        ctypes.c_int, ctypes.c_int, _up, _dp,
+                                        ctypes.c_int, ctypes.c_int, _up, _dp, _dp,
                                         _dp, ctypes.c_int]
     lib.la_oracle_decode.argtypes = [_dp, _dp, _dp, _dp, _dp, ctypes.c_int,
                                      ctypes.c_int, ctypes.c_int, _dp, ctypes.c_int]
@@ -119,20 +120,32 @@ def _sel(head_sel, H):
     return m
 
 
-def quadratic(q, k, v, decay, cu_seqlens, heads=None, nthreads=0, lib=None):
+def _init(initial_state, nseq, H, d):
+    if initial_state is None:
+        return None
+    s0 = _f64(initial_state)
+    assert s0.shape == (nseq, H, d, d), s0.shape
+    return s0
+
+
+def quadratic(q, k, v, decay, cu_seqlens, heads=None, nthreads=0, lib=None,
+              initial_state=None):
     """Left-product form.  q, k, v: [T, H, d]; decay: [H]; cu_seqlens:
-    [nseq+1].  Returns out [T, H, d] fp64 (rows of unselected heads are 0)."""
+    [nseq+1]; initial_state: cached state per sequence [nseq, H, d, d] or
+    None.  Returns out [T, H, d] fp64 (rows of unselected heads are 0)."""
     lib = lib or load()
     q, k, v = _f64(q), _f64(k), _f64(v)
     lam = _f64(decay_as_seen(decay))
     cu = _i32(cu_seqlens)
     T, H, d = _shape(q)
     assert cu[-1] == T
+    s0 = _init(initial_state, len(cu) - 1, H, d)
     out = np.zeros((T, H, d), dtype=np.float64)
     sel = _sel(heads, H)
     rc = lib.la_oracle_quadratic(_ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp),
                                  _ptr(lam, _dp), _ptr(cu, _ip), len(cu) - 1, H,
                                  d, None if sel is None else _ptr(sel, _up),
+                                 None if s0 is None else _ptr(s0, _dp),
                                  _ptr(out, _dp), nthreads)
     if rc:
         raise ValueError(f"la_oracle_quadratic failed ({rc})")
@@ -140,9 +153,10 @@ def quadratic(q, k, v, decay, cu_seqlens, heads=None, nthreads=0, lib=None):
 
 
 def recurrent(q, k, v, decay, cu_seqlens, heads=None, want_out=True,
-              nthreads=0, lib=None):
-    """Right-product recursion.  Returns (out [T,H,d] or None,
-    final_state [nseq,H,d,d]), both fp64."""
+              nthreads=0, lib=None, initial_state=None):
+    """Right-product recursion, from zero or from ``initial_state``
+    [nseq, H, d, d].  Returns (out [T,H,d] or None, final_state [nseq,H,d,d]),
+    both fp64."""
     lib = lib or load()
     q, k, v = _f64(q), _f64(k), _f64(v)
     lam = _f64(decay_as_seen(decay))
@@ -152,10 +166,12 @@ def recurrent(q, k, v, decay, cu_seqlens, heads=None, want_out=True,
     nseq = len(cu) - 1
     out = np.zeros((T, H, d), dtype=np.float64) if want_out else None
     st = np.zeros((nseq, H, d, d), dtype=np.float64)
+    s0 = _init(initial_state, nseq, H, d)
     sel = _sel(heads, H)
     rc = lib.la_oracle_recurrent(_ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp),
                                  _ptr(lam, _dp), _ptr(cu, _ip), nseq, H, d,
                                  None if sel is None else _ptr(sel, _up),
+                                 None if s0 is None else _ptr(s0, _dp),
                                  None if out is None else _ptr(out, _dp),
                                  _ptr(st, _dp), nthreads)
     if rc:

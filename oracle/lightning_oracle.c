@@ -20,6 +20,11 @@
  *     quadratic:  o_t = sum_{u<=t} lambda^(t-u) (q_t . k_u) v_u
  *     recurrent:  kv_t = lambda kv_{t-1} + k_t^T v_t,  o_t = q_t kv_t
  * and the state after the last token is sum_u lambda^(L-1-u) k_u^T v_u.
+ * A sequence may continue from a cached state S0 (the prefix KV cache of
+ * §3.3.1): S0 = sum over the earlier tokens u' < 0 of lambda^(-1-u') k^T v,
+ * so kv_{-1} = S0 in the recursion and the left product gains the earlier
+ * tokens' terms, sum_{u'<0} lambda^(t-u') (q_t . k_u') v_u' =
+ * lambda^(t+1) q_t S0.  Without a cached state S0 = 0.
  * Normalisation, SiLU and gating are left out, as the report's derivation
  * does (§2.2.1).  Packed inputs ("data packing", §3.2) are independent
  * sequences: the state restarts from zero at every sequence start.
@@ -29,6 +34,7 @@
  *   lam            [H]             per-head decay lambda_h in (0, 1]
  *   cu_seqlens     [nseq + 1]      sequence s is tokens [cu[s], cu[s+1])
  *   state          [nseq, H, d, d] state[s][h][i][j] = sum_u w_u k_u[i] v_u[j]
+ *   initial_state  [nseq, H, d, d] cached state S0 per sequence (nullable)
  *
  * Parity pins for every function here live in the CPU test suite (hand
  * examples, closed forms, the agreement of the two independent forms,
@@ -75,14 +81,15 @@ int la_oracle_max_threads(int nthreads)
 /*
  * Quadratic ("left product", eq. 4) form, with the decay mask
  * M_tu = lambda^(t-u) for t >= u and 0 above the diagonal.
- * For every (sequence, head): S = Q K^T, P = S (.) M, O = P V.
+ * For every (sequence, head): S = Q K^T, P = S (.) M, O = P V, plus
+ * lambda^(t+1) q_t S0 for a cached state S0 (initial_state, nullable).
  * head_sel (nullable) restricts the work to heads with head_sel[h] != 0;
  * rows of other heads are left untouched.  O(L^2 d) per (sequence, head).
  */
 int la_oracle_quadratic(const double *q, const double *k, const double *v,
                         const double *lam, const int32_t *cu, int nseq,
-                        int H, int d, const uint8_t *head_sel, double *out,
-                        int nthreads)
+                        int H, int d, const uint8_t *head_sel,
+                        const double *initial_state, double *out, int nthreads)
 {
     if (check_cu(cu, nseq) || H <= 0 || d <= 0) return 1;
     set_threads(nthreads);
@@ -107,6 +114,15 @@ int la_oracle_quadratic(const double *q, const double *k, const double *v,
                 const double p_tu = s_tu * m_tu;
                 for (int j = 0; j < d; ++j) ot[j] += p_tu * vu[j];
             }
+            if (initial_state) {  /* the earlier tokens, through S0 */
+                const double *s0 = initial_state + ((long)s * H + h) * d * d;
+                const double w = pow(la, (double)(t + 1));
+                for (int j = 0; j < d; ++j) {
+                    double acc = 0.0;
+                    for (int i = 0; i < d; ++i) acc += qt[i] * s0[(long)i * d + j];
+                    ot[j] += w * acc;
+                }
+            }
         }
     }
     return 0;
@@ -115,13 +131,15 @@ int la_oracle_quadratic(const double *q, const double *k, const double *v,
 /*
  * Recurrent ("right product", eq. 5) form with decay:
  *   kv <- lambda kv + k_t^T v_t ;  o_t = q_t kv   (update, then read),
- * kv starting at zero for every sequence.  Writes out (nullable) and the
- * state after each sequence's last token (nullable).  O(L d^2) per
+ * kv starting at zero for every sequence, or at its cached state S0 when
+ * initial_state is given.  Writes out (nullable) and the state after each
+ * sequence's last token (nullable; S0 for an empty sequence).  O(L d^2) per
  * (sequence, head).  head_sel as in la_oracle_quadratic.
  */
 int la_oracle_recurrent(const double *q, const double *k, const double *v,
                         const double *lam, const int32_t *cu, int nseq,
-                        int H, int d, const uint8_t *head_sel, double *out,
+                        int H, int d, const uint8_t *head_sel,
+                        const double *initial_state, double *out,
                         double *final_state, int nthreads)
 {
     if (check_cu(cu, nseq) || H <= 0 || d <= 0) return 1;
@@ -139,6 +157,9 @@ int la_oracle_recurrent(const double *q, const double *k, const double *v,
             err = 2;
             continue;
         }
+        if (initial_state)
+            memcpy(kv, initial_state + ((long)s * H + h) * d * d,
+                   sizeof(double) * (size_t)d * d);
         const long t0 = cu[s], L = cu[s + 1] - cu[s];
         const double la = lam[h];
         for (long t = 0; t < L; ++t) {

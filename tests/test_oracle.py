@@ -36,13 +36,14 @@ def rnd(rng, T, H, d):
 # --------------------------------------------------------------- pins
 def pin_golden_prefill(lib, name):
     g = golden(name)
+    s0 = g.get("initial_state")
     for form in ("quadratic", "recurrent"):
         if form == "quadratic":
             out = oracle.quadratic(g["q"], g["k"], g["v"], g["lambda"],
-                                   g["cu_seqlens"], lib=lib)
+                                   g["cu_seqlens"], lib=lib, initial_state=s0)
         else:
             out, st = oracle.recurrent(g["q"], g["k"], g["v"], g["lambda"],
-                                       g["cu_seqlens"], lib=lib)
+                                       g["cu_seqlens"], lib=lib, initial_state=s0)
             np.testing.assert_allclose(st, g["final_state"], rtol=0, atol=1e-15)
         np.testing.assert_allclose(out, g["out"], rtol=0, atol=1e-15,
                                    err_msg=f"{name} {form}")
@@ -73,6 +74,50 @@ def pin_geometric_d1(lib):
             lam32 = float(np.float32(lam))
             want = np.array([(1 - lam32 ** (t + 1)) / (1 - lam32) for t in range(L)])
             np.testing.assert_allclose(out.ravel(), want, rtol=1e-12)
+
+
+def pin_geometric_d1_with_state(lib):
+    """q = k = v = 1, d = 1, cached state S0:
+    kv_t = lambda^(t+1) S0 + (1 - lambda^(t+1)) / (1 - lambda) = o_t."""
+    L = 40
+    for lam, s0 in ((0.5, 3.0), (0.9, -2.0), (0.3997, 0.25)):
+        ones = np.ones((L, 1, 1))
+        lam32 = float(np.float32(lam))
+        want = np.array([lam32 ** (t + 1) * s0 + (1 - lam32 ** (t + 1)) / (1 - lam32)
+                         for t in range(L)])
+        init = np.full((1, 1, 1, 1), s0)
+        outq = oracle.quadratic(ones, ones, ones, [lam], [0, L], lib=lib, initial_state=init)
+        outr, st = oracle.recurrent(ones, ones, ones, [lam], [0, L], lib=lib, initial_state=init)
+        np.testing.assert_allclose(outq.ravel(), want, rtol=1e-12)
+        np.testing.assert_allclose(outr.ravel(), want, rtol=1e-12)
+        np.testing.assert_allclose(st.ravel(), [want[-1]], rtol=1e-12)
+
+
+def pin_prefix_cache_equivalence(lib):
+    """A segment run from the state of its prefix equals the tail of one run
+    over prefix + segment; the prefix state is taken from the closed form
+    sum_u lambda^(P-1-u) k_u^T v_u (numpy), not from the oracle."""
+    rng = np.random.default_rng(9)
+    P, L, H, d = 23, 17, 3, 5
+    q, k, v = rnd(rng, P + L, H, d)
+    lam = np.array([0.3997, 0.8, 0.99])
+    lam32 = np.float32(lam).astype(np.float64)
+    w = lam32[None, :] ** (P - 1 - np.arange(P))[:, None]
+    s_prefix = np.einsum("uh,uhi,uhj->hij", w, k[:P], v[:P])[None]
+    full_q = oracle.quadratic(q, k, v, lam, [0, P + L], lib=lib)
+    full_r, st_full = oracle.recurrent(q, k, v, lam, [0, P + L], lib=lib)
+    seg = slice(P, P + L)
+    seg_q = oracle.quadratic(q[seg], k[seg], v[seg], lam, [0, L], lib=lib,
+                             initial_state=s_prefix)
+    seg_r, st_seg = oracle.recurrent(q[seg], k[seg], v[seg], lam, [0, L], lib=lib,
+                                     initial_state=s_prefix)
+    for got, full in ((seg_q, full_q), (seg_r, full_r)):
+        np.testing.assert_allclose(got, full[seg], rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(st_seg, st_full, rtol=1e-11, atol=1e-12)
+    # an empty segment hands the cached state straight through
+    _, st_empty = oracle.recurrent(q[:0], k[:0], v[:0], lam, [0, 0], lib=lib,
+                                   initial_state=s_prefix)
+    np.testing.assert_array_equal(st_empty, s_prefix)
 
 
 def pin_lambda_one_prefix_sums(lib):
@@ -209,7 +254,10 @@ ALL_PINS = {
     "golden_a": lambda lib: pin_golden_prefill(lib, "hand_example_a.json"),
     "golden_b": lambda lib: pin_golden_prefill(lib, "hand_example_b.json"),
     "golden_packed": lambda lib: pin_golden_prefill(lib, "hand_example_packed.json"),
+    "golden_state": lambda lib: pin_golden_prefill(lib, "hand_example_state.json"),
     "golden_decode": pin_golden_decode,
+    "geometric_d1_state": pin_geometric_d1_with_state,
+    "prefix_cache": pin_prefix_cache_equivalence,
     "geometric_d1": pin_geometric_d1,
     "lambda_one": pin_lambda_one_prefix_sums,
     "lambda_tiny": pin_lambda_tiny,
@@ -228,7 +276,7 @@ def lib():
 
 
 @pytest.mark.parametrize("name", ["hand_example_a.json", "hand_example_b.json",
-                                  "hand_example_packed.json"])
+                                  "hand_example_packed.json", "hand_example_state.json"])
 def test_golden_prefill(lib, name):
     pin_golden_prefill(lib, name)
 
@@ -239,6 +287,14 @@ def test_golden_decode(lib):
 
 def test_geometric_d1(lib):
     pin_geometric_d1(lib)
+
+
+def test_geometric_d1_with_state(lib):
+    pin_geometric_d1_with_state(lib)
+
+
+def test_prefix_cache_equivalence(lib):
+    pin_prefix_cache_equivalence(lib)
 
 
 def test_lambda_one_prefix_sums(lib):
@@ -310,6 +366,11 @@ MUTANTS = {
                             "acc += qt[i] * kv[(long)j * d + i]"),
     "rec_no_reset_between_sequences": ("double *kv = (double *)calloc((size_t)d * d, sizeof(double));",
                                        "static __thread double *kvp = 0; if (!kvp) kvp = (double *)calloc(4096, sizeof(double)); double *kv = kvp; int keep = 1;"),
+    "init_state_ignored": ("        if (initial_state)\n            memcpy(kv,",
+                           "        if (0)\n            memcpy(kv,"),
+    "quad_init_exponent_t": ("pow(la, (double)(t + 1))", "pow(la, (double)(t))"),
+    "quad_init_transposed": ("acc += qt[i] * s0[(long)i * d + j]",
+                             "acc += qt[i] * s0[(long)j * d + i]"),
     "dec_read_before_update": (
         "                kv[(long)i * d + j] = la * kv[(long)i * d + j] + kb[i] * vb[j];\n"
         "        for (int j = 0; j < d; ++j) {\n"

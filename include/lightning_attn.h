@@ -98,6 +98,34 @@ la_status lightning_attn_prefill(const void *q, const void *k, const void *v,
                                  float *final_state, void *stream);
 
 /*
+ * Prefill that continues every sequence from a cached state (the prefix KV
+ * cache of MiniMax-01 report §3.3.1: a new segment of a sequence whose
+ * earlier tokens were already consumed into a d x d state).  With S0 =
+ * initial_state[s][h] the recursion starts at kv_{-1} = S0, so
+ *
+ *     o_t = sum_{u <= t} lambda^(t-u) (q_t . k_u) v_u + lambda^(t+1) q_t S0
+ *     final_state = lambda^L S0 + sum_u lambda^(L-1-u) k_u^T v_u
+ *
+ * (the result of one prefill over the earlier tokens and this segment
+ * together).  Arguments are those of lightning_attn_prefill plus
+ *
+ * initial_state  nullable; [num_seqs, num_heads, head_dim, head_dim] fp32,
+ *                same layout as final_state; NULL means zero states (then
+ *                the call equals lightning_attn_prefill).  It may be the
+ *                same array as final_state (the cache is updated in place:
+ *                every state is read before it is overwritten); any other
+ *                overlap of the two is rejected with LA_ERR_INVALID_ARG.  An
+ *                empty sequence's final state is its initial state.
+ */
+la_status lightning_attn_prefill_with_state(const void *q, const void *k, const void *v,
+                                            const float *decay, const int32_t *cu_seqlens,
+                                            int32_t num_seqs, int32_t total_tokens,
+                                            int32_t num_heads, int32_t head_dim,
+                                            int32_t chunk, la_dtype dtype,
+                                            const float *initial_state, void *out,
+                                            float *final_state, void *stream);
+
+/*
  * One decode step for a batch of sequences, each with one new token.
  *   (MiniMax-01 report §3.3.2: length-1 inputs get their own memory-bound
  *    kernel; §3.3.1: the KV computation and the prefix-KV-cache update are
@@ -145,7 +173,7 @@ const char *lightning_attn_last_error(void);
 /* ABI version of this header: (major << 16) | minor. */
 int32_t lightning_attn_version(void);
 
-#define LIGHTNING_ATTN_VERSION ((1 << 16) | 0)
+#define LIGHTNING_ATTN_VERSION ((1 << 16) | 1)
 
 #ifdef __cplusplus
 }

@@ -61,6 +61,10 @@ def load(path: str = LIB_PATH):
             lib.lightning_attn_prefill.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                                    i32, ctypes.c_int, vp, vp, vp]
             lib.lightning_attn_prefill.restype = ctypes.c_int
+            lib.lightning_attn_prefill_with_state.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32,
+                                                              i32, i32, ctypes.c_int, vp, vp,
+                                                              vp, vp]
+            lib.lightning_attn_prefill_with_state.restype = ctypes.c_int
             lib.lightning_attn_decode.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32,
                                                   ctypes.c_int, vp, vp]
             lib.lightning_attn_decode.restype = ctypes.c_int
@@ -109,7 +113,8 @@ def _stream_handle(stream) -> int:
 
 
 def prefill(q, k, v, decay, cu_seqlens=None, *, chunk: int = 0, out=None,
-            final_state=None, return_state: bool = True, stream=None):
+            final_state=None, return_state: bool = True, stream=None,
+            initial_state=None):
     """Chunkwise lightning-attention prefill.
 
     q, k, v: [T, H, d] (bf16 or fp32, same dtype, CUDA, contiguous), packed
@@ -117,6 +122,10 @@ def prefill(q, k, v, decay, cu_seqlens=None, *, chunk: int = 0, out=None,
     sequence of length T); decay: fp32 [H].  Returns ``(out, final_state)``
     with out [T, H, d] in the input dtype and final_state fp32
     [nseq, H, d, d] (None if ``return_state`` is False).
+
+    initial_state: optional fp32 [nseq, H, d, d] cached state each sequence
+    continues from (prefix KV cache); it may be passed as ``final_state``
+    too, to update the cache in place.
     """
     if q.dim() != 3:
         raise ValueError("q must be [T, H, d]")
@@ -135,13 +144,24 @@ def prefill(q, k, v, decay, cu_seqlens=None, *, chunk: int = 0, out=None,
         out = torch.empty_like(q)
     if final_state is None and return_state:
         final_state = torch.empty((nseq, H, d, d), dtype=torch.float32, device=q.device)
+    if initial_state is not None and (initial_state.dtype != torch.float32 or
+                                      tuple(initial_state.shape) != (nseq, H, d, d)):
+        raise ValueError("initial_state must be fp32 [nseq, H, d, d]")
     lib = load()
-    st = lib.lightning_attn_prefill(
-        _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(decay, "decay"),
-        _dev(cu_seqlens, "cu_seqlens"), nseq, T, H, d, int(chunk), _dtype_code(q),
-        _dev(out, "out"), None if final_state is None else _dev(final_state, "final_state"),
-        _stream_handle(stream))
-    _check(st, "lightning_attn_prefill")
+    fs = None if final_state is None else _dev(final_state, "final_state")
+    if initial_state is None:
+        st = lib.lightning_attn_prefill(
+            _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(decay, "decay"),
+            _dev(cu_seqlens, "cu_seqlens"), nseq, T, H, d, int(chunk), _dtype_code(q),
+            _dev(out, "out"), fs, _stream_handle(stream))
+        _check(st, "lightning_attn_prefill")
+    else:
+        st = lib.lightning_attn_prefill_with_state(
+            _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(decay, "decay"),
+            _dev(cu_seqlens, "cu_seqlens"), nseq, T, H, d, int(chunk), _dtype_code(q),
+            _dev(initial_state, "initial_state"), _dev(out, "out"), fs,
+            _stream_handle(stream))
+        _check(st, "lightning_attn_prefill_with_state")
     return out, final_state
 
 

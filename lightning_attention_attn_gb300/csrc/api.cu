@@ -54,12 +54,13 @@ const char *lightning_attn_last_error(void) { return g_last_error.c_str(); }
 
 int32_t lightning_attn_version(void) { return LIGHTNING_ATTN_VERSION; }
 
-la_status lightning_attn_prefill(const void *q, const void *k, const void *v,
-                                 const float *decay, const int32_t *cu_seqlens,
-                                 int32_t num_seqs, int32_t total_tokens,
-                                 int32_t num_heads, int32_t head_dim,
-                                 int32_t chunk, la_dtype dtype, void *out,
-                                 float *final_state, void *stream) {
+la_status lightning_attn_prefill_with_state(const void *q, const void *k, const void *v,
+                                            const float *decay, const int32_t *cu_seqlens,
+                                            int32_t num_seqs, int32_t total_tokens,
+                                            int32_t num_heads, int32_t head_dim,
+                                            int32_t chunk, la_dtype dtype,
+                                            const float *initial_state, void *out,
+                                            float *final_state, void *stream) {
     if (num_seqs < 0) return fail(LA_ERR_INVALID_ARG, "num_seqs < 0 (%d)", num_seqs);
     if (total_tokens < 0) return fail(LA_ERR_INVALID_ARG, "total_tokens < 0 (%d)", total_tokens);
     if (num_heads < 1) return fail(LA_ERR_INVALID_ARG, "num_heads < 1 (%d)", num_heads);
@@ -75,17 +76,31 @@ la_status lightning_attn_prefill(const void *q, const void *k, const void *v,
         return fail(LA_ERR_INVALID_ARG, "null q, k, v or out");
     if ((q && !aligned16(q)) || (k && !aligned16(k)) || (v && !aligned16(v)) ||
         (out && !aligned16(out)) || (final_state && !aligned16(final_state)) ||
-        !aligned16(decay) || !aligned16(cu_seqlens))
+        (initial_state && !aligned16(initial_state)) || !aligned16(decay) ||
+        !aligned16(cu_seqlens))
         return fail(LA_ERR_INVALID_ARG, "every pointer must be 16-byte aligned");
     if ((long long)num_seqs * num_heads > 0x7fffffffLL / 4)
         return fail(LA_ERR_INVALID_ARG, "num_seqs * num_heads too large");
+    const size_t state_bytes = (size_t)num_seqs * num_heads * head_dim * head_dim * sizeof(float);
+    if (initial_state && final_state && initial_state != final_state) {
+        const uintptr_t a0 = reinterpret_cast<uintptr_t>(initial_state);
+        const uintptr_t b0 = reinterpret_cast<uintptr_t>(final_state);
+        if (a0 < b0 + state_bytes && b0 < a0 + state_bytes)
+            return fail(LA_ERR_INVALID_ARG,
+                        "initial_state and final_state overlap without being the same array");
+    }
 
     la::PrefillArgs a{q, k, v, decay, cu_seqlens, num_seqs, total_tokens, num_heads,
-                      head_dim, chunk, out, final_state, static_cast<cudaStream_t>(stream)};
-    if (total_tokens == 0) {  // every sequence is empty: states are zero
-        if (!final_state) return LA_OK;
-        const size_t bytes = (size_t)num_seqs * num_heads * head_dim * head_dim * sizeof(float);
-        return from_cuda(cudaMemsetAsync(final_state, 0, bytes, a.stream), "prefill (empty)");
+                      head_dim, chunk, out, final_state, static_cast<cudaStream_t>(stream),
+                      initial_state};
+    if (total_tokens == 0) {  // every sequence is empty: each state is its cached state
+        if (!final_state || final_state == initial_state) return LA_OK;
+        if (initial_state)
+            return from_cuda(cudaMemcpyAsync(final_state, initial_state, state_bytes,
+                                             cudaMemcpyDeviceToDevice, a.stream),
+                             "prefill (empty)");
+        return from_cuda(cudaMemsetAsync(final_state, 0, state_bytes, a.stream),
+                         "prefill (empty)");
     }
     const bool tc = dtype == LA_DTYPE_BF16 && head_dim == 128 && (chunk == 0 || chunk == 128);
     if (tc) return from_cuda(la::prefill_tc_bf16(a), "prefill (tcgen05)");
@@ -94,6 +109,17 @@ la_status lightning_attn_prefill(const void *q, const void *k, const void *v,
                     "chunk %d needs the tensor-core path (bf16, head_dim 128)", chunk);
     if (dtype == LA_DTYPE_FP32) return from_cuda(la::prefill_simt_f32(a), "prefill (fp32)");
     return from_cuda(la::prefill_simt_bf16(a), "prefill (bf16, CUDA cores)");
+}
+
+la_status lightning_attn_prefill(const void *q, const void *k, const void *v,
+                                 const float *decay, const int32_t *cu_seqlens,
+                                 int32_t num_seqs, int32_t total_tokens,
+                                 int32_t num_heads, int32_t head_dim,
+                                 int32_t chunk, la_dtype dtype, void *out,
+                                 float *final_state, void *stream) {
+    return lightning_attn_prefill_with_state(q, k, v, decay, cu_seqlens, num_seqs, total_tokens,
+                                             num_heads, head_dim, chunk, dtype, nullptr, out,
+                                             final_state, stream);
 }
 
 la_status lightning_attn_decode(const void *q, const void *k, const void *v,

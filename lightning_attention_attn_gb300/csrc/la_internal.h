@@ -15,6 +15,7 @@ struct PrefillArgs {
     void *out;                  // [T, H, D]
     float *final_state;         // [nseq, H, D, D] or nullptr
     cudaStream_t stream;
+    const float *initial_state; // [nseq, H, D, D] or nullptr (zero state)
 };
 
 struct DecodeArgs {

@@ -7,6 +7,7 @@
 //   [(Q_i K_i^T) (.) M] V_i, inter-block right product Q_i KV_{i-1} and the
 //   recursive state update KV_i = lambda^{B_i} KV_{i-1} + (Lambda_K K_i)^T V_i,
 //   with the decay values (§3.3.1) computed in the kernel.
+// A sequence may continue from a cached state (initial_state): KV_{-1} = S0.
 // Exponents of lambda are never negative (lambda^(j-l) for j >= l,
 // lambda^(j+1), lambda^(B_i-1-l), lambda^(B_i)), so no factor can overflow;
 // B_i is the true length of the (possibly short) last chunk.
@@ -47,7 +48,7 @@ __global__ void __launch_bounds__(kThreads)
 prefill_simt_kernel(const T *__restrict__ q, const T *__restrict__ k,
                     const T *__restrict__ v, const float *__restrict__ decay,
                     const int32_t *__restrict__ cu, int nseq, int T_total, int H,
-                    T *__restrict__ out, float *__restrict__ final_state) {
+                    const float *initial_state, T *__restrict__ out, float *final_state) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     auto &sm = *reinterpret_cast<SimtSmem<D, B> *>(smem_raw);
     const int tid = threadIdx.x;
@@ -62,7 +63,11 @@ prefill_simt_kernel(const T *__restrict__ q, const T *__restrict__ k,
     const float lam = __ldg(decay + h);
 
     for (int e = tid; e <= B; e += kThreads) sm.pw[e] = powf(lam, (float)e);
-    for (int e = tid; e < D * D; e += kThreads) (&sm.kv[0][0])[e] = 0.f;
+    // KV_{-1}: the sequence's cached state (prefix KV cache, §3.3.1), else 0.
+    // initial_state may be final_state itself: it is read here, before any
+    // write of this CTA's final state.
+    const float *s0 = initial_state ? initial_state + ((long)s * H + h) * D * D : nullptr;
+    for (int e = tid; e < D * D; e += kThreads) (&sm.kv[0][0])[e] = s0 ? s0[e] : 0.f;
     __syncthreads();
 
     const long row_stride = (long)H * D;
@@ -143,7 +148,7 @@ cudaError_t launch(const PrefillArgs &a) {
     kern<<<(unsigned)grid, kThreads, smem, a.stream>>>(
         static_cast<const T *>(a.q), static_cast<const T *>(a.k),
         static_cast<const T *>(a.v), a.decay, a.cu_seqlens, a.nseq, a.total_tokens,
-        a.num_heads, static_cast<T *>(a.out), a.final_state);
+        a.num_heads, a.initial_state, static_cast<T *>(a.out), a.final_state);
     return cudaGetLastError();
 }
 

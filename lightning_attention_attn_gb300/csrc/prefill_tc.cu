@@ -180,7 +180,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                   const float *__restrict__ decay, const int32_t *__restrict__ cu, int nseq, int T,
-                  int H, __nv_bfloat16 *__restrict__ out, float *__restrict__ final_state) {
+                  int H, const float *initial_state, __nv_bfloat16 *__restrict__ out,
+                  float *final_state) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *base = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -198,6 +199,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     const int L = t1 - t0;
     const int nch = (L + BC - 1) / BC;
     const float lam = __ldg(decay + h);
+    // A sequence may continue from a cached state S0 (prefix KV cache,
+    // §3.3.1): KV_{-1} = S0 instead of 0.  initial_state may be final_state
+    // itself: every CTA reads its slice of S0 before it writes that slice.
+    const bool has_init = initial_state != nullptr;
 
     auto bar = [&](const uint64_t &b) { return smem_u32(&b); };
     const uint32_t pw_s = smem_u32(&cs.pw[0]);          // lambda^e at pw_s + 4 e
@@ -339,7 +344,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             const uint64_t dvh = sdesc_sw128(vha, kHalf, 1024);
             if (elect_one()) {
                 mma_group_ss<kMNMajorS1, kMNMajorS2, kMNMajorS1, kMNMajorS2>(
-                    tmem_mma + kColDKV, dk, dvh, kIdescKV, i > 0 ? 1u : 0u);
+                    tmem_mma + kColDKV, dk, dvh, kIdescKV, (i > 0 || has_init) ? 1u : 0u);
                 mma_commit(bar(cs.dkv_full));
                 mma_commit(bar(cs.empty_k[st]));
             }
@@ -553,15 +558,119 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
                 if (!load_k(c) || !load_q(c)) break;
         }
         __syncwarp();
-        // KV_{-1} = 0
+        // hi/lo bf16 copy of a state row for the Q KV MMA: hi = x with the
+        // low 16 bits cleared (a bf16, exact); lo = x - hi (exact in fp32),
+        // also truncated: hi + lo = x to about 2^-14 relative
+        auto store_kv_copy = [&](const float(&kv)[DV]) {
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            st_shared_v4(kvb + r * 128 + c * 16, 0u, 0u, 0u, 0u);
-            st_shared_v4(kvb + kHalf + r * 128 + c * 16, 0u, 0u, 0u, 0u);
+            for (int c = 0; c < 8; ++c) {
+                const uint32_t phys = (uint32_t)(c ^ (r & 7));
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const uint32_t ua = __float_as_uint(kv[8 * c + 2 * m]);
+                    const uint32_t ub = __float_as_uint(kv[8 * c + 2 * m + 1]);
+                    hi[m] = __byte_perm(ua, ub, 0x7632);
+                    const float2 l2 = f2_sub(make_float2(__uint_as_float(ua), __uint_as_float(ub)),
+                                             make_float2(__uint_as_float(ua & 0xffff0000u),
+                                                         __uint_as_float(ub & 0xffff0000u)));
+                    lo[m] = __byte_perm(__float_as_uint(l2.x), __float_as_uint(l2.y), 0x7632);
+                }
+                st_shared_v4(kvb + r * 128 + phys * 16, hi[0], hi[1], hi[2], hi[3]);
+                st_shared_v4(kvb + kHalf + r * 128 + phys * 16, lo[0], lo[1], lo[2], lo[3]);
+            }
+            fence_proxy_async_smem();
+        };
+        // lambda^{Lc} KV / 2 into both halves of the dKV accumulator, for
+        // the next dKV MMA to accumulate onto
+        auto write_back = [&](const float(&kv)[DV], float decay_to_next) {
+            const float dh = 0.5f * decay_to_next;
+            const float2 d2 = make_float2(dh, dh);
+#pragma unroll
+            for (int hh = 0; hh < 4; ++hh) {
+                uint32_t w[16];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const float2 x = f2_mul(make_float2(kv[16 * hh + 2 * c], kv[16 * hh + 2 * c + 1]), d2);
+                    w[2 * c] = __float_as_uint(x.x);
+                    w[2 * c + 1] = __float_as_uint(x.y);
+                }
+                tmem_st16(tkv + 16 * hh, w);
+                tmem_st16(tkv + 64 + 16 * hh, w);
+            }
+            tmem_wait_st();
+        };
+        if (has_init) {
+            // KV_{-1} = S0: row r, this CTA's 64 value columns, 16 at a time
+            const float4 *src = reinterpret_cast<const float4 *>(
+                initial_state + (((long)s * H + h) * D + r) * D + vs * DV);
+            float4 *dst = (nch == 0 && final_state)
+                              ? reinterpret_cast<float4 *>(
+                                    final_state + (((long)s * H + h) * D + r) * D + vs * DV)
+                              : nullptr;
+            const float dh = nch > 0 ? 0.5f * pw(min(BC, L)) : 0.f;
+            const float2 d2 = make_float2(dh, dh);
+#pragma unroll 1
+            for (int g = 0; g < 4; ++g) {
+                float x[16];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const float4 f = src[4 * g + c];
+                    x[4 * c] = f.x;
+                    x[4 * c + 1] = f.y;
+                    x[4 * c + 2] = f.z;
+                    x[4 * c + 3] = f.w;
+                }
+                if (dst) {  // empty sequence: the state is the cached one
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        dst[4 * g + c] = make_float4(x[4 * c], x[4 * c + 1], x[4 * c + 2], x[4 * c + 3]);
+                }
+#pragma unroll
+                for (int c2 = 0; c2 < 2; ++c2) {  // smem 16-byte chunks 2g, 2g + 1
+                    const int c = 2 * g + c2;
+                    const uint32_t phys = (uint32_t)(c ^ (r & 7));
+                    uint32_t hi[4], lo[4];
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        const uint32_t ua = __float_as_uint(x[8 * c2 + 2 * m]);
+                        const uint32_t ub = __float_as_uint(x[8 * c2 + 2 * m + 1]);
+                        hi[m] = __byte_perm(ua, ub, 0x7632);
+                        const float2 l2 =
+                            f2_sub(make_float2(__uint_as_float(ua), __uint_as_float(ub)),
+                                   make_float2(__uint_as_float(ua & 0xffff0000u),
+                                               __uint_as_float(ub & 0xffff0000u)));
+                        lo[m] = __byte_perm(__float_as_uint(l2.x), __float_as_uint(l2.y), 0x7632);
+                    }
+                    st_shared_v4(kvb + r * 128 + phys * 16, hi[0], hi[1], hi[2], hi[3]);
+                    st_shared_v4(kvb + kHalf + r * 128 + phys * 16, lo[0], lo[1], lo[2], lo[3]);
+                }
+                if (nch > 0) {
+                    uint32_t w[16];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const float2 y = f2_mul(make_float2(x[2 * c], x[2 * c + 1]), d2);
+                        w[2 * c] = __float_as_uint(y.x);
+                        w[2 * c + 1] = __float_as_uint(y.y);
+                    }
+                    tmem_st16(tkv + 16 * g, w);
+                    tmem_st16(tkv + 64 + 16 * g, w);
+                }
+            }
+            fence_proxy_async_smem();
+            tmem_wait_st();
+        } else {
+            // KV_{-1} = 0
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                st_shared_v4(kvb + r * 128 + c * 16, 0u, 0u, 0u, 0u);
+                st_shared_v4(kvb + kHalf + r * 128 + c * 16, 0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();
         }
-        fence_proxy_async_smem();
+        tc_fence_before();
         mbar_arrive(bar(cs.o2_ready));   // Q_0 KV_{-1} may go
-        mbar_arrive(bar(cs.dkv_ready));  // dKV_0 overwrites the accumulator
+        mbar_arrive(bar(cs.dkv_ready));  // dKV_0 accumulates onto lambda^{B_0} S0 (or overwrites)
 
         for (int i = 0; i < nch; ++i) {
             const int st = i & 1;
@@ -589,25 +698,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
                 }
             }
             if (!last) {
-                const float dh = 0.5f * pw(min(BC, L - (i + 1) * BC));
-                const float2 d2 = make_float2(dh, dh);
-#pragma unroll
-                for (int hh = 0; hh < 4; ++hh) {
-                    uint32_t w[16];
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const float2 x =
-                            f2_mul(make_float2(kv[16 * hh + 2 * c], kv[16 * hh + 2 * c + 1]), d2);
-                        w[2 * c] = __float_as_uint(x.x);
-                        w[2 * c + 1] = __float_as_uint(x.y);
-                    }
-                    tmem_st16(tkv + 16 * hh, w);
-                    tmem_st16(tkv + 64 + 16 * hh, w);
-                }
-                tmem_wait_st();
+                write_back(kv, pw(min(BC, L - (i + 1) * BC)));
             } else if (final_state) {
-                float4 *dst = reinterpret_cast<float4 *>(
-                    final_state + (((long)s * H + h) * D + r) * D + vs * DV);
+                float4 *dst = reinterpret_cast<float4 *>(final_state + (((long)s * H + h) * D + r) * D + vs * DV);
 #pragma unroll
                 for (int c = 0; c < DV / 4; ++c)
                     dst[c] = make_float4(kv[4 * c], kv[4 * c + 1], kv[4 * c + 2], kv[4 * c + 3]);
@@ -619,30 +712,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             // ---- copy ----
             if (!warp_wait(bar(cs.o2_full), ph, abort_flag)) break;
             tc_fence_after();
-            if (!last) {
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    // hi = x with the low 16 bits cleared (a bf16, exact);
-                    // lo = x - hi (exact in fp32), also truncated:
-                    // hi + lo = x to about 2^-14 relative
-                    const uint32_t phys = (uint32_t)(c ^ (r & 7));
-                    uint32_t hi[4], lo[4];
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        const uint32_t ua = __float_as_uint(kv[8 * c + 2 * m]);
-                        const uint32_t ub = __float_as_uint(kv[8 * c + 2 * m + 1]);
-                        hi[m] = __byte_perm(ua, ub, 0x7632);
-                        const float2 l2 =
-                            f2_sub(make_float2(__uint_as_float(ua), __uint_as_float(ub)),
-                                   make_float2(__uint_as_float(ua & 0xffff0000u),
-                                               __uint_as_float(ub & 0xffff0000u)));
-                        lo[m] = __byte_perm(__float_as_uint(l2.x), __float_as_uint(l2.y), 0x7632);
-                    }
-                    st_shared_v4(kvb + r * 128 + phys * 16, hi[0], hi[1], hi[2], hi[3]);
-                    st_shared_v4(kvb + kHalf + r * 128 + phys * 16, lo[0], lo[1], lo[2], lo[3]);
-                }
-                fence_proxy_async_smem();
-            }
+            if (!last) store_kv_copy(kv);
             if (loader && i + 2 < nch) load_q(i + 2);
             __syncwarp();
             // ---- O2 ----
@@ -706,9 +776,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
                 mbar_wait(bar(cs.full_k[c & 1]), (c >> 1) & 1, &no_abort, kTimeoutNs);
         }
         __syncwarp();
-        if (nch == 0 && final_state) {  // empty sequence: the state stays zero
-            float4 *dst = reinterpret_cast<float4 *>(final_state + (((long)s * H + h) * D + r) * D +
-                                                     vs * DV);
+        if (nch == 0 && final_state && !has_init) {  // empty sequence: the state stays zero
+            float4 *dst = reinterpret_cast<float4 *>(final_state + (((long)s * H + h) * D + r) * D + vs * DV);
 #pragma unroll
             for (int c = 0; c < DV / 4; ++c) dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
@@ -898,7 +967,7 @@ cudaError_t prefill_tc_bf16(const PrefillArgs &a) {
     if (grid > 0x7fffffffL) return cudaErrorInvalidConfiguration;
     prefill_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, a.stream>>>(
         mq, mk, mv, mo, a.decay, a.cu_seqlens, a.nseq, a.total_tokens, a.num_heads,
-        static_cast<__nv_bfloat16 *>(a.out), a.final_state);
+        a.initial_state, static_cast<__nv_bfloat16 *>(a.out), a.final_state);
     return cudaGetLastError();
 }
 

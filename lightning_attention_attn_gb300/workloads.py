@@ -13,6 +13,7 @@ Recipe (all draws from a ``torch.Generator`` seeded explicitly):
   * varlen: sequence lengths uniform in [lo, hi] (``torch.randint``), packed
     back to back, ``cu_seqlens`` = int32 exclusive prefix sum.
   * decode: state ~ N(0, 1) * 0.02 in fp32, one fresh token per sequence.
+  * cached states a prefill continues from: ~ N(0, 1) * 0.3 in fp32.
 """
 from __future__ import annotations
 
@@ -85,6 +86,14 @@ def prefill_inputs(lengths, num_heads: int, head_dim: int,
     q, k, v = _qkv(g, (T, num_heads, head_dim), dtype, device)
     lam = decay_schedule(num_heads) if decay is None else decay.to(torch.float32)
     return PrefillInputs(q, k, v, lam.to(device), cu.to(device))
+
+
+def cached_states(num_seqs: int, num_heads: int, head_dim: int, std: float = 0.3,
+                  seed: int = 0, device="cpu") -> torch.Tensor:
+    """A seeded stand-in for a prefix KV cache: fp32 [nseq, H, d, d] ~ N(0, std^2)."""
+    g = _gen(seed, device)
+    return torch.randn((num_seqs, num_heads, head_dim, head_dim), generator=g,
+                       dtype=torch.float32, device=device) * std
 
 
 @dataclass

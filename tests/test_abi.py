@@ -19,7 +19,8 @@ def lib():
 
 def test_header_declares_expected_calls():
     names = la.header_functions()
-    for n in ("lightning_attn_prefill", "lightning_attn_decode",
+    for n in ("lightning_attn_prefill", "lightning_attn_prefill_with_state",
+              "lightning_attn_decode",
               "lightning_attn_status_string", "lightning_attn_last_error",
               "lightning_attn_version", "lightning_attn_device_status",
               "lightning_attn_selftest_wait_timeout"):
@@ -36,7 +37,7 @@ def test_library_exports_every_header_symbol(lib):
 
 
 def test_version(lib):
-    assert la.version() == (1, 0)
+    assert la.version() == (1, 1)
 
 
 def test_status_strings(lib):
@@ -78,6 +79,27 @@ def _prefill(lib, **kw):
 ])
 def test_prefill_host_validation(lib, kw, status):
     assert _prefill(lib, **kw) == status
+
+
+def _prefill_state(lib, init, **kw):
+    args = dict(q=A, k=A, v=A, decay=A, cu=A, nseq=1, T=8, H=2, d=128, chunk=0,
+                dtype=la.LA_DTYPE_BF16, out=A, fs=A + 0x100000, stream=None)
+    args.update(kw)
+    return lib.lightning_attn_prefill_with_state(
+        args["q"], args["k"], args["v"], args["decay"], args["cu"], args["nseq"], args["T"],
+        args["H"], args["d"], args["chunk"], args["dtype"], init, args["out"], args["fs"],
+        args["stream"])
+
+
+@pytest.mark.parametrize("init, kw, status", [
+    (A + 4, {}, la.LA_ERR_INVALID_ARG),                      # misaligned cached state
+    (A + 0x100000 + 16, {}, la.LA_ERR_INVALID_ARG),          # overlaps final_state partly
+    (A + 0x100000 - 16, {}, la.LA_ERR_INVALID_ARG),          # overlaps final_state partly
+    (A, dict(H=0), la.LA_ERR_INVALID_ARG),
+    (A, dict(nseq=0), la.LA_OK),
+])
+def test_prefill_with_state_host_validation(lib, init, kw, status):
+    assert _prefill_state(lib, init, **kw) == status
     if status != la.LA_OK:
         assert lib.lightning_attn_last_error().decode() != ""
 

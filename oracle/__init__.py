@@ -12,6 +12,7 @@ Sources followed (MiniMax-01 technical report, CSDN full translation):
   * Fig. 12 caption -- the diagonal decay matrix: weight lambda_h^(t-u)
   * §3.2 "data packing" -- packed sequences are independent
   * §3.3.1 prefix KV cache -- a sequence may continue from a cached state
+  * gradients of the left product for training (§2.2.1, §2.2.2)
 Parity pins: tests/test_oracle.py (golden hand examples, closed forms,
 two-form agreement, exact rational brute force, invariants).
 """
@@ -62,8 +63,10 @@ def _declare(lib):
     lib.la_oracle_decode.argtypes = [_dp, _dp, _dp, _dp, _dp, ctypes.c_int,
                                      ctypes.c_int, ctypes.c_int, _dp, ctypes.c_int]
     lib.la_oracle_max_threads.argtypes = [ctypes.c_int]
+    lib.la_oracle_backward.argtypes = [_dp, _dp, _dp, _dp, _ip, ctypes.c_int, ctypes.c_int,
+                                       ctypes.c_int, _dp, _dp, _dp, _dp, ctypes.c_int]
     for f in (lib.la_oracle_quadratic, lib.la_oracle_recurrent,
-              lib.la_oracle_decode, lib.la_oracle_max_threads):
+              lib.la_oracle_decode, lib.la_oracle_max_threads, lib.la_oracle_backward):
         f.restype = ctypes.c_int
     return lib
 
@@ -195,6 +198,24 @@ def decode(q, k, v, decay, state, nthreads=0, lib=None):
     if rc:
         raise ValueError(f"la_oracle_decode failed ({rc})")
     return out, st
+
+
+def backward(q, k, v, decay, cu_seqlens, dout, nthreads=0, lib=None):
+    """Gradients (dq, dk, dv) [T, H, d] fp64 of sum_t dout_t . o_t, with o
+    the left-product form (zero state at each sequence start)."""
+    lib = lib or load()
+    q, k, v, g = _f64(q), _f64(k), _f64(v), _f64(dout)
+    lam = _f64(decay_as_seen(decay))
+    cu = _i32(cu_seqlens)
+    T, H, d = _shape(q)
+    assert cu[-1] == T and g.shape == q.shape
+    dq, dk, dv = (np.zeros((T, H, d), dtype=np.float64) for _ in range(3))
+    rc = lib.la_oracle_backward(_ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp), _ptr(lam, _dp),
+                                _ptr(cu, _ip), len(cu) - 1, H, d, _ptr(g, _dp),
+                                _ptr(dq, _dp), _ptr(dk, _dp), _ptr(dv, _dp), nthreads)
+    if rc:
+        raise ValueError(f"la_oracle_backward failed ({rc})")
+    return dq, dk, dv
 
 
 def max_threads(nthreads: int = 0) -> int:

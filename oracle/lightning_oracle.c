@@ -216,3 +216,61 @@ int la_oracle_decode(const double *q, const double *k, const double *v,
     }
     return 0;
 }
+
+/*
+ * Gradients of the quadratic form (training, §2.2.1 and the report's TGS
+ * measurements of §2.2.2): for a loss with dL/do_t = dout_t,
+ *   dq_t = sum_{u<=t} lambda^(t-u) (dout_t . v_u) k_u
+ *   dk_u = sum_{t>=u} lambda^(t-u) (dout_t . v_u) q_t
+ *   dv_u = sum_{t>=u} lambda^(t-u) (q_t . k_u) dout_t
+ * per sequence and head (zero state at every sequence start), written out
+ * term by term from o_t = sum_{u<=t} lambda^(t-u) (q_t . k_u) v_u.
+ * All arrays [T, H, d]; dq, dk, dv are overwritten.  O(L^2 d) per
+ * (sequence, head).
+ */
+int la_oracle_backward(const double *q, const double *k, const double *v,
+                       const double *lam, const int32_t *cu, int nseq, int H,
+                       int d, const double *dout, double *dq, double *dk,
+                       double *dv, int nthreads)
+{
+    if (check_cu(cu, nseq) || H <= 0 || d <= 0) return 1;
+    set_threads(nthreads);
+    const long row = (long)H * d;
+    const long npairs = (long)nseq * H;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long p = 0; p < npairs; ++p) {
+        const int s = (int)(p / H), h = (int)(p % H);
+        const long t0 = cu[s], L = cu[s + 1] - cu[s];
+        const double la = lam[h];
+        for (long t = 0; t < L; ++t)
+            for (int j = 0; j < d; ++j) {
+                const long o = (t0 + t) * row + (long)h * d + j;
+                dq[o] = 0.0;
+                dk[o] = 0.0;
+                dv[o] = 0.0;
+            }
+        for (long t = 0; t < L; ++t) {
+            const double *qt = q + (t0 + t) * row + (long)h * d;
+            const double *gt = dout + (t0 + t) * row + (long)h * d;
+            double *dqt = dq + (t0 + t) * row + (long)h * d;
+            for (long u = 0; u <= t; ++u) {
+                const double *ku = k + (t0 + u) * row + (long)h * d;
+                const double *vu = v + (t0 + u) * row + (long)h * d;
+                double *dku = dk + (t0 + u) * row + (long)h * d;
+                double *dvu = dv + (t0 + u) * row + (long)h * d;
+                const double w = pow(la, (double)(t - u));
+                double g_v = 0.0, q_k = 0.0;   /* dout_t . v_u, q_t . k_u */
+                for (int i = 0; i < d; ++i) {
+                    g_v += gt[i] * vu[i];
+                    q_k += qt[i] * ku[i];
+                }
+                for (int i = 0; i < d; ++i) {
+                    dqt[i] += w * g_v * ku[i];
+                    dku[i] += w * g_v * qt[i];
+                    dvu[i] += w * q_k * gt[i];
+                }
+            }
+        }
+    }
+    return 0;
+}

@@ -49,6 +49,59 @@ def pin_golden_prefill(lib, name):
                                    err_msg=f"{name} {form}")
 
 
+def pin_golden_backward(lib):
+    g = golden("hand_example_backward.json")
+    dq, dk, dv = oracle.backward(g["q"], g["k"], g["v"], g["lambda"], g["cu_seqlens"],
+                                 g["dout"], lib=lib)
+    for got, name in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
+        np.testing.assert_allclose(got, g[name], rtol=0, atol=1e-15, err_msg=name)
+
+
+def pin_backward_finite_differences(lib):
+    """The loss sum_t dout_t . o_t is linear in each of q, k and v, so a
+    central difference of the (separately pinned) forward form with step 1
+    is that argument's exact gradient, up to rounding."""
+    rng = np.random.default_rng(10)
+    lengths, H, d = [5, 0, 7], 2, 3
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    T = int(cu[-1])
+    q, k, v = rnd(rng, T, H, d)
+    g = rng.standard_normal((T, H, d))
+    lam = [0.6, 0.95]
+
+    def loss(q_, k_, v_):
+        return float(np.sum(oracle.quadratic(q_, k_, v_, lam, cu, lib=lib) * g))
+
+    grads = oracle.backward(q, k, v, lam, cu, g, lib=lib)
+    for which, grad in enumerate(grads):
+        num = np.zeros_like(grad)
+        for idx in np.ndindex(T, H, d):
+            args_p = [q.copy(), k.copy(), v.copy()]
+            args_m = [q.copy(), k.copy(), v.copy()]
+            args_p[which][idx] += 1.0
+            args_m[which][idx] -= 1.0
+            num[idx] = 0.5 * (loss(*args_p) - loss(*args_m))
+        np.testing.assert_allclose(grad, num, rtol=1e-10, atol=1e-10,
+                                   err_msg="dq dk dv"[3 * which:3 * which + 2])
+
+
+def pin_backward_lambda_one(lib):
+    """lambda = 1: dq_t = dout_t (prefix sum of v k^T), dk_u = (suffix sum
+    of q dout^T) v_u, dv_u = (suffix sum of dout q^T) k_u (numpy cumsum)."""
+    rng = np.random.default_rng(11)
+    T, H, d = 19, 2, 4
+    q, k, v = rnd(rng, T, H, d)
+    g = rng.standard_normal((T, H, d))
+    pre_vk = np.cumsum(np.einsum("thi,thj->thij", v, k), axis=0)
+    suf_qg = np.cumsum(np.einsum("thi,thj->thij", q, g)[::-1], axis=0)[::-1]
+    want_dq = np.einsum("thi,thij->thj", g, pre_vk)
+    want_dk = np.einsum("thij,thj->thi", suf_qg, v)
+    want_dv = np.einsum("thij,thi->thj", suf_qg, k)
+    dq, dk, dv = oracle.backward(q, k, v, [1.0, 1.0], [0, T], g, lib=lib)
+    for got, want in ((dq, want_dq), (dk, want_dk), (dv, want_dv)):
+        np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+
+
 def pin_golden_decode(lib):
     g = golden("hand_example_decode.json")
     out, st = oracle.decode(g["q"], g["k"], g["v"], g["lambda"], g["state"], lib=lib)
@@ -256,6 +309,9 @@ ALL_PINS = {
     "golden_packed": lambda lib: pin_golden_prefill(lib, "hand_example_packed.json"),
     "golden_state": lambda lib: pin_golden_prefill(lib, "hand_example_state.json"),
     "golden_decode": pin_golden_decode,
+    "golden_backward": pin_golden_backward,
+    "backward_fd": pin_backward_finite_differences,
+    "backward_lambda_one": pin_backward_lambda_one,
     "geometric_d1_state": pin_geometric_d1_with_state,
     "prefix_cache": pin_prefix_cache_equivalence,
     "geometric_d1": pin_geometric_d1,
@@ -279,6 +335,18 @@ def lib():
                                   "hand_example_packed.json", "hand_example_state.json"])
 def test_golden_prefill(lib, name):
     pin_golden_prefill(lib, name)
+
+
+def test_golden_backward(lib):
+    pin_golden_backward(lib)
+
+
+def test_backward_finite_differences(lib):
+    pin_backward_finite_differences(lib)
+
+
+def test_backward_lambda_one(lib):
+    pin_backward_lambda_one(lib)
 
 
 def test_golden_decode(lib):
@@ -371,6 +439,9 @@ MUTANTS = {
     "quad_init_exponent_t": ("pow(la, (double)(t + 1))", "pow(la, (double)(t))"),
     "quad_init_transposed": ("acc += qt[i] * s0[(long)i * d + j]",
                              "acc += qt[i] * s0[(long)j * d + i]"),
+    "bwd_dk_uses_k": ("dku[i] += w * g_v * qt[i]", "dku[i] += w * g_v * ku[i]"),
+    "bwd_dv_wrong_dot": ("dvu[i] += w * q_k * gt[i]", "dvu[i] += w * g_v * gt[i]"),
+    "bwd_dq_no_decay": ("dqt[i] += w * g_v * ku[i]", "dqt[i] += g_v * ku[i]"),
     "dec_read_before_update": (
         "                kv[(long)i * d + j] = la * kv[(long)i * d + j] + kb[i] * vb[j];\n"
         "        for (int j = 0; j < d; ++j) {\n"

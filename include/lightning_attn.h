@@ -147,6 +147,43 @@ la_status lightning_attn_decode(const void *q, const void *k, const void *v,
                                 void *stream);
 
 /*
+ * Gradients for training (MiniMax-01 report §2.2.1; §2.2.2 measures the
+ * training speed of lightning attention): given dout = dL/do for the outputs
+ * of lightning_attn_prefill on the same arguments (zero initial states),
+ *
+ *     dq_t = sum_{u <= t} lambda^(t-u) (dout_t . v_u) k_u
+ *     dk_u = sum_{t >= u} lambda^(t-u) (dout_t . v_u) q_t
+ *     dv_u = sum_{t >= u} lambda^(t-u) (q_t . k_u) dout_t
+ *
+ * per sequence and head.  dq is the forward form applied to (dout, v, k);
+ * dk and dv are the forward form in reversed time, so the call runs the
+ * prefill kernels three times (same dtype / head_dim / chunk rules and
+ * precision as lightning_attn_prefill) plus six time-reversal copies through
+ * `workspace`.
+ *
+ * q, k, v, d_out          [total_tokens, num_heads, head_dim], dtype `dtype`
+ * d_q, d_k, d_v           outputs, same shape and dtype; distinct arrays,
+ *                         none of them equal to an input
+ * workspace               caller-owned device memory, 256-byte aligned, of at
+ *                         least lightning_attn_backward_workspace_bytes(...)
+ *                         bytes; its contents are scratch (overwritten)
+ * other arguments         as for lightning_attn_prefill.
+ * Gradients with respect to decay, to a cached initial state or from a
+ * final-state loss are not computed.
+ */
+la_status lightning_attn_backward(const void *q, const void *k, const void *v,
+                                  const float *decay, const int32_t *cu_seqlens,
+                                  int32_t num_seqs, int32_t total_tokens, int32_t num_heads,
+                                  int32_t head_dim, int32_t chunk, la_dtype dtype,
+                                  const void *d_out, void *d_q, void *d_k, void *d_v,
+                                  void *workspace, int64_t workspace_bytes, void *stream);
+
+/* Bytes of workspace lightning_attn_backward needs (four [T, H, d] arrays,
+ * each rounded up to 256 bytes); -1 for invalid arguments. */
+int64_t lightning_attn_backward_workspace_bytes(int32_t total_tokens, int32_t num_heads,
+                                                int32_t head_dim, la_dtype dtype);
+
+/*
  * Synchronises `stream`, then reports whether a kernel of this library raised
  * its device error word since the last call (and clears it).  The
  * tensor-core prefill bounds every wait of its pipeline (about 2 s); a wait
@@ -173,7 +210,7 @@ const char *lightning_attn_last_error(void);
 /* ABI version of this header: (major << 16) | minor. */
 int32_t lightning_attn_version(void);
 
-#define LIGHTNING_ATTN_VERSION ((1 << 16) | 1)
+#define LIGHTNING_ATTN_VERSION ((1 << 16) | 2)
 
 #ifdef __cplusplus
 }

@@ -65,6 +65,12 @@ def load(path: str = LIB_PATH):
                                                               i32, i32, ctypes.c_int, vp, vp,
                                                               vp, vp]
             lib.lightning_attn_prefill_with_state.restype = ctypes.c_int
+            lib.lightning_attn_backward.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                                    ctypes.c_int, vp, vp, vp, vp, vp,
+                                                    ctypes.c_int64, vp]
+            lib.lightning_attn_backward.restype = ctypes.c_int
+            lib.lightning_attn_backward_workspace_bytes.argtypes = [i32, i32, i32, ctypes.c_int]
+            lib.lightning_attn_backward_workspace_bytes.restype = ctypes.c_int64
             lib.lightning_attn_decode.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32,
                                                   ctypes.c_int, vp, vp]
             lib.lightning_attn_decode.restype = ctypes.c_int
@@ -163,6 +169,53 @@ def prefill(q, k, v, decay, cu_seqlens=None, *, chunk: int = 0, out=None,
             _stream_handle(stream))
         _check(st, "lightning_attn_prefill_with_state")
     return out, final_state
+
+
+def backward_workspace_bytes(total_tokens: int, num_heads: int, head_dim: int,
+                             dtype=torch.bfloat16) -> int:
+    """Bytes of device workspace :func:`backward` needs."""
+    code = LA_DTYPE_BF16 if dtype == torch.bfloat16 else LA_DTYPE_FP32
+    n = int(load().lightning_attn_backward_workspace_bytes(total_tokens, num_heads, head_dim,
+                                                             code))
+    if n < 0:
+        raise ValueError("invalid sizes for the backward workspace")
+    return n
+
+
+def backward(q, k, v, decay, cu_seqlens, dout, *, chunk: int = 0, dq=None, dk=None,
+             dv=None, workspace=None, stream=None):
+    """Gradients (dq, dk, dv) of sum_t dout_t . o_t for o = prefill(q, k, v,
+    decay, cu_seqlens) (zero initial states).  Shapes and dtypes as in
+    :func:`prefill`; ``workspace`` is a uint8 CUDA tensor of at least
+    :func:`backward_workspace_bytes` bytes (allocated here when None).
+    """
+    if q.dim() != 3:
+        raise ValueError("q must be [T, H, d]")
+    T, H, d = q.shape
+    for name, t in (("k", k), ("v", v), ("dout", dout)):
+        if t.shape != q.shape or t.dtype != q.dtype:
+            raise ValueError(f"{name} must match q in shape and dtype")
+    if cu_seqlens is None:
+        cu_seqlens = torch.tensor([0, T], dtype=torch.int32, device=q.device)
+    if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1:
+        raise ValueError("cu_seqlens must be a 1-D int32 tensor")
+    if decay.dtype != torch.float32 or decay.numel() != H:
+        raise ValueError("decay must be fp32 [H]")
+    nseq = cu_seqlens.numel() - 1
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    need = backward_workspace_bytes(T, H, d, q.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    st = load().lightning_attn_backward(
+        _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(decay, "decay"),
+        _dev(cu_seqlens, "cu_seqlens"), nseq, T, H, d, int(chunk), _dtype_code(q),
+        _dev(dout, "dout"), _dev(dq, "dq"), _dev(dk, "dk"), _dev(dv, "dv"),
+        _dev(workspace, "workspace"), int(workspace.numel() * workspace.element_size()),
+        _stream_handle(stream))
+    _check(st, "lightning_attn_backward")
+    return dq, dk, dv
 
 
 def decode(q, k, v, decay, state, *, out=None, stream=None):

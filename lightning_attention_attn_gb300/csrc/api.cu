@@ -35,6 +35,27 @@ la_status from_cuda(cudaError_t e, const char *what) {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Runs the forward kernel that serves (dtype, head_dim, chunk); arguments
+// already validated.
+la_status run_prefill(const la::PrefillArgs &a, la_dtype dtype) {
+    const bool tc = dtype == LA_DTYPE_BF16 && a.head_dim == 128 && (a.chunk == 0 || a.chunk == 128);
+    if (tc) return from_cuda(la::prefill_tc_bf16(a), "prefill (tcgen05)");
+    if (a.chunk == 128 || a.chunk == 256)
+        return fail(LA_ERR_UNSUPPORTED,
+                    "chunk %d needs the tensor-core path (bf16, head_dim 128)", a.chunk);
+    if (dtype == LA_DTYPE_FP32) return from_cuda(la::prefill_simt_f32(a), "prefill (fp32)");
+    return from_cuda(la::prefill_simt_bf16(a), "prefill (bf16, CUDA cores)");
+}
+
+size_t elem_bytes(la_dtype dtype) { return dtype == LA_DTYPE_FP32 ? 4 : 2; }
+
+// Workspace of the backward pass: four [T, H, d] arrays, each 256-byte aligned.
+size_t backward_slot_bytes(int32_t total_tokens, int32_t num_heads, int32_t head_dim,
+                           la_dtype dtype) {
+    const size_t b = (size_t)total_tokens * num_heads * head_dim * elem_bytes(dtype);
+    return (b + 255) & ~(size_t)255;
+}
+
 }  // namespace
 
 extern "C" {
@@ -102,13 +123,7 @@ la_status lightning_attn_prefill_with_state(const void *q, const void *k, const 
         return from_cuda(cudaMemsetAsync(final_state, 0, state_bytes, a.stream),
                          "prefill (empty)");
     }
-    const bool tc = dtype == LA_DTYPE_BF16 && head_dim == 128 && (chunk == 0 || chunk == 128);
-    if (tc) return from_cuda(la::prefill_tc_bf16(a), "prefill (tcgen05)");
-    if (chunk == 128 || chunk == 256)
-        return fail(LA_ERR_UNSUPPORTED,
-                    "chunk %d needs the tensor-core path (bf16, head_dim 128)", chunk);
-    if (dtype == LA_DTYPE_FP32) return from_cuda(la::prefill_simt_f32(a), "prefill (fp32)");
-    return from_cuda(la::prefill_simt_bf16(a), "prefill (bf16, CUDA cores)");
+    return run_prefill(a, dtype);
 }
 
 la_status lightning_attn_prefill(const void *q, const void *k, const void *v,
@@ -144,6 +159,85 @@ la_status lightning_attn_decode(const void *q, const void *k, const void *v,
                      static_cast<cudaStream_t>(stream)};
     if (dtype == LA_DTYPE_FP32) return from_cuda(la::decode_f32(a), "decode (fp32)");
     return from_cuda(la::decode_bf16(a), "decode (bf16)");
+}
+
+int64_t lightning_attn_backward_workspace_bytes(int32_t total_tokens, int32_t num_heads,
+                                                int32_t head_dim, la_dtype dtype) {
+    if (total_tokens < 0 || num_heads < 1 || (head_dim != 64 && head_dim != 128) ||
+        (dtype != LA_DTYPE_BF16 && dtype != LA_DTYPE_FP32))
+        return -1;
+    return (int64_t)(4 * backward_slot_bytes(total_tokens, num_heads, head_dim, dtype));
+}
+
+la_status lightning_attn_backward(const void *q, const void *k, const void *v,
+                                  const float *decay, const int32_t *cu_seqlens,
+                                  int32_t num_seqs, int32_t total_tokens, int32_t num_heads,
+                                  int32_t head_dim, int32_t chunk, la_dtype dtype,
+                                  const void *d_out, void *d_q, void *d_k, void *d_v,
+                                  void *workspace, int64_t workspace_bytes, void *stream) {
+    if (num_seqs < 0) return fail(LA_ERR_INVALID_ARG, "num_seqs < 0 (%d)", num_seqs);
+    if (total_tokens < 0) return fail(LA_ERR_INVALID_ARG, "total_tokens < 0 (%d)", total_tokens);
+    if (num_heads < 1) return fail(LA_ERR_INVALID_ARG, "num_heads < 1 (%d)", num_heads);
+    if (head_dim != 64 && head_dim != 128)
+        return fail(LA_ERR_INVALID_ARG, "head_dim must be 64 or 128 (got %d)", head_dim);
+    if (dtype != LA_DTYPE_BF16 && dtype != LA_DTYPE_FP32)
+        return fail(LA_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+    if (chunk != 0 && chunk != 16 && chunk != 32 && chunk != 64 && chunk != 128 && chunk != 256)
+        return fail(LA_ERR_INVALID_ARG, "chunk must be 0, 16, 32, 64, 128 or 256 (got %d)", chunk);
+    if (num_seqs == 0 || total_tokens == 0) return LA_OK;
+    if (!cu_seqlens || !decay) return fail(LA_ERR_INVALID_ARG, "null decay or cu_seqlens");
+    const void *ptrs[] = {q, k, v, d_out, d_q, d_k, d_v, workspace};
+    for (const void *p : ptrs)
+        if (!p) return fail(LA_ERR_INVALID_ARG, "null tensor or workspace pointer");
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return fail(LA_ERR_INVALID_ARG, "every pointer must be 16-byte aligned");
+    if (!aligned16(decay) || !aligned16(cu_seqlens))
+        return fail(LA_ERR_INVALID_ARG, "every pointer must be 16-byte aligned");
+    if ((long long)num_seqs * num_heads > 0x7fffffffLL / 4)
+        return fail(LA_ERR_INVALID_ARG, "num_seqs * num_heads too large");
+    // outputs are distinct arrays, none of them an input
+    const void *outs[] = {d_q, d_k, d_v};
+    const void *ins[] = {q, k, v, d_out};
+    for (int i = 0; i < 3; ++i) {
+        for (int j = 0; j < 4; ++j)
+            if (outs[i] == ins[j]) return fail(LA_ERR_INVALID_ARG, "a gradient aliases an input");
+        for (int j = i + 1; j < 3; ++j)
+            if (outs[i] == outs[j]) return fail(LA_ERR_INVALID_ARG, "two gradients share an array");
+    }
+    const size_t slot = backward_slot_bytes(total_tokens, num_heads, head_dim, dtype);
+    if (workspace_bytes < 0 || (size_t)workspace_bytes < 4 * slot)
+        return fail(LA_ERR_INVALID_ARG, "workspace too small: %lld bytes, %zu needed",
+                    (long long)workspace_bytes, 4 * slot);
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(LA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    char *ws = static_cast<char *>(workspace);
+    void *rq = ws, *rg = ws + slot, *rkv = ws + 2 * slot, *rout = ws + 3 * slot;
+    const size_t row = (size_t)num_heads * head_dim * elem_bytes(dtype);
+    auto fwd = [&](const void *a, const void *b, const void *c, void *o) {
+        la::PrefillArgs pa{a, b, c, decay, cu_seqlens, num_seqs, total_tokens, num_heads,
+                           head_dim, chunk, o, nullptr, st, nullptr};
+        return run_prefill(pa, dtype);
+    };
+    auto rev = [&](const void *in, void *out) {
+        return from_cuda(la::reverse_sequences(in, out, cu_seqlens, num_seqs, total_tokens, row, st),
+                         "backward (time reversal)");
+    };
+    la_status r;
+    // dq_t = sum_{u<=t} lambda^(t-u) (dout_t . v_u) k_u: the forward form
+    // with (q, k, v) -> (dout, v, k)
+    if ((r = fwd(d_out, v, k, d_q)) != LA_OK) return r;
+    // dv_u = sum_{t>=u} lambda^(t-u) (q_t . k_u) dout_t: the forward form in
+    // reversed time with (q, k, v) -> (k, q, dout)
+    if ((r = rev(q, rq)) != LA_OK || (r = rev(d_out, rg)) != LA_OK || (r = rev(k, rkv)) != LA_OK)
+        return r;
+    if ((r = fwd(rkv, rq, rg, rout)) != LA_OK || (r = rev(rout, d_v)) != LA_OK) return r;
+    // dk_u = sum_{t>=u} lambda^(t-u) (dout_t . v_u) q_t: reversed time with
+    // (q, k, v) -> (v, dout, q)
+    if ((r = rev(v, rkv)) != LA_OK) return r;
+    if ((r = fwd(rkv, rg, rq, rout)) != LA_OK || (r = rev(rout, d_k)) != LA_OK) return r;
+    return LA_OK;
 }
 
 la_status lightning_attn_device_status(void *stream) {

@@ -40,6 +40,11 @@ cudaError_t take_device_error(cudaStream_t stream, unsigned int *err);
 // Launches a kernel whose bounded wait must time out after timeout_ns.
 cudaError_t selftest_wait_timeout(uint64_t timeout_ns, cudaStream_t stream);
 
+// out row (cu[s] + cu[s+1] - 1 - t) = in row t for every token t of
+// sequence s; rows are row_bytes long (a multiple of 16).  in != out.
+cudaError_t reverse_sequences(const void *in, void *out, const int32_t *cu_seqlens, int nseq,
+                              int total_tokens, size_t row_bytes, cudaStream_t stream);
+
 // Memory-bound decode step; head_dim in {64, 128}.
 cudaError_t decode_f32(const DecodeArgs &a);
 cudaError_t decode_bf16(const DecodeArgs &a);

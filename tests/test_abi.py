@@ -20,6 +20,7 @@ def lib():
 def test_header_declares_expected_calls():
     names = la.header_functions()
     for n in ("lightning_attn_prefill", "lightning_attn_prefill_with_state",
+              "lightning_attn_backward", "lightning_attn_backward_workspace_bytes",
               "lightning_attn_decode",
               "lightning_attn_status_string", "lightning_attn_last_error",
               "lightning_attn_version", "lightning_attn_device_status",
@@ -37,7 +38,7 @@ def test_library_exports_every_header_symbol(lib):
 
 
 def test_version(lib):
-    assert la.version() == (1, 1)
+    assert la.version() == (1, 2)
 
 
 def test_status_strings(lib):
@@ -147,3 +148,41 @@ def test_product_path_does_not_import_oracle():
                 text = open(os.path.join(root, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "lightning_oracle" not in text, f
+
+
+def test_backward_workspace_bytes(lib):
+    f = lib.lightning_attn_backward_workspace_bytes
+    assert f(8192, 64, 128, la.LA_DTYPE_BF16) == 4 * 8192 * 64 * 128 * 2
+    assert f(3, 1, 64, la.LA_DTYPE_FP32) == 4 * 768          # 768 B per array, 256-aligned
+    assert f(0, 4, 128, la.LA_DTYPE_BF16) == 0
+    assert f(-1, 4, 128, la.LA_DTYPE_BF16) == -1
+    assert f(8, 4, 96, la.LA_DTYPE_BF16) == -1
+
+
+W = 0x200000  # 256-byte aligned fake workspace address
+
+
+def _backward(lib, **kw):
+    args = dict(q=A, k=A + 0x10, v=A + 0x20, decay=A, cu=A, nseq=1, T=8, H=2, d=128, chunk=0,
+                dtype=la.LA_DTYPE_BF16, g=A + 0x30, dq=A + 0x40000, dk=A + 0x50000,
+                dv=A + 0x60000, ws=W, wsb=1 << 20, stream=None)
+    args.update(kw)
+    return lib.lightning_attn_backward(
+        args["q"], args["k"], args["v"], args["decay"], args["cu"], args["nseq"], args["T"],
+        args["H"], args["d"], args["chunk"], args["dtype"], args["g"], args["dq"], args["dk"],
+        args["dv"], args["ws"], args["wsb"], args["stream"])
+
+
+@pytest.mark.parametrize("kw, status", [
+    (dict(ws=None), la.LA_ERR_INVALID_ARG),
+    (dict(wsb=100), la.LA_ERR_INVALID_ARG),                 # workspace too small
+    (dict(ws=W + 16), la.LA_ERR_INVALID_ARG),               # workspace not 256-aligned
+    (dict(dq=A), la.LA_ERR_INVALID_ARG),                    # gradient aliases q
+    (dict(dk=A + 0x40000), la.LA_ERR_INVALID_ARG),          # dk is dq
+    (dict(g=A + 8), la.LA_ERR_INVALID_ARG),                 # misaligned
+    (dict(d=96), la.LA_ERR_INVALID_ARG),
+    (dict(nseq=0), la.LA_OK),
+    (dict(T=0), la.LA_OK),
+])
+def test_backward_host_validation(lib, kw, status):
+    assert _backward(lib, **kw) == status

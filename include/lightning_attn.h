@@ -184,6 +184,32 @@ int64_t lightning_attn_backward_workspace_bytes(int32_t total_tokens, int32_t nu
                                                 int32_t head_dim, la_dtype dtype);
 
 /*
+ * lightning_attn_backward without a caller workspace (the paper has no
+ * counterpart; this is a convenience of this library).  For callers that
+ * cannot allocate device memory at call time -- code under another
+ * framework's memory manager that forbids raw cudaMalloc, or a loop that
+ * must not call cudaMalloc because it can synchronise the device -- the
+ * scratch comes from one fixed array of lightning_attn_backward_noalloc_max_bytes()
+ * bytes (64 MiB) that every GPU loading the library holds until the process
+ * exits.  Arguments and results are those of lightning_attn_backward; a call
+ * whose lightning_attn_backward_workspace_bytes() exceeds the array returns
+ * LA_ERR_INVALID_ARG before touching the GPU.  The first call on a device
+ * looks up the array's device address (cudaGetSymbolAddress) with that
+ * device current; make that first call before any stream capture.  The
+ * array is shared by all calls: calls that overlap on the GPU race on it;
+ * calls ordered on one stream do not.  Nothing is allocated.
+ */
+la_status lightning_attn_backward_noalloc(const void *q, const void *k, const void *v,
+                                          const float *decay, const int32_t *cu_seqlens,
+                                          int32_t num_seqs, int32_t total_tokens,
+                                          int32_t num_heads, int32_t head_dim, int32_t chunk,
+                                          la_dtype dtype, const void *d_out, void *d_q,
+                                          void *d_k, void *d_v, void *stream);
+
+/* Size in bytes of the fixed scratch array of lightning_attn_backward_noalloc. */
+int64_t lightning_attn_backward_noalloc_max_bytes(void);
+
+/*
  * Synchronises `stream`, then reports whether a kernel of this library raised
  * its device error word since the last call (and clears it).  The
  * tensor-core prefill bounds every wait of its pipeline (about 2 s); a wait

@@ -58,6 +58,17 @@ size_t backward_slot_bytes(int32_t total_tokens, int32_t num_heads, int32_t head
 
 }  // namespace
 
+namespace la {
+void set_last_error(const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+}
+}  // namespace la
+
 extern "C" {
 
 const char *lightning_attn_status_string(la_status s) {

@@ -1,0 +1,93 @@
+// lightning_attn_backward_noalloc: the backward pass with its scratch space
+// in a fixed array inside this library instead of a caller workspace.
+//
+// Who needs it: callers that cannot allocate device memory when they call
+// the backward pass -- for example code running under another framework's
+// memory manager, which owns the device pool and does not allow raw
+// cudaMalloc calls, or a serving or training loop that must not call
+// cudaMalloc in its steady state because cudaMalloc can synchronise the
+// device.  Such callers still pass their inputs and outputs; only the
+// scratch of the time-reversed copies comes from here.
+//
+// The array lives in device memory of every GPU that loads the library, from
+// module load until the process exits.  Its address is looked up once per
+// device (cudaGetSymbolAddress on the first call made with that device
+// current); the array's name in host code is only a stand-in for the symbol
+// and must never be passed to a kernel.  All calls share the one array, so
+// calls that overlap on the GPU (different streams, or different host
+// threads, without ordering between them) race on it and give wrong results;
+// calls serialised on one stream are safe.  Nothing in the array needs to
+// start at zero: every byte the backward pass reads from it was written
+// earlier in the same call.
+#include <cstdint>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "la_internal.h"
+#include "lightning_attn.h"
+
+namespace la {
+namespace {
+
+constexpr size_t kScratchBytes = size_t(64) << 20;  // 64 MiB
+
+static __device__ __align__(256) unsigned char g_backward_scratch[kScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void *g_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_backward_scratch on the current device (looked up on
+// the first call for that device).
+cudaError_t scratch_address(void **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_backward_scratch);
+        if (e != cudaSuccess) return e;
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace la
+
+extern "C" int64_t lightning_attn_backward_noalloc_max_bytes(void) {
+    return (int64_t)la::kScratchBytes;
+}
+
+extern "C" la_status lightning_attn_backward_noalloc(
+    const void *q, const void *k, const void *v, const float *decay, const int32_t *cu_seqlens,
+    int32_t num_seqs, int32_t total_tokens, int32_t num_heads, int32_t head_dim, int32_t chunk,
+    la_dtype dtype, const void *d_out, void *d_q, void *d_k, void *d_v, void *stream) {
+    const int64_t need =
+        lightning_attn_backward_workspace_bytes(total_tokens, num_heads, head_dim, dtype);
+    if (need > (int64_t)la::kScratchBytes) {
+        la::set_last_error(
+            "backward_noalloc: %lld bytes of scratch needed (total_tokens * num_heads * "
+            "head_dim too large), the built-in array holds %lld",
+            (long long)need, (long long)la::kScratchBytes);
+        return LA_ERR_INVALID_ARG;
+    }
+    if (need < 0 || num_seqs <= 0 || total_tokens <= 0)  // argument errors and empty calls
+        return lightning_attn_backward(q, k, v, decay, cu_seqlens, num_seqs, total_tokens,
+                                       num_heads, head_dim, chunk, dtype, d_out, d_q, d_k, d_v,
+                                       nullptr, 0, stream);
+    void *scratch = nullptr;
+    const cudaError_t e = la::scratch_address(&scratch);
+    if (e != cudaSuccess) {
+        la::set_last_error("backward_noalloc: scratch address lookup failed: %s",
+                           cudaGetErrorString(e));
+        return LA_ERR_CUDA;
+    }
+    return lightning_attn_backward(q, k, v, decay, cu_seqlens, num_seqs, total_tokens, num_heads,
+                                   head_dim, chunk, dtype, d_out, d_q, d_k, d_v, scratch,
+                                   (int64_t)la::kScratchBytes, stream);
+}

@@ -45,6 +45,9 @@ cudaError_t selftest_wait_timeout(uint64_t timeout_ns, cudaStream_t stream);
 cudaError_t reverse_sequences(const void *in, void *out, const int32_t *cu_seqlens, int nseq,
                               int total_tokens, size_t row_bytes, cudaStream_t stream);
 
+// Sets the message lightning_attn_last_error() returns on this host thread.
+void set_last_error(const char *fmt, ...) __attribute__((format(printf, 1, 2)));
+
 // Memory-bound decode step; head_dim in {64, 128}.
 cudaError_t decode_f32(const DecodeArgs &a);
 cudaError_t decode_bf16(const DecodeArgs &a);

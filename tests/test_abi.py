@@ -186,3 +186,18 @@ def _backward(lib, **kw):
 ])
 def test_backward_host_validation(lib, kw, status):
     assert _backward(lib, **kw) == status
+
+
+def test_backward_noalloc_rejects_sizes_beyond_its_array(lib):
+    f = lib.lightning_attn_backward_noalloc
+    f.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int32] * 5 + [ctypes.c_int] + \
+        [ctypes.c_void_p] * 5
+    f.restype = ctypes.c_int
+    lib.lightning_attn_backward_noalloc_max_bytes.restype = ctypes.c_int64
+    cap = lib.lightning_attn_backward_noalloc_max_bytes()
+    assert cap == 64 << 20
+    T = cap // (4 * 64 * 128 * 2) + 1  # one token more than the array holds (bf16)
+    st = f(A, A, A, A, A, 1, T, 64, 128, 0, la.LA_DTYPE_BF16, A, A + 0x40000, A + 0x50000,
+           A + 0x60000, None)
+    assert st == la.LA_ERR_INVALID_ARG
+    assert "scratch" in lib.lightning_attn_last_error().decode()

@@ -312,6 +312,43 @@ def run_ours(args, ws, rank, local):
                            "kernel": "decode_kernel", "alg_bytes_per_launch": dbytes}}
     del dinp
 
+    # ---------------- backward on the same 8K-token layer (training step of
+    # the attention; three prefill launches plus six time-reversal copies)
+    g = torch.Generator(device=dev)
+    g.manual_seed(1)
+    dout = torch.randn(inp.q.shape, generator=g, device=dev).to(torch.bfloat16)
+    dq, dk, dv = (torch.empty_like(inp.q) for _ in range(3))
+    bws = torch.empty(la.backward_workspace_bytes(T, H, d, torch.bfloat16), dtype=torch.uint8,
+                      device=dev)
+
+    def bstep():
+        la.backward(inp.q, inp.k, inp.v, inp.decay, inp.cu_seqlens, dout, dq=dq, dk=dk, dv=dv,
+                    workspace=bws, stream=stream)
+
+    for _ in range(3):
+        bstep()
+    torch.cuda.synchronize()
+    b0 = torch.cuda.Event(enable_timing=True)
+    b1 = torch.cuda.Event(enable_timing=True)
+    b0.record(stream)
+    for _ in range(K):
+        bstep()
+    b1.record(stream)
+    torch.cuda.synchronize()
+    la.device_status(stream)
+    bms = b0.elapsed_time(b1) / K
+    bbytes = T * H * d * 2 * 7  # q, k, v, dout read; dq, dk, dv written (bf16)
+    bgbs = bbytes / (bms / 1e3) / 1e9
+    backward = {"value": round(T / (bms / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(bms, 4),
+                "config": {"workload": "prefill_8k backward (dq, dk, dv)"},
+                "launches_per_step": 9,
+                "roofline": {"bound": "hbm", "achieved": round(bgbs, 1), "peak": pk["hbm"],
+                             "unit": "GB/s", "frac": round(bgbs / pk["hbm"], 4),
+                             "alg_bytes_per_step": bbytes,
+                             "note": "algorithmic bytes of the gradients; the implementation "
+                                     "runs 3 prefill launches + 6 time-reversal copies"}}
+    del dout, dq, dk, dv, bws
+
     # ---------------- end to end through the public call, host buffers
     hq, hk, hv = (t.cpu().pin_memory() for t in (inp.q, inp.k, inp.v))
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
@@ -351,7 +388,8 @@ def run_ours(args, ws, rank, local):
                    "head_dim": d, "chunk": B, "value_slices_per_head": 2,
                    "inputs_vs_l2": "q, k, v = 384 MiB > 129 MB L2; no flush needed",
                    "parallelism": f"replicas x{ws}"},
-        "roofline": roofline, "tensor": tensor, "decode": decode, "e2e": e2e,
+        "roofline": roofline, "tensor": tensor, "decode": decode, "backward": backward,
+        "e2e": e2e,
         "gpu_launches": K,
     }
     clocks = clk.summary()

@@ -783,13 +783,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         }
     } else if (warp < kVWarp0 + 4) {
         // ================= V-tile warpgroup =================
-        // Chunk i's V tile, one row (token) per thread, in three steps:
-        //  0. max |v| over the tile (exchanged among the four warps while
-        //     step 1 runs), as soon as the tile has landed;
+        // Chunk i's V tile, one row (token) per thread, read from shared
+        // memory once into registers, then:
+        //  0. max |v| of the row, exchanged among the four warps (for the
+        //     tile's fp16 scale) while step 1 runs;
         //  1. Vhat = Lambda_K V as a hi/lo bf16 pair for the dKV MMA (Vhat_i
         //     may be written once dKV_{i-1} has read Vhat_{i-1});
-        //  2. V itself, converted in place to fp16 with the chunk's
-        //     power-of-two scale for the P V MMA.
+        //  2. V itself, written back in place as fp16 with the chunk's
+        //     power-of-two scale, for the P V MMA.
         // Rows past the chunk end are zero in both.
         const int w4 = warp - kVWarp0;
         const int vr = w4 * 32 + lane;
@@ -800,14 +801,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             const int Lc = min(BC, L - i * BC);
             const bool live = vr < Lc;
             const uint32_t row = vslot(st) + vr * 128;
+            // 16-byte pieces in the row's swizzled order (conflict-free)
+            uint4 x[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) x[c] = ld_shared_v4(row + (uint32_t)((c + vr) & 7) * 16);
             // ---- 0: max |v| (bf16 magnitudes, packed)
             {
                 uint32_t mbits = 0;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
-                    const uint4 x = ld_shared_v4(row + (uint32_t)((c + vr) & 7) * 16);
-                    mbits = __vmaxu2(__vmaxu2(mbits, x.x & 0x7fff7fffu), x.y & 0x7fff7fffu);
-                    mbits = __vmaxu2(__vmaxu2(mbits, x.z & 0x7fff7fffu), x.w & 0x7fff7fffu);
+                    mbits = __vmaxu2(__vmaxu2(mbits, x[c].x & 0x7fff7fffu), x[c].y & 0x7fff7fffu);
+                    mbits = __vmaxu2(__vmaxu2(mbits, x[c].z & 0x7fff7fffu), x[c].w & 0x7fff7fffu);
                 }
                 if (!live) mbits = 0;
                 float m = fmaxf(__uint_as_float(mbits << 16), __uint_as_float(mbits & 0xffff0000u));
@@ -818,8 +822,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             }
             // ---- 1: Vhat.  lambda^(Lc-1-l) split as g_hi + g_lo (bf16
             // each) so that the packed bf16 FMAs give hi + lo = v g to ~16
-            // bits.  The loops stay rolled: the three roles of an SM
-            // sub-partition share its instruction cache.
+            // bits.
             if (i > 0 && !warp_wait(bar(cs.dkv_full), (i - 1) & 1, abort_flag)) break;
             {
                 const float g = live ? pw(Lc - 1 - vr) : 0.f;
@@ -830,8 +833,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     const uint32_t ch = (uint32_t)((c + vr) & 7) * 16;
-                    const uint4 x = ld_shared_v4(row + ch);
-                    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+                    const uint32_t w[4] = {x[c].x, x[c].y, x[c].z, x[c].w};
                     uint32_t hi[4], lo[4];
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
@@ -865,8 +867,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
                 const uint32_t ch = (uint32_t)((c + vr) & 7) * 16;
-                const uint4 x = ld_shared_v4(row + ch);
-                const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+                const uint32_t w[4] = {x[c].x, x[c].y, x[c].z, x[c].w};
                 uint32_t hv[4];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {

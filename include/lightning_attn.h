@@ -158,7 +158,7 @@ la_status lightning_attn_decode(const void *q, const void *k, const void *v,
  * per sequence and head.  dq is the forward form applied to (dout, v, k);
  * dk and dv are the forward form in reversed time, so the call runs the
  * prefill kernels three times (same dtype / head_dim / chunk rules and
- * precision as lightning_attn_prefill) plus six time-reversal copies through
+ * precision as lightning_attn_prefill) plus four time-reversal copies through
  * `workspace`.
  *
  * q, k, v, d_out          [total_tokens, num_heads, head_dim], dtype `dtype`
@@ -178,7 +178,7 @@ la_status lightning_attn_backward(const void *q, const void *k, const void *v,
                                   const void *d_out, void *d_q, void *d_k, void *d_v,
                                   void *workspace, int64_t workspace_bytes, void *stream);
 
-/* Bytes of workspace lightning_attn_backward needs (four [T, H, d] arrays,
+/* Bytes of workspace lightning_attn_backward needs (three [T, H, d] arrays,
  * each rounded up to 256 bytes); -1 for invalid arguments. */
 int64_t lightning_attn_backward_workspace_bytes(int32_t total_tokens, int32_t num_heads,
                                                 int32_t head_dim, la_dtype dtype);

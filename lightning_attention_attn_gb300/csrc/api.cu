@@ -49,7 +49,7 @@ la_status run_prefill(const la::PrefillArgs &a, la_dtype dtype) {
 
 size_t elem_bytes(la_dtype dtype) { return dtype == LA_DTYPE_FP32 ? 4 : 2; }
 
-// Workspace of the backward pass: four [T, H, d] arrays, each 256-byte aligned.
+// Workspace of the backward pass: three [T, H, d] arrays, each 256-byte aligned.
 size_t backward_slot_bytes(int32_t total_tokens, int32_t num_heads, int32_t head_dim,
                            la_dtype dtype) {
     const size_t b = (size_t)total_tokens * num_heads * head_dim * elem_bytes(dtype);
@@ -177,7 +177,7 @@ int64_t lightning_attn_backward_workspace_bytes(int32_t total_tokens, int32_t nu
     if (total_tokens < 0 || num_heads < 1 || (head_dim != 64 && head_dim != 128) ||
         (dtype != LA_DTYPE_BF16 && dtype != LA_DTYPE_FP32))
         return -1;
-    return (int64_t)(4 * backward_slot_bytes(total_tokens, num_heads, head_dim, dtype));
+    return (int64_t)(3 * backward_slot_bytes(total_tokens, num_heads, head_dim, dtype));
 }
 
 la_status lightning_attn_backward(const void *q, const void *k, const void *v,
@@ -216,19 +216,19 @@ la_status lightning_attn_backward(const void *q, const void *k, const void *v,
             if (outs[i] == outs[j]) return fail(LA_ERR_INVALID_ARG, "two gradients share an array");
     }
     const size_t slot = backward_slot_bytes(total_tokens, num_heads, head_dim, dtype);
-    if (workspace_bytes < 0 || (size_t)workspace_bytes < 4 * slot)
+    if (workspace_bytes < 0 || (size_t)workspace_bytes < 3 * slot)
         return fail(LA_ERR_INVALID_ARG, "workspace too small: %lld bytes, %zu needed",
-                    (long long)workspace_bytes, 4 * slot);
+                    (long long)workspace_bytes, 3 * slot);
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
         return fail(LA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
 
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     char *ws = static_cast<char *>(workspace);
-    void *rq = ws, *rg = ws + slot, *rkv = ws + 2 * slot, *rout = ws + 3 * slot;
+    void *rq = ws, *rg = ws + slot, *rkv = ws + 2 * slot;
     const size_t row = (size_t)num_heads * head_dim * elem_bytes(dtype);
-    auto fwd = [&](const void *a, const void *b, const void *c, void *o) {
+    auto fwd = [&](const void *a, const void *b, const void *c, void *o, bool reverse_out) {
         la::PrefillArgs pa{a, b, c, decay, cu_seqlens, num_seqs, total_tokens, num_heads,
-                           head_dim, chunk, o, nullptr, st, nullptr};
+                           head_dim, chunk, o, nullptr, st, nullptr, reverse_out};
         return run_prefill(pa, dtype);
     };
     auto rev = [&](const void *in, void *out) {
@@ -238,16 +238,17 @@ la_status lightning_attn_backward(const void *q, const void *k, const void *v,
     la_status r;
     // dq_t = sum_{u<=t} lambda^(t-u) (dout_t . v_u) k_u: the forward form
     // with (q, k, v) -> (dout, v, k)
-    if ((r = fwd(d_out, v, k, d_q)) != LA_OK) return r;
+    if ((r = fwd(d_out, v, k, d_q, false)) != LA_OK) return r;
     // dv_u = sum_{t>=u} lambda^(t-u) (q_t . k_u) dout_t: the forward form in
-    // reversed time with (q, k, v) -> (k, q, dout)
+    // reversed time with (q, k, v) -> (k, q, dout); the launch writes its
+    // output rows back in forward time order
     if ((r = rev(q, rq)) != LA_OK || (r = rev(d_out, rg)) != LA_OK || (r = rev(k, rkv)) != LA_OK)
         return r;
-    if ((r = fwd(rkv, rq, rg, rout)) != LA_OK || (r = rev(rout, d_v)) != LA_OK) return r;
+    if ((r = fwd(rkv, rq, rg, d_v, true)) != LA_OK) return r;
     // dk_u = sum_{t>=u} lambda^(t-u) (dout_t . v_u) q_t: reversed time with
     // (q, k, v) -> (v, dout, q)
     if ((r = rev(v, rkv)) != LA_OK) return r;
-    if ((r = fwd(rkv, rg, rq, rout)) != LA_OK || (r = rev(rout, d_k)) != LA_OK) return r;
+    if ((r = fwd(rkv, rg, rq, d_k, true)) != LA_OK) return r;
     return LA_OK;
 }
 

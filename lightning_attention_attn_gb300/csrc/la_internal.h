@@ -16,6 +16,7 @@ struct PrefillArgs {
     float *final_state;         // [nseq, H, D, D] or nullptr
     cudaStream_t stream;
     const float *initial_state; // [nseq, H, D, D] or nullptr (zero state)
+    bool reverse_out = false;   // write o_t of sequence s to row cu[s] + cu[s+1] - 1 - t
 };
 
 struct DecodeArgs {

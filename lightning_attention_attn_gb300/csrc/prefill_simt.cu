@@ -48,7 +48,8 @@ __global__ void __launch_bounds__(kThreads)
 prefill_simt_kernel(const T *__restrict__ q, const T *__restrict__ k,
                     const T *__restrict__ v, const float *__restrict__ decay,
                     const int32_t *__restrict__ cu, int nseq, int T_total, int H,
-                    const float *initial_state, T *__restrict__ out, float *final_state) {
+                    const float *initial_state, T *__restrict__ out, float *final_state,
+                    int reverse_out) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     auto &sm = *reinterpret_cast<SimtSmem<D, B> *>(smem_raw);
     const int tid = threadIdx.x;
@@ -114,7 +115,9 @@ prefill_simt_kernel(const T *__restrict__ q, const T *__restrict__ k,
 #pragma unroll 8
             for (int i = 0; i < D; ++i) inter = fmaf(sm.q[j][i], sm.kv[i][n], inter);
             const float o = fmaf(sm.pw[j + 1], inter, intra);
-            out[(long)(t0 + c0 + j) * row_stride + (long)h * D + n] = from_f<T>(o);
+            // with reverse_out the sequence is written back to front
+            const long row = reverse_out ? (long)(t1 - 1 - c0 - j) : (long)(t0 + c0 + j);
+            out[row * row_stride + (long)h * D + n] = from_f<T>(o);
         }
         __syncthreads();  // everyone has read KV_{i-1}
 
@@ -148,7 +151,8 @@ cudaError_t launch(const PrefillArgs &a) {
     kern<<<(unsigned)grid, kThreads, smem, a.stream>>>(
         static_cast<const T *>(a.q), static_cast<const T *>(a.k),
         static_cast<const T *>(a.v), a.decay, a.cu_seqlens, a.nseq, a.total_tokens,
-        a.num_heads, a.initial_state, static_cast<T *>(a.out), a.final_state);
+        a.num_heads, a.initial_state, static_cast<T *>(a.out), a.final_state,
+        a.reverse_out ? 1 : 0);
     return cudaGetLastError();
 }
 

@@ -181,7 +181,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                   const float *__restrict__ decay, const int32_t *__restrict__ cu, int nseq, int T,
                   int H, const float *initial_state, __nv_bfloat16 *__restrict__ out,
-                  float *final_state) {
+                  float *final_state, int reverse_out) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *base = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -743,7 +743,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
                              ld_shared_f32(vscale_s + 4u * (uint32_t)(i & 3));
             const float qf = pw(r + 1);
             const float2 s12 = make_float2(s1, s1), qf2 = make_float2(qf, qf);
-            uint4 *orow = reinterpret_cast<uint4 *>(out + ((long)(t0 + i * BC + r) * H + h) * D +
+            // token row of o_r; with reverse_out the sequence is written back
+            // to front (the backward pass's reversed-time launches)
+            const long orow_t = reverse_out ? (long)(t1 - 1 - i * BC - r) : (long)(t0 + i * BC + r);
+            uint4 *orow = reinterpret_cast<uint4 *>(out + (orow_t * H + h) * D +
                                                     vs * DV);
 #pragma unroll
             for (int hh = 0; hh < 4; ++hh) {
@@ -968,7 +971,7 @@ cudaError_t prefill_tc_bf16(const PrefillArgs &a) {
     if (grid > 0x7fffffffL) return cudaErrorInvalidConfiguration;
     prefill_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, a.stream>>>(
         mq, mk, mv, mo, a.decay, a.cu_seqlens, a.nseq, a.total_tokens, a.num_heads,
-        a.initial_state, static_cast<__nv_bfloat16 *>(a.out), a.final_state);
+        a.initial_state, static_cast<__nv_bfloat16 *>(a.out), a.final_state, a.reverse_out ? 1 : 0);
     return cudaGetLastError();
 }
 

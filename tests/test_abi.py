@@ -152,8 +152,8 @@ def test_product_path_does_not_import_oracle():
 
 def test_backward_workspace_bytes(lib):
     f = lib.lightning_attn_backward_workspace_bytes
-    assert f(8192, 64, 128, la.LA_DTYPE_BF16) == 4 * 8192 * 64 * 128 * 2
-    assert f(3, 1, 64, la.LA_DTYPE_FP32) == 4 * 768          # 768 B per array, 256-aligned
+    assert f(8192, 64, 128, la.LA_DTYPE_BF16) == 3 * 8192 * 64 * 128 * 2
+    assert f(3, 1, 64, la.LA_DTYPE_FP32) == 3 * 768          # 768 B per array, 256-aligned
     assert f(0, 4, 128, la.LA_DTYPE_BF16) == 0
     assert f(-1, 4, 128, la.LA_DTYPE_BF16) == -1
     assert f(8, 4, 96, la.LA_DTYPE_BF16) == -1
@@ -196,7 +196,7 @@ def test_backward_noalloc_rejects_sizes_beyond_its_array(lib):
     lib.lightning_attn_backward_noalloc_max_bytes.restype = ctypes.c_int64
     cap = lib.lightning_attn_backward_noalloc_max_bytes()
     assert cap == 64 << 20
-    T = cap // (4 * 64 * 128 * 2) + 1  # one token more than the array holds (bf16)
+    T = cap // (3 * 64 * 128 * 2) + 1  # one token more than the array holds (bf16)
     st = f(A, A, A, A, A, 1, T, 64, 128, 0, la.LA_DTYPE_BF16, A, A + 0x40000, A + 0x50000,
            A + 0x60000, None)
     assert st == la.LA_ERR_INVALID_ARG

@@ -234,3 +234,18 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     assert lib.lightning_attn_device_status(stream.cuda_stream) == la.LA_OK
     inp, out, st, ref, ref_st = run_case([200], 2, 128, torch.bfloat16, seed=11)
     check(out, st, ref, ref_st, TOL_BF16)
+
+
+@pytest.mark.parametrize("s_qk, s_v", [(1e-3, 1.0), (30.0, 1.0), (1.0, 1e-4), (1.0, 3000.0)])
+def test_tensor_core_input_magnitudes(s_qk, s_v):
+    """The fp16 operands of the tensor-core path (P per row, V per chunk) carry
+    exact power-of-two scales: inputs far from unit size keep the bound."""
+    inp = wl.prefill_inputs([300, 129], 4, 128, dtype=torch.bfloat16, seed=5, device="cuda")
+    q = (inp.q.float() * s_qk).to(torch.bfloat16)
+    k = (inp.k.float() * s_qk).to(torch.bfloat16)
+    v = (inp.v.float() * s_v).to(torch.bfloat16)
+    out, st = la.prefill(q, k, v, inp.decay, inp.cu_seqlens, chunk=128)
+    torch.cuda.synchronize()
+    ref, ref_st = oracle.recurrent(q, k, v, inp.decay, inp.cu_seqlens.cpu())
+    assert torch.isfinite(out.float()).all() and torch.isfinite(st).all()
+    check(out, st, ref, ref_st, TOL_BF16, what=f"tc magnitudes q,k x{s_qk} v x{s_v}")

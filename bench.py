@@ -419,6 +419,13 @@ def run_only(args):
         fs = torch.empty((1, cfg["num_heads"], 128, 128), device="cuda")
         for _ in range(args.warmup + args.steps):
             la.prefill(inp.q, inp.k, inp.v, inp.decay, inp.cu_seqlens, out=out, final_state=fs)
+    elif args.only == "backward":
+        cfg = wl.PREFILL_8K
+        inp = wl.prefill_inputs(cfg["lengths"], cfg["num_heads"], cfg["head_dim"],
+                                dtype=torch.bfloat16, seed=0, device="cuda")
+        dout = torch.randn_like(inp.q, dtype=torch.float32).to(torch.bfloat16)
+        for _ in range(args.warmup + args.steps):
+            la.backward(inp.q, inp.k, inp.v, inp.decay, inp.cu_seqlens, dout)
     else:
         cfg = wl.DECODE_128
         n = args.warmup + args.steps
@@ -474,7 +481,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--only", choices=["prefill", "decode"], default=None,
+    ap.add_argument("--only", choices=["prefill", "decode", "backward"], default=None,
                     help="profiling aid: run just W + K launches of one kernel on its "
                          "workload and print nothing else")
     args = ap.parse_args(argv)

@@ -349,6 +349,50 @@ def run_ours(args, ws, rank, local):
                                      "runs 3 prefill launches + 4 time-reversal copies"}}
     del dout, dq, dk, dv, bws
 
+    # ---------------- mixed serving step (decode + prefill on two streams):
+    # 128 sequences x 64 heads with cached states, two of them with 256 new
+    # tokens, the rest one new token
+    mlen = [256 if s_ in (0, 77) else 1 for s_ in range(128)]
+    minp = wl.prefill_inputs(mlen, H, d, dtype=torch.bfloat16, seed=2, device=dev)
+    mstate = wl.cached_states(len(mlen), H, d, seed=3, device=dev)
+    mcu = minp.cu_seqlens.cpu().tolist()
+    mout = torch.empty_like(minp.q)
+    dstream = torch.cuda.Stream(device=dev)
+
+    def mstep(two):
+        if two:
+            la.mixed_step(minp.q, minp.k, minp.v, minp.decay, minp.cu_seqlens, mstate, out=mout,
+                          prefill_stream=stream, decode_stream=dstream, cu_seqlens_host=mcu)
+        else:  # the same update through one prefill launch for every sequence
+            la.prefill(minp.q, minp.k, minp.v, minp.decay, minp.cu_seqlens, out=mout,
+                       initial_state=mstate, final_state=mstate, stream=stream)
+
+    mixed = {"config": {"workload": "mixed step: 128 sequences x 64 heads, 2 with 256 new "
+                                    "tokens, 126 with 1, cached fp32 states"}}
+    for two in (True, False):
+        for _ in range(3):
+            mstep(two)
+        torch.cuda.synchronize()
+        m0 = torch.cuda.Event(enable_timing=True)
+        m1 = torch.cuda.Event(enable_timing=True)
+        m0.record(stream)
+        for _ in range(K):
+            mstep(two)
+        m1.record(stream)
+        torch.cuda.synchronize()
+        mixed["ms_two_streams" if two else "ms_one_prefill_launch"] = round(
+            m0.elapsed_time(m1) / K, 4)
+    la.device_status(stream)
+    mbytes = len(mlen) * H * d * d * 4 * 2 + sum(mlen) * H * d * 2 * 4
+    mixed["tokens_per_s"] = round(sum(mlen) / (mixed["ms_two_streams"] / 1e3), 1)
+    mixed["speedup_vs_one_launch"] = round(mixed["ms_one_prefill_launch"] /
+                                           mixed["ms_two_streams"], 2)
+    mixed["roofline"] = {"bound": "hbm", "alg_bytes_per_step": mbytes,
+                         "achieved": round(mbytes / (mixed["ms_two_streams"] / 1e3) / 1e9, 1),
+                         "peak": pk["hbm"], "unit": "GB/s"}
+    mixed["roofline"]["frac"] = round(mixed["roofline"]["achieved"] / pk["hbm"], 4)
+    del minp, mstate, mout
+
     # ---------------- end to end through the public call, host buffers
     hq, hk, hv = (t.cpu().pin_memory() for t in (inp.q, inp.k, inp.v))
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
@@ -389,6 +433,7 @@ def run_ours(args, ws, rank, local):
                    "inputs_vs_l2": "q, k, v = 384 MiB > 129 MB L2; no flush needed",
                    "parallelism": f"replicas x{ws}"},
         "roofline": roofline, "tensor": tensor, "decode": decode, "backward": backward,
+        "mixed": mixed,
         "e2e": e2e,
         "gpu_launches": K,
     }

@@ -210,6 +210,40 @@ la_status lightning_attn_backward_noalloc(const void *q, const void *k, const vo
 int64_t lightning_attn_backward_noalloc_max_bytes(void);
 
 /*
+ * One serving step over a packed batch in which every sequence continues from
+ * its cached state (MiniMax-01 report §3.3.2: inputs of length 1 and of
+ * length > 1 get separate kernels on separate CUDA streams; §3.3.1 prefix KV
+ * cache).  For every sequence s with L_s = cu_seqlens[s+1] - cu_seqlens[s]
+ * new tokens, the result is that of lightning_attn_prefill_with_state with
+ * initial_state = final_state = state:
+ *   L_s == 1: the decode step (kv <- lambda kv + k^T v, o = q kv) on
+ *             decode_stream;
+ *   L_s >= 2: the chunkwise prefill on prefill_stream, state updated in place;
+ *   L_s == 0: nothing (the state is unchanged).
+ * Both launches read cu_seqlens on the device, so no host copy of the lengths
+ * is needed.  The decode launch waits for the work already queued on
+ * prefill_stream and prefill_stream waits for the decode launch before its
+ * next work, so the whole step is ordered on prefill_stream (two events per
+ * device are created on first use for this fork and join; calls from
+ * several host threads are serialised while they enqueue).  With
+ * decode_stream == prefill_stream the two launches simply run one after the
+ * other.  chunk is the path's default; dtype rules as for prefill.
+ *
+ * q, k, v, out    [total_tokens, num_heads, head_dim], dtype `dtype`
+ * state           [num_seqs, num_heads, head_dim, head_dim] fp32, read and written
+ * cu_seqlens_host nullable HOST copy of cu_seqlens.  When given (and
+ *                 num_seqs <= 128) the prefill launch covers only the
+ *                 sequences with >= 2 new tokens; without it every sequence
+ *                 gets prefill CTAs that exit at once for the short ones.
+ */
+la_status lightning_attn_mixed_step(const void *q, const void *k, const void *v,
+                                    const float *decay, const int32_t *cu_seqlens,
+                                    int32_t num_seqs, int32_t total_tokens, int32_t num_heads,
+                                    int32_t head_dim, la_dtype dtype, float *state, void *out,
+                                    const int32_t *cu_seqlens_host, void *prefill_stream,
+                                    void *decode_stream);
+
+/*
  * Synchronises `stream`, then reports whether a kernel of this library raised
  * its device error word since the last call (and clears it).  The
  * tensor-core prefill bounds every wait of its pipeline (about 2 s); a wait
@@ -236,7 +270,7 @@ const char *lightning_attn_last_error(void);
 /* ABI version of this header: (major << 16) | minor. */
 int32_t lightning_attn_version(void);
 
-#define LIGHTNING_ATTN_VERSION ((1 << 16) | 2)
+#define LIGHTNING_ATTN_VERSION ((1 << 16) | 3)
 
 #ifdef __cplusplus
 }

@@ -71,6 +71,9 @@ def load(path: str = LIB_PATH):
             lib.lightning_attn_backward.restype = ctypes.c_int
             lib.lightning_attn_backward_workspace_bytes.argtypes = [i32, i32, i32, ctypes.c_int]
             lib.lightning_attn_backward_workspace_bytes.restype = ctypes.c_int64
+            lib.lightning_attn_mixed_step.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32,
+                                                      ctypes.c_int, vp, vp, vp, vp, vp]
+            lib.lightning_attn_mixed_step.restype = ctypes.c_int
             lib.lightning_attn_decode.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32,
                                                   ctypes.c_int, vp, vp]
             lib.lightning_attn_decode.restype = ctypes.c_int
@@ -216,6 +219,43 @@ def backward(q, k, v, decay, cu_seqlens, dout, *, chunk: int = 0, dq=None, dk=No
         _stream_handle(stream))
     _check(st, "lightning_attn_backward")
     return dq, dk, dv
+
+
+def mixed_step(q, k, v, decay, cu_seqlens, state, *, out=None, prefill_stream=None,
+               decode_stream=None, cu_seqlens_host=None):
+    """One serving step over a packed batch continuing from cached states:
+    sequences with one new token take the decode kernel on ``decode_stream``,
+    longer ones the chunkwise prefill on ``prefill_stream``; ``state`` fp32
+    [nseq, H, d, d] is updated in place.  Returns out [T, H, d]; the step is
+    ordered on ``prefill_stream`` (the current stream when None).
+    ``cu_seqlens_host`` (a host sequence of ints, optional) lets the prefill
+    launch cover only the sequences with two or more new tokens."""
+    if q.dim() != 3:
+        raise ValueError("q must be [T, H, d]")
+    T, H, d = q.shape
+    for name, t in (("k", k), ("v", v)):
+        if t.shape != q.shape or t.dtype != q.dtype:
+            raise ValueError(f"{name} must match q in shape and dtype")
+    if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1:
+        raise ValueError("cu_seqlens must be a 1-D int32 tensor")
+    if decay.dtype != torch.float32 or decay.numel() != H:
+        raise ValueError("decay must be fp32 [H]")
+    nseq = cu_seqlens.numel() - 1
+    if state.dtype != torch.float32 or tuple(state.shape) != (nseq, H, d, d):
+        raise ValueError("state must be fp32 [nseq, H, d, d]")
+    if out is None:
+        out = torch.empty_like(q)
+    ps = _stream_handle(prefill_stream)
+    ds = ps if decode_stream is None else int(decode_stream.cuda_stream)
+    host_cu = None
+    if cu_seqlens_host is not None:
+        host_cu = (ctypes.c_int32 * (nseq + 1))(*[int(x) for x in cu_seqlens_host])
+    st = load().lightning_attn_mixed_step(
+        _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(decay, "decay"),
+        _dev(cu_seqlens, "cu_seqlens"), nseq, T, H, d, _dtype_code(q), _dev(state, "state"),
+        _dev(out, "out"), None if host_cu is None else ctypes.addressof(host_cu), ps, ds)
+    _check(st, "lightning_attn_mixed_step")
+    return out
 
 
 def decode(q, k, v, decay, state, *, out=None, stream=None):

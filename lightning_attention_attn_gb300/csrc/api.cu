@@ -4,12 +4,14 @@
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
+#include <mutex>
 #include <string>
 
 #include <cuda_runtime.h>
 
 #include "lightning_attn.h"
 #include "la_internal.h"
+#include "sched.cuh"
 
 namespace {
 
@@ -48,6 +50,13 @@ la_status run_prefill(const la::PrefillArgs &a, la_dtype dtype) {
 }
 
 size_t elem_bytes(la_dtype dtype) { return dtype == LA_DTYPE_FP32 ? 4 : 2; }
+
+// Fork/join events of the two-stream mixed step, one pair per device,
+// created on first use; the mutex makes each call's record/wait sequence
+// atomic with respect to other host threads.
+constexpr int kMaxDevices = 64;
+std::mutex g_mixed_mu;
+cudaEvent_t g_fork[kMaxDevices] = {}, g_join[kMaxDevices] = {};
 
 // Workspace of the backward pass: three [T, H, d] arrays, each 256-byte aligned.
 size_t backward_slot_bytes(int32_t total_tokens, int32_t num_heads, int32_t head_dim,
@@ -249,6 +258,79 @@ la_status lightning_attn_backward(const void *q, const void *k, const void *v,
     // (q, k, v) -> (v, dout, q)
     if ((r = rev(v, rkv)) != LA_OK) return r;
     if ((r = fwd(rkv, rg, rq, d_k, true)) != LA_OK) return r;
+    return LA_OK;
+}
+
+la_status lightning_attn_mixed_step(const void *q, const void *k, const void *v,
+                                    const float *decay, const int32_t *cu_seqlens,
+                                    int32_t num_seqs, int32_t total_tokens, int32_t num_heads,
+                                    int32_t head_dim, la_dtype dtype, float *state, void *out,
+                                    const int32_t *cu_seqlens_host, void *prefill_stream,
+                                    void *decode_stream) {
+    if (num_seqs < 0) return fail(LA_ERR_INVALID_ARG, "num_seqs < 0 (%d)", num_seqs);
+    if (total_tokens < 0) return fail(LA_ERR_INVALID_ARG, "total_tokens < 0 (%d)", total_tokens);
+    if (num_heads < 1) return fail(LA_ERR_INVALID_ARG, "num_heads < 1 (%d)", num_heads);
+    if (head_dim != 64 && head_dim != 128)
+        return fail(LA_ERR_INVALID_ARG, "head_dim must be 64 or 128 (got %d)", head_dim);
+    if (dtype != LA_DTYPE_BF16 && dtype != LA_DTYPE_FP32)
+        return fail(LA_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+    if (num_seqs == 0 || total_tokens == 0) return LA_OK;
+    if (!q || !k || !v || !out || !decay || !cu_seqlens || !state)
+        return fail(LA_ERR_INVALID_ARG, "null pointer argument");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+        !aligned16(decay) || !aligned16(cu_seqlens) || !aligned16(state))
+        return fail(LA_ERR_INVALID_ARG, "every pointer must be 16-byte aligned");
+    if ((long long)num_seqs * num_heads > 0x7fffffffLL / 4)
+        return fail(LA_ERR_INVALID_ARG, "num_seqs * num_heads too large");
+
+    const cudaStream_t ps = static_cast<cudaStream_t>(prefill_stream);
+    const cudaStream_t ds = static_cast<cudaStream_t>(decode_stream);
+    // sequences of >= 2 new tokens: chunkwise prefill continuing from their
+    // cached state, updated in place
+    la::PrefillArgs pa{q, k, v, decay, cu_seqlens, num_seqs, total_tokens, num_heads, head_dim,
+                       0, out, state, ps, state, false, 2};
+    // With the lengths on the host, launch prefill work only for the
+    // sequences that need it: the kernels take sequences longest first, so
+    // the first n_long ranks are exactly those with >= 2 new tokens.
+    bool any_long = true;
+    if (cu_seqlens_host && num_seqs <= la::kMaxSortedSeqs) {
+        int n_long = 0;
+        for (int s = 0; s < num_seqs; ++s) n_long += cu_seqlens_host[s + 1] - cu_seqlens_host[s] >= 2;
+        pa.rank_limit = n_long;
+        any_long = n_long > 0;
+    }
+    // sequences of exactly 1 new token: the decode step
+    la::DecodeArgs da{q, k, v, decay, state, num_seqs, num_heads, head_dim, out, ds,
+                      cu_seqlens, total_tokens};
+    auto decode = [&]() {
+        return from_cuda(dtype == LA_DTYPE_FP32 ? la::decode_f32(da) : la::decode_bf16(da),
+                         "mixed step (decode)");
+    };
+    if (ps == ds) {
+        la_status r = decode();
+        return (r != LA_OK || !any_long) ? r : run_prefill(pa, dtype);
+    }
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return from_cuda(e, "mixed step");
+    if (dev < 0 || dev >= kMaxDevices) return fail(LA_ERR_UNSUPPORTED, "device index %d", dev);
+    std::lock_guard<std::mutex> lock(g_mixed_mu);
+    if (!g_fork[dev]) {
+        if ((e = cudaEventCreateWithFlags(&g_fork[dev], cudaEventDisableTiming)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&g_join[dev], cudaEventDisableTiming)) != cudaSuccess)
+            return from_cuda(e, "mixed step (events)");
+    }
+    // fork: the decode stream starts after the work already queued on the
+    // prefill stream; join: the prefill stream continues after the decode
+    if ((e = cudaEventRecord(g_fork[dev], ps)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(ds, g_fork[dev], 0)) != cudaSuccess)
+        return from_cuda(e, "mixed step (fork)");
+    la_status r = decode();
+    if (r != LA_OK) return r;
+    if (any_long && (r = run_prefill(pa, dtype)) != LA_OK) return r;
+    if ((e = cudaEventRecord(g_join[dev], ds)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(ps, g_join[dev], 0)) != cudaSuccess)
+        return from_cuda(e, "mixed step (join)");
     return LA_OK;
 }
 

@@ -50,7 +50,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kThreads)
 decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
               const float *__restrict__ decay, float *__restrict__ state, int H,
-              T *__restrict__ out) {
+              T *__restrict__ out, const int32_t *__restrict__ cu, int T_total) {
     constexpr int VEC = D / 32;             // columns per lane
     constexpr int RPW = D / kWarps;         // rows per warp
     constexpr int kRowsPerPass = 16;
@@ -64,7 +64,17 @@ decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const float lam = __ldg(decay + h);
 
-    const T *qp = q + pair * D, *kp = k + pair * D, *vp = v + pair * D;
+    // token row of entry b: b itself, or in a packed batch (mixed prefill +
+    // decode step, §3.3.2) the start of sequence b when it has exactly one
+    // new token; other sequences belong to the prefill launch
+    long row = pair / H;
+    if (cu) {
+        const int t0 = __ldg(cu + row), t1 = __ldg(cu + row + 1);
+        if (t1 - t0 != 1 || t0 < 0 || t0 >= T_total) return;
+        row = t0;
+    }
+    const long io = (row * H + h) * D;
+    const T *qp = q + io, *kp = k + io, *vp = v + io;
     for (int i = threadIdx.x; i < D; i += kThreads) {
         qs[i] = to_f(qp[i]);
         ks[i] = to_f(kp[i]);
@@ -108,7 +118,7 @@ decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
         float o = 0.f;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) o += red[w][j];
-        out[pair * D + j] = from_f<T>(o);
+        out[io + j] = from_f<T>(o);
     }
 }
 
@@ -120,7 +130,7 @@ cudaError_t launch(const DecodeArgs &a) {
     decode_kernel<T, D><<<(unsigned)grid, kThreads, 0, a.stream>>>(
         static_cast<const T *>(a.q), static_cast<const T *>(a.k),
         static_cast<const T *>(a.v), a.decay, a.state, a.num_heads,
-        static_cast<T *>(a.out));
+        static_cast<T *>(a.out), a.cu_seqlens, a.total_tokens);
     return cudaGetLastError();
 }
 

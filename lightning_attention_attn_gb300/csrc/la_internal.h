@@ -17,6 +17,10 @@ struct PrefillArgs {
     cudaStream_t stream;
     const float *initial_state; // [nseq, H, D, D] or nullptr (zero state)
     bool reverse_out = false;   // write o_t of sequence s to row cu[s] + cu[s+1] - 1 - t
+    int min_len = 0;            // sequences shorter than this are left untouched
+    // > 0: launch only the work of the rank_limit longest sequences (ranks
+    // are in order of length, longest first, for nseq <= kMaxSortedSeqs)
+    int rank_limit = 0;
 };
 
 struct DecodeArgs {
@@ -26,6 +30,11 @@ struct DecodeArgs {
     int batch, num_heads, head_dim;
     void *out;                  // [B, H, D]
     cudaStream_t stream;
+    // Packed mode (cu_seqlens != nullptr): entry b is sequence b of a packed
+    // batch; its token row is cu_seqlens[b], and only sequences of length
+    // exactly 1 are stepped (the others are left untouched).
+    const int32_t *cu_seqlens = nullptr;
+    int total_tokens = 0;
 };
 
 // CUDA-core chunkwise prefill; chunk in {16, 32, 64}, head_dim in {64, 128}.

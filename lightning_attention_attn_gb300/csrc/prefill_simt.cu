@@ -49,7 +49,7 @@ prefill_simt_kernel(const T *__restrict__ q, const T *__restrict__ k,
                     const T *__restrict__ v, const float *__restrict__ decay,
                     const int32_t *__restrict__ cu, int nseq, int T_total, int H,
                     const float *initial_state, T *__restrict__ out, float *final_state,
-                    int reverse_out) {
+                    int reverse_out, int min_len) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     auto &sm = *reinterpret_cast<SimtSmem<D, B> *>(smem_raw);
     const int tid = threadIdx.x;
@@ -61,6 +61,7 @@ prefill_simt_kernel(const T *__restrict__ q, const T *__restrict__ k,
     t0 = min(max(t0, 0), T_total);
     t1 = min(max(t1, t0), T_total);
     const int L = t1 - t0;
+    if (L < min_len) return;  // a mixed step's decode launch owns this sequence
     const float lam = __ldg(decay + h);
 
     for (int e = tid; e <= B; e += kThreads) sm.pw[e] = powf(lam, (float)e);
@@ -145,14 +146,14 @@ cudaError_t launch(const PrefillArgs &a) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    const long grid = (long)a.nseq * a.num_heads;
+    const long grid = (long)(a.rank_limit > 0 ? a.rank_limit : a.nseq) * a.num_heads;
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffffL) return cudaErrorInvalidConfiguration;
     kern<<<(unsigned)grid, kThreads, smem, a.stream>>>(
         static_cast<const T *>(a.q), static_cast<const T *>(a.k),
         static_cast<const T *>(a.v), a.decay, a.cu_seqlens, a.nseq, a.total_tokens,
         a.num_heads, a.initial_state, static_cast<T *>(a.out), a.final_state,
-        a.reverse_out ? 1 : 0);
+        a.reverse_out ? 1 : 0, a.min_len);
     return cudaGetLastError();
 }
 

@@ -176,12 +176,13 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     return __all_sync(0xffffffffu, ok);
 }
 
+template <bool kRevOut>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                   const float *__restrict__ decay, const int32_t *__restrict__ cu, int nseq, int T,
                   int H, const float *initial_state, __nv_bfloat16 *__restrict__ out,
-                  float *final_state, int reverse_out) {
+                  float *final_state, int min_len) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *base = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -197,6 +198,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     t0 = min(max(t0, 0), T);
     t1 = min(max(t1, t0), T);
     const int L = t1 - t0;
+    if (L < min_len) return;  // a mixed step's decode launch owns this sequence
     const int nch = (L + BC - 1) / BC;
     const float lam = __ldg(decay + h);
     // A sequence may continue from a cached state S0 (prefix KV cache,
@@ -743,9 +745,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
                              ld_shared_f32(vscale_s + 4u * (uint32_t)(i & 3));
             const float qf = pw(r + 1);
             const float2 s12 = make_float2(s1, s1), qf2 = make_float2(qf, qf);
-            // token row of o_r; with reverse_out the sequence is written back
-            // to front (the backward pass's reversed-time launches)
-            const long orow_t = reverse_out ? (long)(t1 - 1 - i * BC - r) : (long)(t0 + i * BC + r);
+            // token row of o_r; with kRevOut the sequence is written back to
+            // front (the backward pass's reversed-time launches)
+            const long orow_t = kRevOut ? (long)(t1 - 1 - i * BC - r) : (long)(t0 + i * BC + r);
             uint4 *orow = reinterpret_cast<uint4 *>(out + (orow_t * H + h) * D +
                                                     vs * DV);
 #pragma unroll
@@ -959,19 +961,21 @@ cudaError_t prefill_tc_bf16(const PrefillArgs &a) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    static int attr_set_for[64] = {0};
-    if (dev < 64 && !attr_set_for[dev]) {
-        e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kSmemBytes);
+    static int attr_set_for[64] = {0};  // bit 0: forward kernel, bit 1: reversed-output kernel
+    const int bit = a.reverse_out ? 2 : 1;
+    if (dev < 64 && !(attr_set_for[dev] & bit)) {
+        e = cudaFuncSetAttribute(a.reverse_out ? prefill_tc_kernel<true> : prefill_tc_kernel<false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
         if (e != cudaSuccess) return e;
-        attr_set_for[dev] = 1;
+        attr_set_for[dev] |= bit;
     }
-    const long grid = (long)a.nseq * a.num_heads * NVS;
+    const long grid = (long)(a.rank_limit > 0 ? a.rank_limit : a.nseq) * a.num_heads * NVS;
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffffL) return cudaErrorInvalidConfiguration;
-    prefill_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, a.stream>>>(
+    auto kern = a.reverse_out ? prefill_tc_kernel<true> : prefill_tc_kernel<false>;
+    kern<<<(unsigned)grid, kThreads, kSmemBytes, a.stream>>>(
         mq, mk, mv, mo, a.decay, a.cu_seqlens, a.nseq, a.total_tokens, a.num_heads,
-        a.initial_state, static_cast<__nv_bfloat16 *>(a.out), a.final_state, a.reverse_out ? 1 : 0);
+        a.initial_state, static_cast<__nv_bfloat16 *>(a.out), a.final_state, a.min_len);
     return cudaGetLastError();
 }
 

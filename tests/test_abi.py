@@ -21,6 +21,7 @@ def test_header_declares_expected_calls():
     names = la.header_functions()
     for n in ("lightning_attn_prefill", "lightning_attn_prefill_with_state",
               "lightning_attn_backward", "lightning_attn_backward_workspace_bytes",
+              "lightning_attn_mixed_step",
               "lightning_attn_decode",
               "lightning_attn_status_string", "lightning_attn_last_error",
               "lightning_attn_version", "lightning_attn_device_status",
@@ -38,7 +39,7 @@ def test_library_exports_every_header_symbol(lib):
 
 
 def test_version(lib):
-    assert la.version() == (1, 2)
+    assert la.version() == (1, 3)
 
 
 def test_status_strings(lib):
@@ -201,3 +202,20 @@ def test_backward_noalloc_rejects_sizes_beyond_its_array(lib):
            A + 0x60000, None)
     assert st == la.LA_ERR_INVALID_ARG
     assert "scratch" in lib.lightning_attn_last_error().decode()
+
+
+@pytest.mark.parametrize("kw, status", [
+    (dict(state=None), la.LA_ERR_INVALID_ARG),
+    (dict(state=A + 4), la.LA_ERR_INVALID_ARG),
+    (dict(d=80), la.LA_ERR_INVALID_ARG),
+    (dict(nseq=0), la.LA_OK),
+])
+def test_mixed_step_host_validation(lib, kw, status):
+    args = dict(q=A, k=A, v=A, decay=A, cu=A, nseq=4, T=9, H=2, d=128,
+                dtype=la.LA_DTYPE_BF16, state=A + 0x100000, out=A + 0x200000)
+    args.update(kw)
+    st = lib.lightning_attn_mixed_step(args["q"], args["k"], args["v"], args["decay"], args["cu"],
+                                       args["nseq"], args["T"], args["H"], args["d"],
+                                       args["dtype"], args["state"], args["out"], None, None,
+                                       None)
+    assert st == status

@@ -278,6 +278,43 @@ def run_ours(args, ws, rank, local):
               "peak_tflops": pk["bf16"], "frac_of_bf16_peak": round(tflops / pk["bf16"], 4),
               "frac_of_roofline": round(t_roof / avg_launch_s, 4)}
 
+    # ---------------- the other prefill workloads of the benchmark set:
+    # 128K-token context (chunk 128 on tensor cores; chunk 64 on the
+    # CUDA-core kernel timed once) and the 16-sequence varlen batch
+    def time_prefill(lengths, chunk, reps):
+        pin = wl.prefill_inputs(lengths, H, d, dtype=torch.bfloat16, seed=0, device=dev)
+        pout = torch.empty_like(pin.q)
+        pfs = torch.empty((len(lengths), H, d, d), dtype=torch.float32, device=dev)
+
+        def run():
+            la.prefill(pin.q, pin.k, pin.v, pin.decay, pin.cu_seqlens, chunk=chunk, out=pout,
+                       final_state=pfs, stream=stream)
+        run()
+        torch.cuda.synchronize()
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(reps):
+            run()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        la.device_status(stream)
+        ms = a0.elapsed_time(a1) / reps
+        Tn = sum(lengths)
+        byts, flops = prefill_alg(Tn, H, d, 128, len(lengths))
+        return {"ms_per_launch": round(ms, 4), "tokens_per_s": round(Tn / (ms / 1e3), 1),
+                "tokens": Tn, "chunk": chunk,
+                "roofline": {"bound": "hbm", "alg_bytes": byts,
+                             "achieved": round(byts / (ms / 1e3) / 1e9, 1), "peak": pk["hbm"],
+                             "unit": "GB/s", "frac": round(byts / (ms / 1e3) / 1e9 / pk["hbm"], 4)}}
+
+    more = {"prefill_128k": time_prefill([131072], 0, 5),
+            "prefill_128k_chunk64_cuda_cores": time_prefill([131072], 64, 1),
+            "prefill_128k_chunk256": "not run: the tensor-core block is 128 (chunk 256 returns "
+                                     "LA_ERR_UNSUPPORTED)",
+            "varlen_16": time_prefill(wl.varlen_lengths().tolist(), 0, 5)}
+    torch.cuda.empty_cache()
+
     # ---------------- decode: 128 seqs x 64 heads, 1000 consecutive steps
     dcfg = wl.DECODE_128
     dsteps = dcfg["steps"]
@@ -464,7 +501,7 @@ def run_ours(args, ws, rank, local):
                    "inputs_vs_l2": "q, k, v = 384 MiB > 129 MB L2; no flush needed",
                    "parallelism": f"replicas x{ws}"},
         "roofline": roofline, "tensor": tensor, "decode": decode, "backward": backward,
-        "mixed": mixed,
+        "mixed": mixed, "more_prefill": more,
         "e2e": e2e,
         "gpu_launches": K,
     }

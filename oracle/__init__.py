@@ -13,6 +13,7 @@ Sources followed (MiniMax-01 technical report, CSDN full translation):
   * §3.2 "data packing" -- packed sequences are independent
   * §3.3.1 prefix KV cache -- a sequence may continue from a cached state
   * gradients of the left product for training (§2.2.1, §2.2.2)
+  * channel-wise (per key channel) decay -- K3 report reading notes
 Parity pins: tests/test_oracle.py (golden hand examples, closed forms,
 two-form agreement, exact rational brute force, invariants).
 """
@@ -65,8 +66,15 @@ def _declare(lib):
     lib.la_oracle_max_threads.argtypes = [ctypes.c_int]
     lib.la_oracle_backward.argtypes = [_dp, _dp, _dp, _dp, _ip, ctypes.c_int, ctypes.c_int,
                                        ctypes.c_int, _dp, _dp, _dp, _dp, ctypes.c_int]
+    lib.la_oracle_quadratic_cw.argtypes = [_dp, _dp, _dp, _dp, _ip, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_int, _dp, _dp, ctypes.c_int]
+    lib.la_oracle_recurrent_cw.argtypes = [_dp, _dp, _dp, _dp, _ip, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_int, _dp, _dp, _dp, ctypes.c_int]
+    lib.la_oracle_decode_cw.argtypes = [_dp, _dp, _dp, _dp, _dp, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_int, _dp, ctypes.c_int]
     for f in (lib.la_oracle_quadratic, lib.la_oracle_recurrent,
-              lib.la_oracle_decode, lib.la_oracle_max_threads, lib.la_oracle_backward):
+              lib.la_oracle_decode, lib.la_oracle_max_threads, lib.la_oracle_backward,
+              lib.la_oracle_quadratic_cw, lib.la_oracle_recurrent_cw, lib.la_oracle_decode_cw):
         f.restype = ctypes.c_int
     return lib
 
@@ -216,6 +224,68 @@ def backward(q, k, v, decay, cu_seqlens, dout, nthreads=0, lib=None):
     if rc:
         raise ValueError(f"la_oracle_backward failed ({rc})")
     return dq, dk, dv
+
+
+def _decay_cw(decay, H, d):
+    lam = _f64(decay_as_seen(decay)).reshape(-1)
+    assert lam.size == H * d, "channel-wise decay must be [H, d]"
+    return np.ascontiguousarray(lam)
+
+
+def quadratic_cw(q, k, v, decay, cu_seqlens, nthreads=0, lib=None, initial_state=None):
+    """Left-product form with channel-wise decay (decay [H, d]: lambda of
+    each key channel).  Returns out [T, H, d] fp64."""
+    lib = lib or load()
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    cu = _i32(cu_seqlens)
+    T, H, d = _shape(q)
+    assert cu[-1] == T
+    lam = _decay_cw(decay, H, d)
+    s0 = _init(initial_state, len(cu) - 1, H, d)
+    out = np.zeros((T, H, d), dtype=np.float64)
+    rc = lib.la_oracle_quadratic_cw(_ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp), _ptr(lam, _dp),
+                                    _ptr(cu, _ip), len(cu) - 1, H, d,
+                                    None if s0 is None else _ptr(s0, _dp), _ptr(out, _dp),
+                                    nthreads)
+    if rc:
+        raise ValueError(f"la_oracle_quadratic_cw failed ({rc})")
+    return out
+
+
+def recurrent_cw(q, k, v, decay, cu_seqlens, nthreads=0, lib=None, initial_state=None):
+    """Recursion with channel-wise decay.  Returns (out, final_state) fp64."""
+    lib = lib or load()
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    cu = _i32(cu_seqlens)
+    T, H, d = _shape(q)
+    assert cu[-1] == T
+    nseq = len(cu) - 1
+    lam = _decay_cw(decay, H, d)
+    s0 = _init(initial_state, nseq, H, d)
+    out = np.zeros((T, H, d), dtype=np.float64)
+    st = np.zeros((nseq, H, d, d), dtype=np.float64)
+    rc = lib.la_oracle_recurrent_cw(_ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp), _ptr(lam, _dp),
+                                    _ptr(cu, _ip), nseq, H, d,
+                                    None if s0 is None else _ptr(s0, _dp), _ptr(out, _dp),
+                                    _ptr(st, _dp), nthreads)
+    if rc:
+        raise ValueError(f"la_oracle_recurrent_cw failed ({rc})")
+    return out, st
+
+
+def decode_cw(q, k, v, decay, state, nthreads=0, lib=None):
+    """One decode step with channel-wise decay; returns (out, new_state)."""
+    lib = lib or load()
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    st = _f64(state).copy()
+    B, H, d = q.shape
+    lam = _decay_cw(decay, H, d)
+    out = np.zeros((B, H, d), dtype=np.float64)
+    rc = lib.la_oracle_decode_cw(_ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp), _ptr(lam, _dp),
+                                 _ptr(st, _dp), B, H, d, _ptr(out, _dp), nthreads)
+    if rc:
+        raise ValueError(f"la_oracle_decode_cw failed ({rc})")
+    return out, st
 
 
 def max_threads(nthreads: int = 0) -> int:

@@ -274,3 +274,125 @@ int la_oracle_backward(const double *q, const double *k, const double *v,
     }
     return 0;
 }
+
+/*
+ * Channel-wise decay (the K3 report reading notes, "gated DeltaNet ...
+ * changes the scalar decay to a channel-wise decay, which can fall back to
+ * the uniform one"; the decay acts on the key channels, the dimension Q and
+ * K share): lam_cw[h][i] is the decay of key channel i of head h, so
+ *   quadratic:  o_t = sum_{u<=t} (sum_i q_t[i] k_u[i] lam_i^(t-u)) v_u
+ *   recurrent:  kv_t[i][j] = lam_i kv_{t-1}[i][j] + k_t[i] v_t[j],
+ *               o_t = q_t kv_t
+ * starting from zero (or initial_state) at every sequence start.  With all
+ * lam_i equal these are la_oracle_quadratic / la_oracle_recurrent.
+ */
+int la_oracle_quadratic_cw(const double *q, const double *k, const double *v,
+                           const double *lam_cw, const int32_t *cu, int nseq, int H,
+                           int d, const double *initial_state, double *out, int nthreads)
+{
+    if (check_cu(cu, nseq) || H <= 0 || d <= 0) return 1;
+    set_threads(nthreads);
+    const long row = (long)H * d;
+    const long npairs = (long)nseq * H;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long p = 0; p < npairs; ++p) {
+        const int s = (int)(p / H), h = (int)(p % H);
+        const double *la = lam_cw + (long)h * d;
+        const long t0 = cu[s], L = cu[s + 1] - cu[s];
+        for (long t = 0; t < L; ++t) {
+            const double *qt = q + (t0 + t) * row + (long)h * d;
+            double *ot = out + (t0 + t) * row + (long)h * d;
+            for (int j = 0; j < d; ++j) ot[j] = 0.0;
+            for (long u = 0; u <= t; ++u) {
+                const double *ku = k + (t0 + u) * row + (long)h * d;
+                const double *vu = v + (t0 + u) * row + (long)h * d;
+                double s_tu = 0.0;  /* sum_i q_t[i] k_u[i] lam_i^(t-u) */
+                for (int i = 0; i < d; ++i) s_tu += qt[i] * ku[i] * pow(la[i], (double)(t - u));
+                for (int j = 0; j < d; ++j) ot[j] += s_tu * vu[j];
+            }
+            if (initial_state) {  /* the earlier tokens, through S0 */
+                const double *s0 = initial_state + ((long)s * H + h) * d * d;
+                for (int j = 0; j < d; ++j) {
+                    double acc = 0.0;
+                    for (int i = 0; i < d; ++i)
+                        acc += qt[i] * pow(la[i], (double)(t + 1)) * s0[(long)i * d + j];
+                    ot[j] += acc;
+                }
+            }
+        }
+    }
+    return 0;
+}
+
+int la_oracle_recurrent_cw(const double *q, const double *k, const double *v,
+                           const double *lam_cw, const int32_t *cu, int nseq, int H,
+                           int d, const double *initial_state, double *out,
+                           double *final_state, int nthreads)
+{
+    if (check_cu(cu, nseq) || H <= 0 || d <= 0) return 1;
+    set_threads(nthreads);
+    const long row = (long)H * d;
+    const long npairs = (long)nseq * H;
+    int err = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long p = 0; p < npairs; ++p) {
+        const int s = (int)(p / H), h = (int)(p % H);
+        const double *la = lam_cw + (long)h * d;
+        double *kv = (double *)calloc((size_t)d * d, sizeof(double));
+        if (!kv) {
+#pragma omp atomic write
+            err = 2;
+            continue;
+        }
+        if (initial_state)
+            memcpy(kv, initial_state + ((long)s * H + h) * d * d, sizeof(double) * (size_t)d * d);
+        const long t0 = cu[s], L = cu[s + 1] - cu[s];
+        for (long t = 0; t < L; ++t) {
+            const double *qt = q + (t0 + t) * row + (long)h * d;
+            const double *kt = k + (t0 + t) * row + (long)h * d;
+            const double *vt = v + (t0 + t) * row + (long)h * d;
+            for (int i = 0; i < d; ++i)
+                for (int j = 0; j < d; ++j)
+                    kv[(long)i * d + j] = la[i] * kv[(long)i * d + j] + kt[i] * vt[j];
+            if (out) {
+                double *ot = out + (t0 + t) * row + (long)h * d;
+                for (int j = 0; j < d; ++j) {
+                    double acc = 0.0;
+                    for (int i = 0; i < d; ++i) acc += qt[i] * kv[(long)i * d + j];
+                    ot[j] = acc;
+                }
+            }
+        }
+        if (final_state)
+            memcpy(final_state + ((long)s * H + h) * d * d, kv, sizeof(double) * (size_t)d * d);
+        free(kv);
+    }
+    return err;
+}
+
+/* One decode step with channel-wise decay: state[i][j] <- lam_i state[i][j]
+ * + k[i] v[j], o = q state (after the update). */
+int la_oracle_decode_cw(const double *q, const double *k, const double *v,
+                        const double *lam_cw, double *state, int batch, int H, int d,
+                        double *out, int nthreads)
+{
+    if (batch < 0 || H <= 0 || d <= 0) return 1;
+    set_threads(nthreads);
+    const long npairs = (long)batch * H;
+#pragma omp parallel for schedule(static)
+    for (long p = 0; p < npairs; ++p) {
+        const int h = (int)(p % H);
+        const double *qb = q + p * d, *kb = k + p * d, *vb = v + p * d;
+        const double *la = lam_cw + (long)h * d;
+        double *kv = state + p * d * d;
+        for (int i = 0; i < d; ++i)
+            for (int j = 0; j < d; ++j)
+                kv[(long)i * d + j] = la[i] * kv[(long)i * d + j] + kb[i] * vb[j];
+        for (int j = 0; j < d; ++j) {
+            double acc = 0.0;
+            for (int i = 0; i < d; ++i) acc += qb[i] * kv[(long)i * d + j];
+            out[p * d + j] = acc;
+        }
+    }
+    return 0;
+}

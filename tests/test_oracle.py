@@ -102,6 +102,64 @@ def pin_backward_lambda_one(lib):
         np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
 
 
+def pin_golden_channel_decay(lib):
+    g = golden("hand_example_channel_decay.json")
+    outq = oracle.quadratic_cw(g["q"], g["k"], g["v"], g["lambda_cw"], g["cu_seqlens"], lib=lib)
+    outr, st = oracle.recurrent_cw(g["q"], g["k"], g["v"], g["lambda_cw"], g["cu_seqlens"],
+                                   lib=lib)
+    for got in (outq, outr):
+        np.testing.assert_allclose(got, g["out"], rtol=0, atol=1e-15)
+    np.testing.assert_allclose(st, g["final_state"], rtol=0, atol=1e-15)
+
+
+def pin_channel_decay_uniform_reduces(lib):
+    """Equal channel decays reduce to the (separately pinned) scalar forms,
+    with and without a cached state; the decode step likewise."""
+    rng = np.random.default_rng(12)
+    lengths, H, d = [7, 0, 19], 3, 5
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    q, k, v = rnd(rng, int(cu[-1]), H, d)
+    lam = np.array([0.4, 0.9, 1.0])
+    lam_cw = np.repeat(lam[:, None], d, axis=1)
+    s0 = rng.standard_normal((len(lengths), H, d, d))
+    for init in (None, s0):
+        want_q = oracle.quadratic(q, k, v, lam, cu, lib=lib, initial_state=init)
+        want_r, want_st = oracle.recurrent(q, k, v, lam, cu, lib=lib, initial_state=init)
+        got_q = oracle.quadratic_cw(q, k, v, lam_cw, cu, lib=lib, initial_state=init)
+        got_r, got_st = oracle.recurrent_cw(q, k, v, lam_cw, cu, lib=lib, initial_state=init)
+        np.testing.assert_allclose(got_q, want_q, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(got_r, want_r, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(got_st, want_st, rtol=1e-12, atol=1e-12)
+    qd, kd, vd = (rng.standard_normal((4, H, d)) for _ in range(3))
+    st = rng.standard_normal((4, H, d, d))
+    o1, n1 = oracle.decode(qd, kd, vd, lam, st, lib=lib)
+    o2, n2 = oracle.decode_cw(qd, kd, vd, lam_cw, st, lib=lib)
+    np.testing.assert_allclose(o2, o1, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(n2, n1, rtol=1e-12, atol=1e-12)
+
+
+def pin_channel_decay_two_forms(lib):
+    """With distinct channel decays the left product and the recursion
+    (independent formulations) agree, from zero and from a cached state;
+    the decode step continues the recursion."""
+    rng = np.random.default_rng(13)
+    lengths, H, d = [40, 1, 0, 23], 2, 6
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    q, k, v = rnd(rng, int(cu[-1]), H, d)
+    lam_cw = rng.uniform(0.3, 1.0, size=(H, d))
+    s0 = rng.standard_normal((len(lengths), H, d, d))
+    for init in (None, s0):
+        oq = oracle.quadratic_cw(q, k, v, lam_cw, cu, lib=lib, initial_state=init)
+        orr, _ = oracle.recurrent_cw(q, k, v, lam_cw, cu, lib=lib, initial_state=init)
+        assert np.max(np.abs(oq - orr)) <= 1e-10 * max(1.0, float(np.sqrt(np.mean(orr ** 2))))
+    L = 12
+    full, st_full = oracle.recurrent_cw(q[:L + 1], k[:L + 1], v[:L + 1], lam_cw, [0, L + 1], lib=lib)
+    _, st = oracle.recurrent_cw(q[:L], k[:L], v[:L], lam_cw, [0, L], lib=lib)
+    o, st2 = oracle.decode_cw(q[L:L + 1], k[L:L + 1], v[L:L + 1], lam_cw, st, lib=lib)
+    np.testing.assert_allclose(o[0], full[L], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(st2, st_full, rtol=1e-12, atol=1e-13)
+
+
 def pin_golden_decode(lib):
     g = golden("hand_example_decode.json")
     out, st = oracle.decode(g["q"], g["k"], g["v"], g["lambda"], g["state"], lib=lib)
@@ -310,6 +368,9 @@ ALL_PINS = {
     "golden_state": lambda lib: pin_golden_prefill(lib, "hand_example_state.json"),
     "golden_decode": pin_golden_decode,
     "golden_backward": pin_golden_backward,
+    "golden_channel_decay": pin_golden_channel_decay,
+    "cw_uniform": pin_channel_decay_uniform_reduces,
+    "cw_two_forms": pin_channel_decay_two_forms,
     "backward_fd": pin_backward_finite_differences,
     "backward_lambda_one": pin_backward_lambda_one,
     "geometric_d1_state": pin_geometric_d1_with_state,
@@ -347,6 +408,18 @@ def test_backward_finite_differences(lib):
 
 def test_backward_lambda_one(lib):
     pin_backward_lambda_one(lib)
+
+
+def test_golden_channel_decay(lib):
+    pin_golden_channel_decay(lib)
+
+
+def test_channel_decay_uniform_reduces(lib):
+    pin_channel_decay_uniform_reduces(lib)
+
+
+def test_channel_decay_two_forms(lib):
+    pin_channel_decay_two_forms(lib)
 
 
 def test_golden_decode(lib):
@@ -442,6 +515,12 @@ MUTANTS = {
     "bwd_dk_uses_k": ("dku[i] += w * g_v * qt[i]", "dku[i] += w * g_v * ku[i]"),
     "bwd_dv_wrong_dot": ("dvu[i] += w * q_k * gt[i]", "dvu[i] += w * g_v * gt[i]"),
     "bwd_dq_no_decay": ("dqt[i] += w * g_v * ku[i]", "dqt[i] += g_v * ku[i]"),
+    "cw_decay_on_value_columns": ("la[i] * kv[(long)i * d + j] + kt[i] * vt[j]",
+                                  "la[j] * kv[(long)i * d + j] + kt[i] * vt[j]"),
+    "cw_quad_uniform_decay": ("qt[i] * ku[i] * pow(la[i], (double)(t - u))",
+                              "qt[i] * ku[i] * pow(la[0], (double)(t - u))"),
+    "cw_dec_decay_on_value_columns": ("la[i] * kv[(long)i * d + j] + kb[i] * vb[j]",
+                                      "la[j] * kv[(long)i * d + j] + kb[i] * vb[j]"),
     "dec_read_before_update": (
         "                kv[(long)i * d + j] = la * kv[(long)i * d + j] + kb[i] * vb[j];\n"
         "        for (int j = 0; j < d; ++j) {\n"

@@ -308,7 +308,35 @@ def run_ours(args, ws, rank, local):
                              "achieved": round(byts / (ms / 1e3) / 1e9, 1), "peak": pk["hbm"],
                              "unit": "GB/s", "frac": round(byts / (ms / 1e3) / 1e9 / pk["hbm"], 4)}}
 
-    more = {"prefill_128k": time_prefill([131072], 0, 5),
+    def time_channel_decay(lengths, reps):
+        pin = wl.prefill_inputs(lengths, H, d, dtype=torch.bfloat16, seed=0, device=dev)
+        lam_cw = pin.decay[:, None].repeat(1, d).contiguous()
+        lam_cw = lam_cw * (1.0 - 0.01 * torch.linspace(0, 1, d, device=dev))[None, :]
+        pout = torch.empty_like(pin.q)
+
+        def run():
+            la.prefill_channel_decay(pin.q, pin.k, pin.v, lam_cw, pin.cu_seqlens, chunk=64,
+                                     out=pout, stream=stream)
+        run()
+        torch.cuda.synchronize()
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(reps):
+            run()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        ms = a0.elapsed_time(a1) / reps
+        Tn = sum(lengths)
+        byts, _ = prefill_alg(Tn, H, d, 64, len(lengths))
+        return {"ms_per_launch": round(ms, 3), "tokens_per_s": round(Tn / (ms / 1e3), 1),
+                "kernel": "CUDA-core (FFMA) prefill, chunk 64",
+                "roofline": {"bound": "hbm", "alg_bytes": byts,
+                             "achieved": round(byts / (ms / 1e3) / 1e9, 1), "peak": pk["hbm"],
+                             "unit": "GB/s", "frac": round(byts / (ms / 1e3) / 1e9 / pk["hbm"], 4)}}
+
+    more = {"prefill_8k_channel_decay": time_channel_decay([8192], 2),
+            "prefill_128k": time_prefill([131072], 0, 5),
             "prefill_128k_chunk64_cuda_cores": time_prefill([131072], 64, 1),
             "prefill_128k_chunk256": "not run: the tensor-core block is 128 (chunk 256 returns "
                                      "LA_ERR_UNSUPPORTED)",

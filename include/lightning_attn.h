@@ -126,6 +126,36 @@ la_status lightning_attn_prefill_with_state(const void *q, const void *k, const 
                                             float *final_state, void *stream);
 
 /*
+ * Prefill with a channel-wise decay: one lambda per head and KEY channel
+ * (K3 report reading notes: the scalar decay generalised to a channel-wise
+ * one that can fall back to the uniform decay; it acts on the channels Q and
+ * K share).  With lam_i = decay[h * head_dim + i] the state recursion is
+ *     kv_t[i][j] = lam_i kv_{t-1}[i][j] + k_t[i] v_t[j],   o_t = q_t kv_t
+ * i.e. o_t = sum_{u <= t} (sum_i q_t[i] k_u[i] lam_i^(t-u)) v_u
+ *            + sum_i q_t[i] lam_i^(t+1) S0[i][:]  (from a cached state S0).
+ * Arguments as for lightning_attn_prefill_with_state, except
+ *   decay  [num_heads, head_dim] fp32, each in (0, 1].
+ * Runs on the CUDA-core (FFMA) kernel: chunk 0 (= 64), 16, 32 or 64;
+ * 128 and 256 return LA_ERR_UNSUPPORTED.
+ */
+la_status lightning_attn_prefill_channel_decay(const void *q, const void *k, const void *v,
+                                               const float *decay, const int32_t *cu_seqlens,
+                                               int32_t num_seqs, int32_t total_tokens,
+                                               int32_t num_heads, int32_t head_dim, int32_t chunk,
+                                               la_dtype dtype, const float *initial_state,
+                                               void *out, float *final_state, void *stream);
+
+/*
+ * Decode step with a channel-wise decay (decay [num_heads, head_dim]):
+ *     state[b][h][i][j] <- lam_i state[b][h][i][j] + k[i] v[j],  out = q state.
+ * Other arguments as for lightning_attn_decode.
+ */
+la_status lightning_attn_decode_channel_decay(const void *q, const void *k, const void *v,
+                                              const float *decay, float *state, int32_t batch,
+                                              int32_t num_heads, int32_t head_dim,
+                                              la_dtype dtype, void *out, void *stream);
+
+/*
  * One decode step for a batch of sequences, each with one new token.
  *   (MiniMax-01 report §3.3.2: length-1 inputs get their own memory-bound
  *    kernel; §3.3.1: the KV computation and the prefix-KV-cache update are
@@ -270,7 +300,7 @@ const char *lightning_attn_last_error(void);
 /* ABI version of this header: (major << 16) | minor. */
 int32_t lightning_attn_version(void);
 
-#define LIGHTNING_ATTN_VERSION ((1 << 16) | 3)
+#define LIGHTNING_ATTN_VERSION ((1 << 16) | 4)
 
 #ifdef __cplusplus
 }

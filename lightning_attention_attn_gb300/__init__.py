@@ -74,6 +74,13 @@ def load(path: str = LIB_PATH):
             lib.lightning_attn_mixed_step.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                                       ctypes.c_int, vp, vp, vp, vp, vp]
             lib.lightning_attn_mixed_step.restype = ctypes.c_int
+            lib.lightning_attn_prefill_channel_decay.argtypes = [vp, vp, vp, vp, vp, i32, i32,
+                                                                 i32, i32, i32, ctypes.c_int, vp,
+                                                                 vp, vp, vp]
+            lib.lightning_attn_prefill_channel_decay.restype = ctypes.c_int
+            lib.lightning_attn_decode_channel_decay.argtypes = [vp, vp, vp, vp, vp, i32, i32,
+                                                                i32, ctypes.c_int, vp, vp]
+            lib.lightning_attn_decode_channel_decay.restype = ctypes.c_int
             lib.lightning_attn_decode.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32,
                                                   ctypes.c_int, vp, vp]
             lib.lightning_attn_decode.restype = ctypes.c_int
@@ -255,6 +262,50 @@ def mixed_step(q, k, v, decay, cu_seqlens, state, *, out=None, prefill_stream=No
         _dev(cu_seqlens, "cu_seqlens"), nseq, T, H, d, _dtype_code(q), _dev(state, "state"),
         _dev(out, "out"), None if host_cu is None else ctypes.addressof(host_cu), ps, ds)
     _check(st, "lightning_attn_mixed_step")
+    return out
+
+
+def prefill_channel_decay(q, k, v, decay, cu_seqlens=None, *, chunk: int = 0, out=None,
+                          final_state=None, return_state: bool = True, stream=None,
+                          initial_state=None):
+    """Prefill with one decay per head and key channel: ``decay`` fp32
+    [H, d].  Otherwise as :func:`prefill` (CUDA-core kernel, chunk <= 64)."""
+    if q.dim() != 3:
+        raise ValueError("q must be [T, H, d]")
+    T, H, d = q.shape
+    for name, t in (("k", k), ("v", v)):
+        if t.shape != q.shape or t.dtype != q.dtype:
+            raise ValueError(f"{name} must match q in shape and dtype")
+    if cu_seqlens is None:
+        cu_seqlens = torch.tensor([0, T], dtype=torch.int32, device=q.device)
+    if decay.dtype != torch.float32 or tuple(decay.shape) != (H, d):
+        raise ValueError("decay must be fp32 [H, d]")
+    nseq = cu_seqlens.numel() - 1
+    if out is None:
+        out = torch.empty_like(q)
+    if final_state is None and return_state:
+        final_state = torch.empty((nseq, H, d, d), dtype=torch.float32, device=q.device)
+    st = load().lightning_attn_prefill_channel_decay(
+        _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(decay, "decay"),
+        _dev(cu_seqlens, "cu_seqlens"), nseq, T, H, d, int(chunk), _dtype_code(q),
+        None if initial_state is None else _dev(initial_state, "initial_state"),
+        _dev(out, "out"), None if final_state is None else _dev(final_state, "final_state"),
+        _stream_handle(stream))
+    _check(st, "lightning_attn_prefill_channel_decay")
+    return out, final_state
+
+
+def decode_channel_decay(q, k, v, decay, state, *, out=None, stream=None):
+    """Decode step with one decay per head and key channel (decay fp32 [H, d])."""
+    Bn, H, d = q.shape
+    if decay.dtype != torch.float32 or tuple(decay.shape) != (H, d):
+        raise ValueError("decay must be fp32 [H, d]")
+    if out is None:
+        out = torch.empty_like(q)
+    st = load().lightning_attn_decode_channel_decay(
+        _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(decay, "decay"), _dev(state, "state"),
+        Bn, H, d, _dtype_code(q), _dev(out, "out"), _stream_handle(stream))
+    _check(st, "lightning_attn_decode_channel_decay")
     return out
 
 

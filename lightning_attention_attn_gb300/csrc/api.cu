@@ -65,6 +65,56 @@ size_t backward_slot_bytes(int32_t total_tokens, int32_t num_heads, int32_t head
     return (b + 255) & ~(size_t)255;
 }
 
+// Argument checks shared by the prefill entry points.  Returns an error, or
+// LA_OK with *work = false when there is nothing to launch (no sequences, or
+// every sequence empty: then the final states have been set here).
+la_status check_prefill(const void *q, const void *k, const void *v, const float *decay,
+                        const int32_t *cu_seqlens, int32_t num_seqs, int32_t total_tokens,
+                        int32_t num_heads, int32_t head_dim, int32_t chunk, la_dtype dtype,
+                        const float *initial_state, void *out, float *final_state,
+                        void *stream, bool *work) {
+    *work = false;
+    if (num_seqs < 0) return fail(LA_ERR_INVALID_ARG, "num_seqs < 0 (%d)", num_seqs);
+    if (total_tokens < 0) return fail(LA_ERR_INVALID_ARG, "total_tokens < 0 (%d)", total_tokens);
+    if (num_heads < 1) return fail(LA_ERR_INVALID_ARG, "num_heads < 1 (%d)", num_heads);
+    if (head_dim != 64 && head_dim != 128)
+        return fail(LA_ERR_INVALID_ARG, "head_dim must be 64 or 128 (got %d)", head_dim);
+    if (dtype != LA_DTYPE_BF16 && dtype != LA_DTYPE_FP32)
+        return fail(LA_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+    if (chunk != 0 && chunk != 16 && chunk != 32 && chunk != 64 && chunk != 128 && chunk != 256)
+        return fail(LA_ERR_INVALID_ARG, "chunk must be 0, 16, 32, 64, 128 or 256 (got %d)", chunk);
+    if (num_seqs == 0) return LA_OK;
+    if (!cu_seqlens || !decay) return fail(LA_ERR_INVALID_ARG, "null decay or cu_seqlens");
+    if (total_tokens > 0 && (!q || !k || !v || !out))
+        return fail(LA_ERR_INVALID_ARG, "null q, k, v or out");
+    if ((q && !aligned16(q)) || (k && !aligned16(k)) || (v && !aligned16(v)) ||
+        (out && !aligned16(out)) || (final_state && !aligned16(final_state)) ||
+        (initial_state && !aligned16(initial_state)) || !aligned16(decay) ||
+        !aligned16(cu_seqlens))
+        return fail(LA_ERR_INVALID_ARG, "every pointer must be 16-byte aligned");
+    if ((long long)num_seqs * num_heads > 0x7fffffffLL / 4)
+        return fail(LA_ERR_INVALID_ARG, "num_seqs * num_heads too large");
+    const size_t state_bytes = (size_t)num_seqs * num_heads * head_dim * head_dim * sizeof(float);
+    if (initial_state && final_state && initial_state != final_state) {
+        const uintptr_t a0 = reinterpret_cast<uintptr_t>(initial_state);
+        const uintptr_t b0 = reinterpret_cast<uintptr_t>(final_state);
+        if (a0 < b0 + state_bytes && b0 < a0 + state_bytes)
+            return fail(LA_ERR_INVALID_ARG,
+                        "initial_state and final_state overlap without being the same array");
+    }
+    if (total_tokens == 0) {  // every sequence is empty: each state is its cached state
+        const cudaStream_t st = static_cast<cudaStream_t>(stream);
+        if (!final_state || final_state == initial_state) return LA_OK;
+        if (initial_state)
+            return from_cuda(cudaMemcpyAsync(final_state, initial_state, state_bytes,
+                                             cudaMemcpyDeviceToDevice, st),
+                             "prefill (empty)");
+        return from_cuda(cudaMemsetAsync(final_state, 0, state_bytes, st), "prefill (empty)");
+    }
+    *work = true;
+    return LA_OK;
+}
+
 }  // namespace
 
 namespace la {
@@ -102,47 +152,14 @@ la_status lightning_attn_prefill_with_state(const void *q, const void *k, const 
                                             int32_t chunk, la_dtype dtype,
                                             const float *initial_state, void *out,
                                             float *final_state, void *stream) {
-    if (num_seqs < 0) return fail(LA_ERR_INVALID_ARG, "num_seqs < 0 (%d)", num_seqs);
-    if (total_tokens < 0) return fail(LA_ERR_INVALID_ARG, "total_tokens < 0 (%d)", total_tokens);
-    if (num_heads < 1) return fail(LA_ERR_INVALID_ARG, "num_heads < 1 (%d)", num_heads);
-    if (head_dim != 64 && head_dim != 128)
-        return fail(LA_ERR_INVALID_ARG, "head_dim must be 64 or 128 (got %d)", head_dim);
-    if (dtype != LA_DTYPE_BF16 && dtype != LA_DTYPE_FP32)
-        return fail(LA_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
-    if (chunk != 0 && chunk != 16 && chunk != 32 && chunk != 64 && chunk != 128 && chunk != 256)
-        return fail(LA_ERR_INVALID_ARG, "chunk must be 0, 16, 32, 64, 128 or 256 (got %d)", chunk);
-    if (num_seqs == 0) return LA_OK;
-    if (!cu_seqlens || !decay) return fail(LA_ERR_INVALID_ARG, "null decay or cu_seqlens");
-    if (total_tokens > 0 && (!q || !k || !v || !out))
-        return fail(LA_ERR_INVALID_ARG, "null q, k, v or out");
-    if ((q && !aligned16(q)) || (k && !aligned16(k)) || (v && !aligned16(v)) ||
-        (out && !aligned16(out)) || (final_state && !aligned16(final_state)) ||
-        (initial_state && !aligned16(initial_state)) || !aligned16(decay) ||
-        !aligned16(cu_seqlens))
-        return fail(LA_ERR_INVALID_ARG, "every pointer must be 16-byte aligned");
-    if ((long long)num_seqs * num_heads > 0x7fffffffLL / 4)
-        return fail(LA_ERR_INVALID_ARG, "num_seqs * num_heads too large");
-    const size_t state_bytes = (size_t)num_seqs * num_heads * head_dim * head_dim * sizeof(float);
-    if (initial_state && final_state && initial_state != final_state) {
-        const uintptr_t a0 = reinterpret_cast<uintptr_t>(initial_state);
-        const uintptr_t b0 = reinterpret_cast<uintptr_t>(final_state);
-        if (a0 < b0 + state_bytes && b0 < a0 + state_bytes)
-            return fail(LA_ERR_INVALID_ARG,
-                        "initial_state and final_state overlap without being the same array");
-    }
-
+    bool work = false;
+    const la_status st = check_prefill(q, k, v, decay, cu_seqlens, num_seqs, total_tokens,
+                                       num_heads, head_dim, chunk, dtype, initial_state, out,
+                                       final_state, stream, &work);
+    if (st != LA_OK || !work) return st;
     la::PrefillArgs a{q, k, v, decay, cu_seqlens, num_seqs, total_tokens, num_heads,
                       head_dim, chunk, out, final_state, static_cast<cudaStream_t>(stream),
                       initial_state};
-    if (total_tokens == 0) {  // every sequence is empty: each state is its cached state
-        if (!final_state || final_state == initial_state) return LA_OK;
-        if (initial_state)
-            return from_cuda(cudaMemcpyAsync(final_state, initial_state, state_bytes,
-                                             cudaMemcpyDeviceToDevice, a.stream),
-                             "prefill (empty)");
-        return from_cuda(cudaMemsetAsync(final_state, 0, state_bytes, a.stream),
-                         "prefill (empty)");
-    }
     return run_prefill(a, dtype);
 }
 
@@ -155,6 +172,54 @@ la_status lightning_attn_prefill(const void *q, const void *k, const void *v,
     return lightning_attn_prefill_with_state(q, k, v, decay, cu_seqlens, num_seqs, total_tokens,
                                              num_heads, head_dim, chunk, dtype, nullptr, out,
                                              final_state, stream);
+}
+
+la_status lightning_attn_prefill_channel_decay(const void *q, const void *k, const void *v,
+                                               const float *decay, const int32_t *cu_seqlens,
+                                               int32_t num_seqs, int32_t total_tokens,
+                                               int32_t num_heads, int32_t head_dim, int32_t chunk,
+                                               la_dtype dtype, const float *initial_state,
+                                               void *out, float *final_state, void *stream) {
+    bool work = false;
+    const la_status st = check_prefill(q, k, v, decay, cu_seqlens, num_seqs, total_tokens,
+                                       num_heads, head_dim, chunk, dtype, initial_state, out,
+                                       final_state, stream, &work);
+    if (st != LA_OK || !work) return st;
+    if (chunk == 128 || chunk == 256)
+        return fail(LA_ERR_UNSUPPORTED,
+                    "channel-wise decay runs on the CUDA-core kernel: chunk 0, 16, 32 or 64");
+    la::PrefillArgs a{q, k, v, decay, cu_seqlens, num_seqs, total_tokens, num_heads,
+                      head_dim, chunk, out, final_state, static_cast<cudaStream_t>(stream),
+                      initial_state};
+    a.channel_decay = true;
+    if (dtype == LA_DTYPE_FP32)
+        return from_cuda(la::prefill_simt_f32(a), "prefill (channel-wise decay, fp32)");
+    return from_cuda(la::prefill_simt_bf16(a), "prefill (channel-wise decay, bf16)");
+}
+
+la_status lightning_attn_decode_channel_decay(const void *q, const void *k, const void *v,
+                                              const float *decay, float *state, int32_t batch,
+                                              int32_t num_heads, int32_t head_dim,
+                                              la_dtype dtype, void *out, void *stream) {
+    if (batch < 0) return fail(LA_ERR_INVALID_ARG, "batch < 0 (%d)", batch);
+    if (num_heads < 1) return fail(LA_ERR_INVALID_ARG, "num_heads < 1 (%d)", num_heads);
+    if (head_dim != 64 && head_dim != 128)
+        return fail(LA_ERR_INVALID_ARG, "head_dim must be 64 or 128 (got %d)", head_dim);
+    if (dtype != LA_DTYPE_BF16 && dtype != LA_DTYPE_FP32)
+        return fail(LA_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+    if (batch == 0) return LA_OK;
+    if (!q || !k || !v || !decay || !state || !out)
+        return fail(LA_ERR_INVALID_ARG, "null pointer argument");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(decay) ||
+        !aligned16(state) || !aligned16(out))
+        return fail(LA_ERR_INVALID_ARG, "every pointer must be 16-byte aligned");
+    if ((long long)batch * num_heads > 0x7fffffffLL)
+        return fail(LA_ERR_INVALID_ARG, "batch * num_heads too large");
+    la::DecodeArgs a{q, k, v, decay, state, batch, num_heads, head_dim, out,
+                     static_cast<cudaStream_t>(stream)};
+    a.channel_decay = true;
+    if (dtype == LA_DTYPE_FP32) return from_cuda(la::decode_f32(a), "decode (channel-wise, fp32)");
+    return from_cuda(la::decode_bf16(a), "decode (channel-wise, bf16)");
 }
 
 la_status lightning_attn_decode(const void *q, const void *k, const void *v,

@@ -46,7 +46,7 @@ __device__ __forceinline__ float vget(const float2 &x, int c) { return c == 0 ? 
 
 // Rows are processed in groups of kRowsPerPass to bound registers while
 // keeping that many independent 16-byte loads in flight per thread.
-template <typename T, int D>
+template <typename T, int D, bool CW>
 __global__ void __launch_bounds__(kThreads)
 decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
               const float *__restrict__ decay, float *__restrict__ state, int H,
@@ -62,7 +62,8 @@ decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
     const long pair = blockIdx.x;           // b * H + h
     const int h = (int)(pair % H);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const float lam = __ldg(decay + h);
+    // one lambda per head, or per key channel (state row) with CW
+    const float lam = CW ? 0.f : __ldg(decay + h);
 
     // token row of entry b: b itself, or in a packed batch (mixed prefill +
     // decode step, §3.3.2) the start of sequence b when it has exactly one
@@ -101,9 +102,10 @@ decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
         for (int r = 0; r < kRowsPerPass; ++r) {
             const int i = warp * RPW + r0 + r;
             const float ki = ks[i], qi = qs[i];
+            const float li = CW ? __ldg(decay + (long)h * D + i) : lam;
 #pragma unroll
             for (int c = 0; c < VEC; ++c) {
-                const float nv = fmaf(lam, vget(sv[r], c), ki * vj[c]);
+                const float nv = fmaf(li, vget(sv[r], c), ki * vj[c]);
                 vset(sv[r], c, nv);
                 acc[c] = fmaf(qi, nv, acc[c]);
             }
@@ -127,7 +129,8 @@ cudaError_t launch(const DecodeArgs &a) {
     const long grid = (long)a.batch * a.num_heads;
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffffL) return cudaErrorInvalidConfiguration;
-    decode_kernel<T, D><<<(unsigned)grid, kThreads, 0, a.stream>>>(
+    auto kern = a.channel_decay ? decode_kernel<T, D, true> : decode_kernel<T, D, false>;
+    kern<<<(unsigned)grid, kThreads, 0, a.stream>>>(
         static_cast<const T *>(a.q), static_cast<const T *>(a.k),
         static_cast<const T *>(a.v), a.decay, a.state, a.num_heads,
         static_cast<T *>(a.out), a.cu_seqlens, a.total_tokens);

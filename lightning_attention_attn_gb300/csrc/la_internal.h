@@ -21,6 +21,7 @@ struct PrefillArgs {
     // > 0: launch only the work of the rank_limit longest sequences (ranks
     // are in order of length, longest first, for nseq <= kMaxSortedSeqs)
     int rank_limit = 0;
+    bool channel_decay = false; // decay is [H, D]: one lambda per key channel
 };
 
 struct DecodeArgs {
@@ -35,9 +36,11 @@ struct DecodeArgs {
     // exactly 1 are stepped (the others are left untouched).
     const int32_t *cu_seqlens = nullptr;
     int total_tokens = 0;
+    bool channel_decay = false; // decay is [H, D]: one lambda per key channel (state row)
 };
 
-// CUDA-core chunkwise prefill; chunk in {16, 32, 64}, head_dim in {64, 128}.
+// CUDA-core chunkwise prefill; chunk in {16, 32, 64}, head_dim in {64, 128};
+// also the channel-wise decay variant.
 cudaError_t prefill_simt_f32(const PrefillArgs &a);
 cudaError_t prefill_simt_bf16(const PrefillArgs &a);
 

@@ -30,7 +30,7 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float
     return __float2bfloat16_rn(x);
 }
 
-template <int D, int B>
+template <int D, int B, bool CW>
 struct SimtSmem {
     static constexpr int DP = D + 1;  // padded row: conflict-free column walks
     float q[B][DP];
@@ -40,10 +40,12 @@ struct SimtSmem {
     float p[B][B + 1];
     float pw[B + 1];  // pw[e] = lambda^e, e = 0..B
     float gk[B];      // lambda^(B_i-1-l) for l < B_i, else 0
+    // channel-wise decay: pwc[e][i] = lambda_i^e, e = 0..B
+    float pwc[CW ? B + 1 : 1][CW ? D : 1];
     int slot;
 };
 
-template <typename T, int D, int B>
+template <typename T, int D, int B, bool CW>
 __global__ void __launch_bounds__(kThreads)
 prefill_simt_kernel(const T *__restrict__ q, const T *__restrict__ k,
                     const T *__restrict__ v, const float *__restrict__ decay,
@@ -51,7 +53,7 @@ prefill_simt_kernel(const T *__restrict__ q, const T *__restrict__ k,
                     const float *initial_state, T *__restrict__ out, float *final_state,
                     int reverse_out, int min_len) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    auto &sm = *reinterpret_cast<SimtSmem<D, B> *>(smem_raw);
+    auto &sm = *reinterpret_cast<SimtSmem<D, B, CW> *>(smem_raw);
     const int tid = threadIdx.x;
 
     const int h = blockIdx.x % H;
@@ -62,9 +64,16 @@ prefill_simt_kernel(const T *__restrict__ q, const T *__restrict__ k,
     t1 = min(max(t1, t0), T_total);
     const int L = t1 - t0;
     if (L < min_len) return;  // a mixed step's decode launch owns this sequence
-    const float lam = __ldg(decay + h);
+    const float lam = CW ? 1.f : __ldg(decay + h);
 
     for (int e = tid; e <= B; e += kThreads) sm.pw[e] = powf(lam, (float)e);
+    if constexpr (CW) {
+        // channel-wise decay (K3 report reading notes): lambda per key
+        // channel i, decay[h * D + i]; every factor below is lambda_i^e with
+        // e >= 0 from this table
+        for (int e = tid; e < (B + 1) * D; e += kThreads)
+            sm.pwc[e / D][e % D] = powf(__ldg(decay + (long)h * D + e % D), (float)(e / D));
+    }
     // KV_{-1}: the sequence's cached state (prefix KV cache, §3.3.1), else 0.
     // initial_state may be final_state itself: it is read here, before any
     // write of this CTA's final state.
@@ -98,9 +107,15 @@ prefill_simt_kernel(const T *__restrict__ q, const T *__restrict__ k,
             const int j = e / B, l = e % B;
             float acc = 0.f;
             if (l <= j && j < Lc) {
+                if constexpr (CW) {
+                    const float *w = sm.pwc[j - l];
 #pragma unroll 8
-                for (int i = 0; i < D; ++i) acc = fmaf(sm.q[j][i], sm.k[l][i], acc);
-                acc *= sm.pw[j - l];
+                    for (int i = 0; i < D; ++i) acc = fmaf(sm.q[j][i] * w[i], sm.k[l][i], acc);
+                } else {
+#pragma unroll 8
+                    for (int i = 0; i < D; ++i) acc = fmaf(sm.q[j][i], sm.k[l][i], acc);
+                    acc *= sm.pw[j - l];
+                }
             }
             sm.p[j][l] = acc;
         }
@@ -113,9 +128,17 @@ prefill_simt_kernel(const T *__restrict__ q, const T *__restrict__ k,
             float intra = 0.f;
             for (int l = 0; l <= j; ++l) intra = fmaf(sm.p[j][l], sm.v[l][n], intra);
             float inter = 0.f;
+            float o;
+            if constexpr (CW) {
+                const float *w = sm.pwc[j + 1];
 #pragma unroll 8
-            for (int i = 0; i < D; ++i) inter = fmaf(sm.q[j][i], sm.kv[i][n], inter);
-            const float o = fmaf(sm.pw[j + 1], inter, intra);
+                for (int i = 0; i < D; ++i) inter = fmaf(sm.q[j][i] * w[i], sm.kv[i][n], inter);
+                o = intra + inter;
+            } else {
+#pragma unroll 8
+                for (int i = 0; i < D; ++i) inter = fmaf(sm.q[j][i], sm.kv[i][n], inter);
+                o = fmaf(sm.pw[j + 1], inter, intra);
+            }
             // with reverse_out the sequence is written back to front
             const long row = reverse_out ? (long)(t1 - 1 - c0 - j) : (long)(t0 + c0 + j);
             out[row * row_stride + (long)h * D + n] = from_f<T>(o);
@@ -127,8 +150,14 @@ prefill_simt_kernel(const T *__restrict__ q, const T *__restrict__ k,
         for (int e = tid; e < D * D; e += kThreads) {
             const int i = e / D, n = e % D;
             float acc = 0.f;
-            for (int l = 0; l < Lc; ++l) acc = fmaf(sm.gk[l] * sm.k[l][i], sm.v[l][n], acc);
-            sm.kv[i][n] = fmaf(dec, sm.kv[i][n], acc);
+            if constexpr (CW) {
+                for (int l = 0; l < Lc; ++l)
+                    acc = fmaf(sm.pwc[Lc - 1 - l][i] * sm.k[l][i], sm.v[l][n], acc);
+                sm.kv[i][n] = fmaf(sm.pwc[Lc][i], sm.kv[i][n], acc);
+            } else {
+                for (int l = 0; l < Lc; ++l) acc = fmaf(sm.gk[l] * sm.k[l][i], sm.v[l][n], acc);
+                sm.kv[i][n] = fmaf(dec, sm.kv[i][n], acc);
+            }
         }
         __syncthreads();
     }
@@ -139,10 +168,10 @@ prefill_simt_kernel(const T *__restrict__ q, const T *__restrict__ k,
     }
 }
 
-template <typename T, int D, int B>
+template <typename T, int D, int B, bool CW>
 cudaError_t launch(const PrefillArgs &a) {
-    auto kern = prefill_simt_kernel<T, D, B>;
-    const size_t smem = sizeof(SimtSmem<D, B>);
+    auto kern = prefill_simt_kernel<T, D, B, CW>;
+    const size_t smem = sizeof(SimtSmem<D, B, CW>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
@@ -157,24 +186,28 @@ cudaError_t launch(const PrefillArgs &a) {
     return cudaGetLastError();
 }
 
-template <typename T>
+template <typename T, bool CW>
 cudaError_t dispatch(const PrefillArgs &a) {
     const int B = a.chunk == 0 ? 64 : a.chunk;
     if (a.head_dim == 64) {
-        if (B == 16) return launch<T, 64, 16>(a);
-        if (B == 32) return launch<T, 64, 32>(a);
-        if (B == 64) return launch<T, 64, 64>(a);
+        if (B == 16) return launch<T, 64, 16, CW>(a);
+        if (B == 32) return launch<T, 64, 32, CW>(a);
+        if (B == 64) return launch<T, 64, 64, CW>(a);
     } else if (a.head_dim == 128) {
-        if (B == 16) return launch<T, 128, 16>(a);
-        if (B == 32) return launch<T, 128, 32>(a);
-        if (B == 64) return launch<T, 128, 64>(a);
+        if (B == 16) return launch<T, 128, 16, CW>(a);
+        if (B == 32) return launch<T, 128, 32, CW>(a);
+        if (B == 64) return launch<T, 128, 64, CW>(a);
     }
     return cudaErrorNotSupported;
 }
 
 }  // namespace
 
-cudaError_t prefill_simt_f32(const PrefillArgs &a) { return dispatch<float>(a); }
-cudaError_t prefill_simt_bf16(const PrefillArgs &a) { return dispatch<__nv_bfloat16>(a); }
+cudaError_t prefill_simt_f32(const PrefillArgs &a) {
+    return a.channel_decay ? dispatch<float, true>(a) : dispatch<float, false>(a);
+}
+cudaError_t prefill_simt_bf16(const PrefillArgs &a) {
+    return a.channel_decay ? dispatch<__nv_bfloat16, true>(a) : dispatch<__nv_bfloat16, false>(a);
+}
 
 }  // namespace la

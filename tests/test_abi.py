@@ -21,7 +21,8 @@ def test_header_declares_expected_calls():
     names = la.header_functions()
     for n in ("lightning_attn_prefill", "lightning_attn_prefill_with_state",
               "lightning_attn_backward", "lightning_attn_backward_workspace_bytes",
-              "lightning_attn_mixed_step",
+              "lightning_attn_mixed_step", "lightning_attn_prefill_channel_decay",
+              "lightning_attn_decode_channel_decay",
               "lightning_attn_decode",
               "lightning_attn_status_string", "lightning_attn_last_error",
               "lightning_attn_version", "lightning_attn_device_status",
@@ -39,7 +40,7 @@ def test_library_exports_every_header_symbol(lib):
 
 
 def test_version(lib):
-    assert la.version() == (1, 3)
+    assert la.version() == (1, 4)
 
 
 def test_status_strings(lib):
@@ -219,3 +220,17 @@ def test_mixed_step_host_validation(lib, kw, status):
                                        args["dtype"], args["state"], args["out"], None, None,
                                        None)
     assert st == status
+
+
+def test_channel_decay_host_validation(lib):
+    f = lib.lightning_attn_prefill_channel_decay
+    common = (A, A, A, A, A, 1, 8, 2, 128)
+    # chunk 128 is the tensor-core block, which has no channel-wise variant
+    assert f(*common, 128, la.LA_DTYPE_BF16, None, A, A, None) == la.LA_ERR_UNSUPPORTED
+    assert f(*common, 48, la.LA_DTYPE_BF16, None, A, A, None) == la.LA_ERR_INVALID_ARG
+    assert f(A, A, A, A + 4, A, 1, 8, 2, 128, 0, la.LA_DTYPE_BF16, None, A, A, None) == \
+        la.LA_ERR_INVALID_ARG
+    assert f(A, A, A, A, A, 0, 8, 2, 128, 0, la.LA_DTYPE_BF16, None, A, A, None) == la.LA_OK
+    g = lib.lightning_attn_decode_channel_decay
+    assert g(A, A, A, A, A, 4, 2, 96, la.LA_DTYPE_BF16, A, None) == la.LA_ERR_INVALID_ARG
+    assert g(A, A, A, A, A, 0, 2, 128, la.LA_DTYPE_BF16, A, None) == la.LA_OK

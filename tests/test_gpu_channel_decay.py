@@ -1,0 +1,74 @@
+"""GPU parity of the channel-wise (per key channel) decay variant against the
+fp64 CPU oracle (K3 report reading notes: the scalar decay generalised to one
+decay per channel; kv_t[i][j] = lambda_i kv_{t-1}[i][j] + k_t[i] v_t[j]).
+Tolerances as in parity.py."""
+import pytest
+import torch
+
+import oracle
+import lightning_attention_attn_gb300 as la
+from lightning_attention_attn_gb300 import build as labuild
+from lightning_attention_attn_gb300 import workloads as wl
+from parity import TOL_BF16, TOL_FP32, assert_close
+
+pytestmark = pytest.mark.gpu
+
+RAGGED = [1, 0, 15, 16, 17, 63, 64, 65, 129, 300, 0, 257]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    la.load(labuild.build())
+    yield
+    la.device_status()
+
+
+def channel_decays(H, d, seed):
+    """lambda_{h,i} spread over [0.3, 1.0] (seeded), fp32 [H, d]."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    return (0.3 + 0.7 * torch.rand((H, d), generator=g)).to(torch.float32)
+
+
+@pytest.mark.parametrize("dtype, d, chunk, tol", [
+    (torch.float32, 64, 16, TOL_FP32), (torch.float32, 128, 64, TOL_FP32),
+    (torch.bfloat16, 128, 64, TOL_BF16), (torch.bfloat16, 64, 32, TOL_BF16)])
+def test_channel_decay_prefill(dtype, d, chunk, tol):
+    H = 3
+    inp = wl.prefill_inputs(RAGGED, H, d, dtype=dtype, seed=51, device="cuda")
+    lam = channel_decays(H, d, 52)
+    s0 = wl.cached_states(len(RAGGED), H, d, seed=53, device="cuda")
+    out, st = la.prefill_channel_decay(inp.q, inp.k, inp.v, lam.cuda(), inp.cu_seqlens,
+                                       chunk=chunk, initial_state=s0)
+    torch.cuda.synchronize()
+    ref, ref_st = oracle.recurrent_cw(inp.q, inp.k, inp.v, lam, inp.cu_seqlens.cpu(),
+                                      initial_state=s0.cpu())
+    assert_close(out, ref, tol, f"channel decay {dtype} d={d} B={chunk} out")
+    assert_close(st, ref_st, tol, f"channel decay {dtype} d={d} B={chunk} state")
+
+
+def test_channel_decay_uniform_equals_scalar_kernel():
+    """Equal channel decays give the scalar-decay result (CUDA-core path)."""
+    H, d = 4, 128
+    inp = wl.prefill_inputs([300, 65], H, d, dtype=torch.float32, seed=54, device="cuda")
+    lam_cw = inp.decay[:, None].repeat(1, d).contiguous()
+    a, sa = la.prefill_channel_decay(inp.q, inp.k, inp.v, lam_cw, inp.cu_seqlens, chunk=64)
+    b, sb = la.prefill(inp.q, inp.k, inp.v, inp.decay, inp.cu_seqlens, chunk=64)
+    torch.cuda.synchronize()
+    assert_close(a, b.double(), TOL_FP32, "uniform channel decay vs scalar out")
+    assert_close(sa, sb.double(), TOL_FP32, "uniform channel decay vs scalar state")
+
+
+@pytest.mark.parametrize("dtype, tol", [(torch.float32, TOL_FP32), (torch.bfloat16, TOL_BF16)])
+def test_channel_decay_decode(dtype, tol):
+    B, H, d = 6, 4, 128
+    dinp = wl.decode_inputs(B, H, d, steps=1, dtype=dtype, seed=55, device="cuda")
+    lam = channel_decays(H, d, 56)
+    st0 = dinp.state.cpu()
+    out = la.decode_channel_decay(dinp.q[0], dinp.k[0], dinp.v[0], lam.cuda(), dinp.state)
+    torch.cuda.synchronize()
+    ref, ref_st = oracle.decode_cw(dinp.q[0], dinp.k[0], dinp.v[0], lam, st0)
+    assert_close(out, ref, tol, f"channel decay decode {dtype} out")
+    assert_close(dinp.state, ref_st, TOL_FP32, f"channel decay decode {dtype} state")

@@ -50,6 +50,22 @@ def peaks():
     return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
 
 
+def fp32_alu_peak_tflops(sms):
+    """FFMA peak of the CUDA cores: 128 fp32 lanes per SM, 2 flops per FMA,
+    at the maximum SM clock of 2070 MHz."""
+    return sms * 128 * 2 * 2.070e9 / 1e12
+
+
+def cuda_core_roofline(flops, byts, ms, pk, sms):
+    """The CUDA-core (FFMA) prefill is bound by fp32 arithmetic, not HBM."""
+    peak = fp32_alu_peak_tflops(sms)
+    tf = flops / (ms / 1e3) / 1e12
+    return {"bound": "alu", "alg_flops": flops, "achieved": round(tf, 2),
+            "peak": round(peak, 2), "unit": "TFLOP/s", "frac": round(tf / peak, 4),
+            "peak_source": "derived: SMs x 128 fp32 lanes x 2 x 2070 MHz",
+            "hbm_frac": round(byts / (ms / 1e3) / 1e9 / pk["hbm"], 4)}
+
+
 def src_hash(path):
     with open(path, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
@@ -301,6 +317,11 @@ def run_ours(args, ws, rank, local):
         la.device_status(stream)
         ms = a0.elapsed_time(a1) / reps
         Tn = sum(lengths)
+        if chunk not in (0, 128):
+            byts, flops = prefill_alg(Tn, H, d, chunk, len(lengths))
+            return {"ms_per_launch": round(ms, 4), "tokens_per_s": round(Tn / (ms / 1e3), 1),
+                    "tokens": Tn, "chunk": chunk, "kernel": "prefill_simt_kernel (FFMA)",
+                    "roofline": cuda_core_roofline(flops, byts, ms, pk, sms)}
         byts, flops = prefill_alg(Tn, H, d, 128, len(lengths))
         return {"ms_per_launch": round(ms, 4), "tokens_per_s": round(Tn / (ms / 1e3), 1),
                 "tokens": Tn, "chunk": chunk,
@@ -328,16 +349,16 @@ def run_ours(args, ws, rank, local):
         torch.cuda.synchronize()
         ms = a0.elapsed_time(a1) / reps
         Tn = sum(lengths)
-        byts, _ = prefill_alg(Tn, H, d, 64, len(lengths))
+        byts, flops = prefill_alg(Tn, H, d, 64, len(lengths))
         return {"ms_per_launch": round(ms, 3), "tokens_per_s": round(Tn / (ms / 1e3), 1),
-                "kernel": "CUDA-core (FFMA) prefill, chunk 64",
-                "roofline": {"bound": "hbm", "alg_bytes": byts,
-                             "achieved": round(byts / (ms / 1e3) / 1e9, 1), "peak": pk["hbm"],
-                             "unit": "GB/s", "frac": round(byts / (ms / 1e3) / 1e9 / pk["hbm"], 4)}}
+                "chunk": 64, "kernel": "prefill_simt_kernel (FFMA), per-channel decay",
+                "roofline": cuda_core_roofline(flops, byts, ms, pk, sms)}
 
-    more = {"prefill_8k_channel_decay": time_channel_decay([8192], 2),
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    more = {"prefill_8k_channel_decay": time_channel_decay([8192], 10),
+            "prefill_8k_chunk64_cuda_cores": time_prefill([8192], 64, 10),
             "prefill_128k": time_prefill([131072], 0, 5),
-            "prefill_128k_chunk64_cuda_cores": time_prefill([131072], 64, 1),
+            "prefill_128k_chunk64_cuda_cores": time_prefill([131072], 64, 3),
             "prefill_128k_chunk256": "not run: the tensor-core block is 128 (chunk 256 returns "
                                      "LA_ERR_UNSUPPORTED)",
             "varlen_16": time_prefill(wl.varlen_lengths().tolist(), 0, 5)}
@@ -560,6 +581,23 @@ def run_only(args):
         fs = torch.empty((1, cfg["num_heads"], 128, 128), device="cuda")
         for _ in range(args.warmup + args.steps):
             la.prefill(inp.q, inp.k, inp.v, inp.decay, inp.cu_seqlens, out=out, final_state=fs)
+    elif args.only in ("channel_decay", "prefill_chunk64"):
+        # the CUDA-core kernel on the 8K-token layer: per-channel decay
+        # (lambda_h scaled by 1 - 0.01 i / (d - 1) for key channel i), or the
+        # scalar decay at chunk 64
+        cfg = wl.PREFILL_8K
+        inp = wl.prefill_inputs(cfg["lengths"], cfg["num_heads"], cfg["head_dim"],
+                                dtype=torch.bfloat16, seed=0, device="cuda")
+        d = cfg["head_dim"]
+        lam_cw = inp.decay[:, None].repeat(1, d).contiguous()
+        lam_cw = lam_cw * (1.0 - 0.01 * torch.linspace(0, 1, d, device="cuda"))[None, :]
+        out = torch.empty_like(inp.q)
+        for _ in range(args.warmup + args.steps):
+            if args.only == "channel_decay":
+                la.prefill_channel_decay(inp.q, inp.k, inp.v, lam_cw, inp.cu_seqlens, chunk=64,
+                                         out=out)
+            else:
+                la.prefill(inp.q, inp.k, inp.v, inp.decay, inp.cu_seqlens, chunk=64, out=out)
     elif args.only == "backward":
         cfg = wl.PREFILL_8K
         inp = wl.prefill_inputs(cfg["lengths"], cfg["num_heads"], cfg["head_dim"],
@@ -622,7 +660,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--only", choices=["prefill", "decode", "backward"], default=None,
+    ap.add_argument("--only", choices=["prefill", "decode", "backward", "channel_decay",
+                                       "prefill_chunk64"], default=None,
                     help="profiling aid: run just W + K launches of one kernel on its "
                          "workload and print nothing else")
     args = ap.parse_args(argv)

@@ -21,142 +21,459 @@ namespace la {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kDV = 64;  // value columns per CTA
 
-__device__ __forceinline__ float to_f(float x) { return x; }
-__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
-template <typename T> __device__ __forceinline__ T from_f(float x);
-template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
-template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) {
-    return __float2bfloat16_rn(x);
+// two adjacent elements as they are loaded from global memory
+template <typename T> struct Pair;
+template <> struct Pair<float> { using type = float2; };
+template <> struct Pair<__nv_bfloat16> { using type = __nv_bfloat162; };
+__device__ __forceinline__ float2 to_f2(float2 x) { return x; }
+__device__ __forceinline__ float2 to_f2(__nv_bfloat162 x) { return __bfloat1622float2(x); }
+template <typename R> __device__ __forceinline__ R zero_pair();
+template <> __device__ __forceinline__ float2 zero_pair<float2>() { return make_float2(0.f, 0.f); }
+template <> __device__ __forceinline__ __nv_bfloat162 zero_pair<__nv_bfloat162>() {
+    return __floats2bfloat162_rn(0.f, 0.f);
+}
+
+// four consecutive outputs of one row
+__device__ __forceinline__ void store4(float *p, float a, float b, float c, float d) {
+    *reinterpret_cast<float4 *>(p) = make_float4(a, b, c, d);
+}
+__device__ __forceinline__ void store4(__nv_bfloat16 *p, float a, float b, float c, float d) {
+    uint2 u;
+    __nv_bfloat162 lo = __floats2bfloat162_rn(a, b), hi = __floats2bfloat162_rn(c, d);
+    u.x = *reinterpret_cast<uint32_t *>(&lo);
+    u.y = *reinterpret_cast<uint32_t *>(&hi);
+    *reinterpret_cast<uint2 *>(p) = u;
+}
+
+// N consecutive floats of shared memory (N in {1, 2, 4, 8}; p aligned to N floats)
+template <int N> __device__ __forceinline__ void lds(float (&x)[N], const float *p) {
+    if constexpr (N == 1) {
+        x[0] = *p;
+    } else if constexpr (N == 2) {
+        const float2 a = *reinterpret_cast<const float2 *>(p);
+        x[0] = a.x; x[1] = a.y;
+    } else {
+#pragma unroll
+        for (int c = 0; c < N; c += 4) {
+            const float4 a = *reinterpret_cast<const float4 *>(p + c);
+            x[c] = a.x; x[c + 1] = a.y; x[c + 2] = a.z; x[c + 3] = a.w;
+        }
+    }
+}
+
+// Runs mac() over n steps (n a multiple of 2 * G), G steps per stage, with the
+// shared-memory operands of the next stage loaded while the current one
+// computes: two register stages, so that a load's latency is covered by the
+// FMAs of a whole stage instead of stalling the next step.
+template <class Stage, int G, class Ld, class Mac>
+__device__ __forceinline__ void pipelined(int n, Ld &&ld, Mac &&mac) {
+    Stage a, b;
+    ld(a, 0);
+    for (int s = 0; s < n; s += 2 * G) {
+        ld(b, s + G);
+        mac(a);
+        if (s + 2 * G < n) ld(a, s + 2 * G);
+        mac(b);
+    }
 }
 
 template <int D, int B, bool CW>
 struct SimtSmem {
-    static constexpr int DP = D + 1;  // padded row: conflict-free column walks
-    float q[B][DP];
-    float k[B][DP];
-    float v[B][D];
-    float kv[D][D];
-    float p[B][B + 1];
-    float pw[B + 1];  // pw[e] = lambda^e, e = 0..B
-    float gk[B];      // lambda^(B_i-1-l) for l < B_i, else 0
-    // channel-wise decay: pwc[e][i] = lambda_i^e, e = 0..B
-    float pwc[CW ? B + 1 : 1][CW ? D : 1];
+    static constexpr int P = B + 4;   // padded row: conflict-free transposing stores
+    static constexpr int WP = B + 8;  // channel-decay table row (see below)
+    float qT[D][P];                   // Q_i channel-major: qT[i][j] = q_j[i]
+    float kT[D][P];                   // K_i channel-major; after the scores it holds P^T
+    float kS[B][D];                   // K_i token-major, rows scaled by the state's decay
+    float vS[B][kDV];                 // the CTA's value slice of V_i
+    float kv[D][kDV];                 // the CTA's value slice of the state KV
+    float pw[B + 4];                  // lambda^e, e = 0..B (scalar decay)
+    // channel-wise decay: wz[i][4 + e] = lambda_i^e for e = 0..B, zero elsewhere,
+    // so that an 8-wide window starting at 4 (j - l) - 4 below a 4 x 4 tile
+    // reads zero for every l > j
+    float wz[CW ? D : 1][CW ? WP : 1];
+    // the same powers exponent-major, wk[e][i] = lambda_i^e (e = 0..B), for
+    // the staging of K_s, whose lanes walk consecutive channels
+    float wk[CW ? B + 1 : 1][CW ? D : 1];
     int slot;
 };
 
+// One CTA per (sequence, head, 64-column value slice); 256 threads.  Every
+// product is a register-tiled outer product over shared-memory operands:
+//   scores  S = Q_i K_i^T        4 x 4 tile per thread (K split over lanes for B < 64)
+//   output  P V_i + Q_i KV       (B/16) x 4 tile per thread
+//   state   K_s^T V_i            (D/16) x 4 tile per thread
+// The next chunk's global loads are issued before the state update, which
+// hides their latency.
 template <typename T, int D, int B, bool CW>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 1)
 prefill_simt_kernel(const T *__restrict__ q, const T *__restrict__ k,
                     const T *__restrict__ v, const float *__restrict__ decay,
                     const int32_t *__restrict__ cu, int nseq, int T_total, int H,
                     const float *initial_state, T *__restrict__ out, float *final_state,
                     int reverse_out, int min_len) {
+    using Smem = SimtSmem<D, B, CW>;
+    using R2 = typename Pair<T>::type;
+    constexpr int P = Smem::P, WP = Smem::WP;
+    constexpr int NVS = D / kDV;
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    auto &sm = *reinterpret_cast<SimtSmem<D, B, CW> *>(smem_raw);
+    auto &sm = *reinterpret_cast<Smem *>(smem_raw);
+    float (*pT)[P] = sm.kT;  // P^T[l][j] reuses the K_i^T rows once the scores are done
     const int tid = threadIdx.x;
 
-    const int h = blockIdx.x % H;
-    const int s = sequence_of_rank(cu, nseq, blockIdx.x / H, &sm.slot);
+    const int vs = blockIdx.x % NVS;
+    const int h = (blockIdx.x / NVS) % H;
+    const int s = sequence_of_rank(cu, nseq, blockIdx.x / (NVS * H), &sm.slot);
     // Clamp so that a malformed cu_seqlens can never index outside [0, T).
     int t0 = __ldg(cu + s), t1 = __ldg(cu + s + 1);
     t0 = min(max(t0, 0), T_total);
     t1 = min(max(t1, t0), T_total);
     const int L = t1 - t0;
     if (L < min_len) return;  // a mixed step's decode launch owns this sequence
-    const float lam = CW ? 1.f : __ldg(decay + h);
+    const int nv0 = vs * kDV;
+    const long row_stride = (long)H * D;
 
-    for (int e = tid; e <= B; e += kThreads) sm.pw[e] = powf(lam, (float)e);
     if constexpr (CW) {
         // channel-wise decay (K3 report reading notes): lambda per key
         // channel i, decay[h * D + i]; every factor below is lambda_i^e with
         // e >= 0 from this table
+        for (int e = tid; e < D * WP; e += kThreads) {
+            const int i = e / WP, c = e % WP;
+            sm.wz[i][c] = (c >= 4 && c <= B + 4)
+                              ? powf(__ldg(decay + (long)h * D + i), (float)(c - 4)) : 0.f;
+        }
         for (int e = tid; e < (B + 1) * D; e += kThreads)
-            sm.pwc[e / D][e % D] = powf(__ldg(decay + (long)h * D + e % D), (float)(e / D));
+            sm.wk[e / D][e % D] = powf(__ldg(decay + (long)h * D + e % D), (float)(e / D));
+    } else {
+        const float lam = __ldg(decay + h);
+        for (int e = tid; e < B + 4; e += kThreads) sm.pw[e] = powf(lam, (float)e);
     }
     // KV_{-1}: the sequence's cached state (prefix KV cache, §3.3.1), else 0.
-    // initial_state may be final_state itself: it is read here, before any
-    // write of this CTA's final state.
-    const float *s0 = initial_state ? initial_state + ((long)s * H + h) * D * D : nullptr;
-    for (int e = tid; e < D * D; e += kThreads) (&sm.kv[0][0])[e] = s0 ? s0[e] : 0.f;
+    // initial_state may be final_state itself: each CTA reads its own value
+    // slice here, before it writes that slice back.
+    {
+        const float *s0 = initial_state ? initial_state + ((long)s * H + h) * D * D : nullptr;
+        for (int e = tid; e < D * kDV / 4; e += kThreads) {
+            const int i = e / (kDV / 4), n = 4 * (e % (kDV / 4));
+            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (s0) x = *reinterpret_cast<const float4 *>(s0 + (long)i * D + nv0 + n);
+            *reinterpret_cast<float4 *>(&sm.kv[i][n]) = x;
+        }
+    }
+
+    // ---- staging: thread item = (channel pair, 4 consecutive tokens) ----
+    constexpr int NP = D / 2, NQ = B / 4;
+    constexpr int NQK = (NP * NQ + kThreads - 1) / kThreads;
+    constexpr int NV = (B * kDV / 2 + kThreads - 1) / kThreads;
+    R2 rq[NQK][4], rk[NQK][4], rv[NV];
+    auto load_chunk = [&](int c0) {
+        const int Lc = min(B, L - c0);
+#pragma unroll
+        for (int it = 0; it < NQK; ++it) {
+            const int e = tid + it * kThreads;
+            const int ip = e % NP, lq = e / NP;
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int l = 4 * lq + r;
+                rq[it][r] = rk[it][r] = zero_pair<R2>();
+                if (e < NP * NQ && l < Lc) {
+                    const long g = (long)(t0 + c0 + l) * row_stride + (long)h * D + 2 * ip;
+                    rq[it][r] = __ldg(reinterpret_cast<const R2 *>(q + g));
+                    rk[it][r] = __ldg(reinterpret_cast<const R2 *>(k + g));
+                }
+            }
+        }
+#pragma unroll
+        for (int iv = 0; iv < NV; ++iv) {
+            const int e = tid + iv * kThreads;
+            const int l = e / (kDV / 2), n = 2 * (e % (kDV / 2));
+            rv[iv] = zero_pair<R2>();
+            if (e < B * kDV / 2 && l < Lc)
+                rv[iv] = __ldg(reinterpret_cast<const R2 *>(
+                    v + (long)(t0 + c0 + l) * row_stride + (long)h * D + nv0 + n));
+        }
+    };
+    auto store_chunk = [&](int Lc) {
+#pragma unroll
+        for (int it = 0; it < NQK; ++it) {
+            const int e = tid + it * kThreads;
+            if (e >= NP * NQ) break;
+            const int i = 2 * (e % NP), l0 = 4 * (e / NP);
+            float2 fq[4], fk[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                fq[r] = to_f2(rq[it][r]);
+                fk[r] = to_f2(rk[it][r]);
+            }
+            store4(&sm.qT[i][l0], fq[0].x, fq[1].x, fq[2].x, fq[3].x);
+            store4(&sm.qT[i + 1][l0], fq[0].y, fq[1].y, fq[2].y, fq[3].y);
+            store4(&sm.kT[i][l0], fk[0].x, fk[1].x, fk[2].x, fk[3].x);
+            store4(&sm.kT[i + 1][l0], fk[0].y, fk[1].y, fk[2].y, fk[3].y);
+            // state operand: lambda^(B_i - 1 - l) K_i (per channel with CW)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int l = l0 + r;
+                float w0 = 0.f, w1 = 0.f;
+                if (l < Lc) {
+                    if constexpr (CW) {
+                        const float2 w = *reinterpret_cast<const float2 *>(&sm.wk[Lc - 1 - l][i]);
+                        w0 = w.x;
+                        w1 = w.y;
+                    } else {
+                        w0 = w1 = sm.pw[Lc - 1 - l];
+                    }
+                }
+                *reinterpret_cast<float2 *>(&sm.kS[l][i]) = make_float2(fk[r].x * w0, fk[r].y * w1);
+            }
+        }
+#pragma unroll
+        for (int iv = 0; iv < NV; ++iv) {
+            const int e = tid + iv * kThreads;
+            if (e >= B * kDV / 2) break;
+            const int l = e / (kDV / 2), n = 2 * (e % (kDV / 2));
+            *reinterpret_cast<float2 *>(&sm.vS[l][n]) = to_f2(rv[iv]);
+        }
+    };
+
+    // thread tiles
+    constexpr int NT = B / 4;                    // 4 x 4 score tiles per side
+    constexpr int KS = kThreads / (NT * NT);     // lanes sharing one score tile
+    constexpr int DK = D / KS;                   // channels per lane
+    static_assert(KS >= 1 && KS <= 32 && NT * NT * KS == kThreads, "score tiling");
+    const int ks = tid % KS, stile = tid / KS;
+    const int jt = stile / NT, lt = stile % NT;
+    const int sj0 = 4 * jt, sl0 = 4 * lt;
+    constexpr int TJ = B / 16;                   // output rows per thread
+    constexpr int TI = D / 16;                   // state rows per thread
+    const int n0 = 4 * (tid % 16);               // value columns of the output and state tiles
+    const int i0 = TI * (tid / 16);
+    // output rows: warp w owns row band w (w < 4) or 11 - w, so that the two
+    // warps of each scheduler (w, w + 4) together own bands k and 7 - k and
+    // carry the same share of the causal P V work
+    const int band = (tid / 32) < 4 ? (tid / 32) : 11 - (tid / 32);
+    const int jo = TJ * (2 * band + ((tid / 16) & 1));
+
+    if (L > 0) load_chunk(0);
     __syncthreads();
 
-    const long row_stride = (long)H * D;
     for (int c0 = 0; c0 < L; c0 += B) {
         const int Lc = min(B, L - c0);
-        // ---- stage the chunk (rows >= Lc are zero) ----
-        for (int e = tid; e < B * D; e += kThreads) {
-            const int l = e / D, i = e % D;
-            float qv = 0.f, kv_ = 0.f, vv = 0.f;
-            if (l < Lc) {
-                const long g = (long)(t0 + c0 + l) * row_stride + (long)h * D + i;
-                qv = to_f(q[g]);
-                kv_ = to_f(k[g]);
-                vv = to_f(v[g]);
-            }
-            sm.q[l][i] = qv;
-            sm.k[l][i] = kv_;
-            sm.v[l][i] = vv;
-        }
-        for (int l = tid; l < B; l += kThreads)
-            sm.gk[l] = (l < Lc) ? sm.pw[Lc - 1 - l] : 0.f;
+        store_chunk(Lc);
         __syncthreads();
 
         // ---- intra-block scores with the decay mask: P = (Q K^T) (.) M ----
-        for (int e = tid; e < B * B; e += kThreads) {
-            const int j = e / B, l = e % B;
-            float acc = 0.f;
-            if (l <= j && j < Lc) {
-                if constexpr (CW) {
-                    const float *w = sm.pwc[j - l];
-#pragma unroll 8
-                    for (int i = 0; i < D; ++i) acc = fmaf(sm.q[j][i] * w[i], sm.k[l][i], acc);
-                } else {
-#pragma unroll 8
-                    for (int i = 0; i < D; ++i) acc = fmaf(sm.q[j][i], sm.k[l][i], acc);
-                    acc *= sm.pw[j - l];
-                }
+        float acc[4][4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
+        if (lt <= jt && sj0 < Lc) {  // tiles above the diagonal or past the tail are 0
+            if constexpr (CW) {
+                // lambda_i^(j - l) = w8[4 + r - c], zero for l > j
+                struct St { float qa[2][4], kb[2][4], w8[2][8]; };
+                pipelined<St, 2>(
+                    DK,
+                    [&](St &st, int s2) {
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            const int i = ks + KS * (s2 + u);
+                            lds<4>(st.qa[u], &sm.qT[i][sj0]);
+                            lds<4>(st.kb[u], &sm.kT[i][sl0]);
+                            lds<8>(st.w8[u], &sm.wz[i][4 * (jt - lt)]);
+                        }
+                    },
+                    [&](const St &st) {
+#pragma unroll
+                        for (int u = 0; u < 2; ++u)
+#pragma unroll
+                            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                                for (int c = 0; c < 4; ++c)
+                                    acc[r][c] = fmaf(st.qa[u][r] * st.w8[u][4 + r - c],
+                                                     st.kb[u][c], acc[r][c]);
+                    });
+            } else {
+                struct St { float qa[2][4], kb[2][4]; };
+                pipelined<St, 2>(
+                    DK,
+                    [&](St &st, int s2) {
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            const int i = ks + KS * (s2 + u);
+                            lds<4>(st.qa[u], &sm.qT[i][sj0]);
+                            lds<4>(st.kb[u], &sm.kT[i][sl0]);
+                        }
+                    },
+                    [&](const St &st) {
+#pragma unroll
+                        for (int u = 0; u < 2; ++u)
+#pragma unroll
+                            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                                for (int c = 0; c < 4; ++c)
+                                    acc[r][c] = fmaf(st.qa[u][r], st.kb[u][c], acc[r][c]);
+                    });
             }
-            sm.p[j][l] = acc;
+        }
+#pragma unroll
+        for (int m = 1; m < KS; m <<= 1)
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    acc[r][c] += __shfl_xor_sync(0xffffffffu, acc[r][c], m);
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int j = sj0 + r, l = sl0 + c;
+                if (l > j) acc[r][c] = 0.f;
+                else if constexpr (!CW) acc[r][c] *= sm.pw[j - l];
+            }
+        __syncthreads();  // every read of K_i^T is done
+        if (ks == 0) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                store4(&pT[sl0 + c][sj0], acc[0][c], acc[1][c], acc[2][c], acc[3][c]);
         }
         __syncthreads();
 
         // ---- output: P V_i + lambda^(j+1) Q_i KV_{i-1} ----
-        for (int e = tid; e < B * D; e += kThreads) {
-            const int j = e / D, n = e % D;
-            if (j >= Lc) continue;
-            float intra = 0.f;
-            for (int l = 0; l <= j; ++l) intra = fmaf(sm.p[j][l], sm.v[l][n], intra);
-            float inter = 0.f;
-            float o;
-            if constexpr (CW) {
-                const float *w = sm.pwc[j + 1];
-#pragma unroll 8
-                for (int i = 0; i < D; ++i) inter = fmaf(sm.q[j][i] * w[i], sm.kv[i][n], inter);
-                o = intra + inter;
-            } else {
-#pragma unroll 8
-                for (int i = 0; i < D; ++i) inter = fmaf(sm.q[j][i], sm.kv[i][n], inter);
-                o = fmaf(sm.pw[j + 1], inter, intra);
+        {
+            float oi[TJ][4], oe[TJ][4];
+#pragma unroll
+            for (int r = 0; r < TJ; ++r)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) oi[r][c] = oe[r][c] = 0.f;
+            // P is zero above the diagonal (and V past the tail): the warp
+            // stops after its last row, rounded up to whole pipeline stages
+            const int lmax = (min(Lc, TJ * (2 * band + 2)) + 3) & ~3;
+            {
+                struct St { float pa[2][TJ], vb[2][4]; };
+                pipelined<St, 2>(
+                    lmax,
+                    [&](St &st, int l) {
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            lds<TJ>(st.pa[u], &pT[l + u][jo]);
+                            lds<4>(st.vb[u], &sm.vS[l + u][n0]);
+                        }
+                    },
+                    [&](const St &st) {
+#pragma unroll
+                        for (int u = 0; u < 2; ++u)
+#pragma unroll
+                            for (int r = 0; r < TJ; ++r)
+#pragma unroll
+                                for (int c = 0; c < 4; ++c)
+                                    oi[r][c] = fmaf(st.pa[u][r], st.vb[u][c], oi[r][c]);
+                    });
             }
-            // with reverse_out the sequence is written back to front
-            const long row = reverse_out ? (long)(t1 - 1 - c0 - j) : (long)(t0 + c0 + j);
-            out[row * row_stride + (long)h * D + n] = from_f<T>(o);
-        }
-        __syncthreads();  // everyone has read KV_{i-1}
-
-        // ---- state: KV_i = lambda^{Lc} KV_{i-1} + (gk (.) K_i)^T V_i ----
-        const float dec = sm.pw[Lc];
-        for (int e = tid; e < D * D; e += kThreads) {
-            const int i = e / D, n = e % D;
-            float acc = 0.f;
             if constexpr (CW) {
-                for (int l = 0; l < Lc; ++l)
-                    acc = fmaf(sm.pwc[Lc - 1 - l][i] * sm.k[l][i], sm.v[l][n], acc);
-                sm.kv[i][n] = fmaf(sm.pwc[Lc][i], sm.kv[i][n], acc);
+                // q_j[i] lambda_i^(j+1) = (q_j[i] lambda_i^j) lambda_i
+                struct St { float qa[2][TJ], wq[2][TJ], kb[2][4], l1[2]; };
+                pipelined<St, 2>(
+                    D,
+                    [&](St &st, int i) {
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            lds<TJ>(st.qa[u], &sm.qT[i + u][jo]);
+                            lds<TJ>(st.wq[u], &sm.wz[i + u][4 + jo]);
+                            lds<4>(st.kb[u], &sm.kv[i + u][n0]);
+                            st.l1[u] = sm.wz[i + u][5];
+                        }
+                    },
+                    [&](const St &st) {
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            float qw[TJ], kl[4];
+#pragma unroll
+                            for (int r = 0; r < TJ; ++r) qw[r] = st.qa[u][r] * st.wq[u][r];
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) kl[c] = st.kb[u][c] * st.l1[u];
+#pragma unroll
+                            for (int r = 0; r < TJ; ++r)
+#pragma unroll
+                                for (int c = 0; c < 4; ++c)
+                                    oe[r][c] = fmaf(qw[r], kl[c], oe[r][c]);
+                        }
+                    });
             } else {
-                for (int l = 0; l < Lc; ++l) acc = fmaf(sm.gk[l] * sm.k[l][i], sm.v[l][n], acc);
-                sm.kv[i][n] = fmaf(dec, sm.kv[i][n], acc);
+                struct St { float qa[2][TJ], kb[2][4]; };
+                pipelined<St, 2>(
+                    D,
+                    [&](St &st, int i) {
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            lds<TJ>(st.qa[u], &sm.qT[i + u][jo]);
+                            lds<4>(st.kb[u], &sm.kv[i + u][n0]);
+                        }
+                    },
+                    [&](const St &st) {
+#pragma unroll
+                        for (int u = 0; u < 2; ++u)
+#pragma unroll
+                            for (int r = 0; r < TJ; ++r)
+#pragma unroll
+                                for (int c = 0; c < 4; ++c)
+                                    oe[r][c] = fmaf(st.qa[u][r], st.kb[u][c], oe[r][c]);
+                    });
+            }
+#pragma unroll
+            for (int r = 0; r < TJ; ++r) {
+                const int j = jo + r;
+                if (j >= Lc) break;
+                float o[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    o[c] = CW ? oi[r][c] + oe[r][c] : fmaf(sm.pw[j + 1], oe[r][c], oi[r][c]);
+                // with reverse_out the sequence is written back to front
+                const long row = reverse_out ? (long)(t1 - 1 - c0 - j) : (long)(t0 + c0 + j);
+                store4(out + row * row_stride + (long)h * D + nv0 + n0, o[0], o[1], o[2], o[3]);
+            }
+        }
+        __syncthreads();  // everyone has read KV_{i-1} and P
+
+        if (c0 + B < L) load_chunk(c0 + B);  // in flight during the state update
+
+        // ---- state: KV_i = lambda^{B_i} KV_{i-1} + (Lambda_K K_i)^T V_i ----
+        {
+            float a[TI][4];
+#pragma unroll
+            for (int r = 0; r < TI; ++r)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) a[r][c] = 0.f;
+            {
+                // rows past the tail of K_s and V_i are zero: whole stages
+                struct St { float ka[2][TI], vb[2][4]; };
+                pipelined<St, 2>(
+                    (Lc + 3) & ~3,
+                    [&](St &st, int l) {
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            lds<TI>(st.ka[u], &sm.kS[l + u][i0]);
+                            lds<4>(st.vb[u], &sm.vS[l + u][n0]);
+                        }
+                    },
+                    [&](const St &st) {
+#pragma unroll
+                        for (int u = 0; u < 2; ++u)
+#pragma unroll
+                            for (int r = 0; r < TI; ++r)
+#pragma unroll
+                                for (int c = 0; c < 4; ++c)
+                                    a[r][c] = fmaf(st.ka[u][r], st.vb[u][c], a[r][c]);
+                    });
+            }
+#pragma unroll
+            for (int r = 0; r < TI; ++r) {
+                const int i = i0 + r;
+                const float dec = CW ? sm.wz[i][4 + Lc] : sm.pw[Lc];
+                float4 *p = reinterpret_cast<float4 *>(&sm.kv[i][n0]);
+                const float4 old = *p;
+                *p = make_float4(fmaf(dec, old.x, a[r][0]), fmaf(dec, old.y, a[r][1]),
+                                 fmaf(dec, old.z, a[r][2]), fmaf(dec, old.w, a[r][3]));
             }
         }
         __syncthreads();
@@ -164,7 +481,11 @@ prefill_simt_kernel(const T *__restrict__ q, const T *__restrict__ k,
 
     if (final_state) {
         float *dst = final_state + ((long)s * H + h) * D * D;
-        for (int e = tid; e < D * D; e += kThreads) dst[e] = (&sm.kv[0][0])[e];
+        for (int e = tid; e < D * kDV / 4; e += kThreads) {
+            const int i = e / (kDV / 4), n = 4 * (e % (kDV / 4));
+            *reinterpret_cast<float4 *>(dst + (long)i * D + nv0 + n) =
+                *reinterpret_cast<const float4 *>(&sm.kv[i][n]);
+        }
     }
 }
 
@@ -175,7 +496,7 @@ cudaError_t launch(const PrefillArgs &a) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    const long grid = (long)(a.rank_limit > 0 ? a.rank_limit : a.nseq) * a.num_heads;
+    const long grid = (long)(a.rank_limit > 0 ? a.rank_limit : a.nseq) * a.num_heads * (D / kDV);
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffffL) return cudaErrorInvalidConfiguration;
     kern<<<(unsigned)grid, kThreads, smem, a.stream>>>(

@@ -34,6 +34,7 @@ def channel_decays(H, d, seed):
 
 @pytest.mark.parametrize("dtype, d, chunk, tol", [
     (torch.float32, 64, 16, TOL_FP32), (torch.float32, 128, 64, TOL_FP32),
+    (torch.float32, 128, 32, TOL_FP32), (torch.float32, 128, 16, TOL_FP32),
     (torch.bfloat16, 128, 64, TOL_BF16), (torch.bfloat16, 64, 32, TOL_BF16)])
 def test_channel_decay_prefill(dtype, d, chunk, tol):
     H = 3
@@ -47,6 +48,25 @@ def test_channel_decay_prefill(dtype, d, chunk, tol):
                                       initial_state=s0.cpu())
     assert_close(out, ref, tol, f"channel decay {dtype} d={d} B={chunk} out")
     assert_close(st, ref_st, tol, f"channel decay {dtype} d={d} B={chunk} state")
+
+
+@pytest.mark.parametrize("chunk", [16, 64])
+def test_channel_decay_extreme_decays(chunk):
+    """Channels with lambda = 1 (no decay) next to lambda = 1e-30 (every power
+    above the first underflows in fp32): the per-channel tables hold only
+    non-negative exponents, so nothing overflows and no NaN appears."""
+    H, d = 2, 128
+    inp = wl.prefill_inputs([200, 3, 64], H, d, dtype=torch.float32, seed=55, device="cuda")
+    lam = channel_decays(H, d, 56)
+    lam[:, 0::3] = 1.0
+    lam[:, 1::3] = 1e-30
+    out, st = la.prefill_channel_decay(inp.q, inp.k, inp.v, lam.cuda(), inp.cu_seqlens,
+                                       chunk=chunk)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out).all() and torch.isfinite(st).all()
+    ref, ref_st = oracle.recurrent_cw(inp.q, inp.k, inp.v, lam, inp.cu_seqlens.cpu())
+    assert_close(out, ref, TOL_FP32, f"extreme channel decays B={chunk} out")
+    assert_close(st, ref_st, TOL_FP32, f"extreme channel decays B={chunk} state")
 
 
 def test_channel_decay_uniform_equals_scalar_kernel():

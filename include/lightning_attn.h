@@ -186,10 +186,12 @@ la_status lightning_attn_decode(const void *q, const void *k, const void *v,
  *     dv_u = sum_{t >= u} lambda^(t-u) (q_t . k_u) dout_t
  *
  * per sequence and head.  dq is the forward form applied to (dout, v, k);
- * dk and dv are the forward form in reversed time, so the call runs the
- * prefill kernels three times (same dtype / head_dim / chunk rules and
- * precision as lightning_attn_prefill) plus four time-reversal copies through
- * `workspace`.
+ * dk and dv are anti-causal forms (sums over t >= u).  On the tensor-core
+ * path (bf16, head_dim 128, chunk 0/128) the call makes three launches of
+ * the prefill kernel, one causal and two anti-causal, and does not touch
+ * `workspace`; on the CUDA-core path it runs the forward form in reversed
+ * time, with four time-reversal copies through `workspace`.  Same dtype /
+ * head_dim / chunk rules and precision as lightning_attn_prefill.
  *
  * q, k, v, d_out          [total_tokens, num_heads, head_dim], dtype `dtype`
  * d_q, d_k, d_v           outputs, same shape and dtype; distinct arrays,

@@ -42,6 +42,8 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 la_status run_prefill(const la::PrefillArgs &a, la_dtype dtype) {
     const bool tc = dtype == LA_DTYPE_BF16 && a.head_dim == 128 && (a.chunk == 0 || a.chunk == 128);
     if (tc) return from_cuda(la::prefill_tc_bf16(a), "prefill (tcgen05)");
+    if (a.anti_causal)
+        return fail(LA_ERR_UNSUPPORTED, "the anti-causal form runs on the tensor-core path only");
     if (a.chunk == 128 || a.chunk == 256)
         return fail(LA_ERR_UNSUPPORTED,
                     "chunk %d needs the tensor-core path (bf16, head_dim 128)", a.chunk);
@@ -305,6 +307,13 @@ la_status lightning_attn_backward(const void *q, const void *k, const void *v,
                            head_dim, chunk, o, nullptr, st, nullptr, reverse_out};
         return run_prefill(pa, dtype);
     };
+    // o_t = sum_{u >= t} lambda^(u-t) (a_t . b_u) c_u, rows in place
+    auto anti = [&](const void *a, const void *b, const void *c, void *o) {
+        la::PrefillArgs pa{a, b, c, decay, cu_seqlens, num_seqs, total_tokens, num_heads,
+                           head_dim, chunk, o, nullptr, st, nullptr};
+        pa.anti_causal = true;
+        return run_prefill(pa, dtype);
+    };
     auto rev = [&](const void *in, void *out) {
         return from_cuda(la::reverse_sequences(in, out, cu_seqlens, num_seqs, total_tokens, row, st),
                          "backward (time reversal)");
@@ -313,6 +322,14 @@ la_status lightning_attn_backward(const void *q, const void *k, const void *v,
     // dq_t = sum_{u<=t} lambda^(t-u) (dout_t . v_u) k_u: the forward form
     // with (q, k, v) -> (dout, v, k)
     if ((r = fwd(d_out, v, k, d_q, false)) != LA_OK) return r;
+    if (dtype == LA_DTYPE_BF16 && head_dim == 128 && (chunk == 0 || chunk == 128)) {
+        // tensor-core path: dv_u = sum_{t>=u} lambda^(t-u) (q_t . k_u) dout_t and
+        // dk_u = sum_{t>=u} lambda^(t-u) (dout_t . v_u) q_t are anti-causal
+        // forms, computed in place (the workspace is not touched)
+        if ((r = anti(k, q, d_out, d_v)) != LA_OK) return r;
+        return anti(v, d_out, q, d_k);
+    }
+    // CUDA-core path: the anti-causal sums as the forward form in reversed time
     // dv_u = sum_{t>=u} lambda^(t-u) (q_t . k_u) dout_t: the forward form in
     // reversed time with (q, k, v) -> (k, q, dout); the launch writes its
     // output rows back in forward time order

@@ -22,6 +22,11 @@ struct PrefillArgs {
     // are in order of length, longest first, for nseq <= kMaxSortedSeqs)
     int rank_limit = 0;
     bool channel_decay = false; // decay is [H, D]: one lambda per key channel
+    // Anti-causal sum o_t = sum_{u >= t} lambda^(u-t) (q_t . k_u) v_u (the
+    // backward pass's reversed-time products), output rows in place; the
+    // final state is then sum_u lambda^(u - t0) k_u^T v_u.  Tensor-core
+    // kernel only, zero initial state.
+    bool anti_causal = false;
 };
 
 struct DecodeArgs {

@@ -83,10 +83,16 @@ constexpr int BC = 128;      // chunk (block) size
 constexpr int kThreads = 512;  // 16 warps: 4 per SM sub-partition, 128 registers
 constexpr int kStateWarp0 = 4;
 constexpr int kVWarp0 = 8;
-constexpr int kMmaWarpA = 12;  // S and P V
-constexpr int kMmaWarpB = 13;  // dKV and Q KV
-constexpr int kMaskHelp2 = 14; // helps mask warp 2 (TMEM lanes 64-95)
-constexpr int kMaskHelp3 = 15; // helps mask warp 3 (TMEM lanes 96-127)
+// Warps 12-15: two MMA issuers and two mask helpers.  A helper must sit on
+// the TMEM lane quadrant it helps (a warp reads lanes 32 (warp % 4) ..), and
+// the quadrants with the most mask blocks are 2 and 3 in the causal
+// direction, 1 and 0 in the anti-causal one; the issuers take the other two.
+template <bool kAnti> struct Roles {
+    static constexpr int mma_a = kAnti ? 14 : 12;  // S and P V
+    static constexpr int mma_b = kAnti ? 15 : 13;  // dKV and Q KV
+    static constexpr int help2 = kAnti ? 13 : 14;  // second warp of the 3-block quadrant
+    static constexpr int help3 = kAnti ? 12 : 15;  // second warp of the 4-block quadrant
+};
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
 
 // Shared memory (offsets from a 1024-byte aligned base).  Operand tiles are
@@ -176,7 +182,16 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     return __all_sync(0xffffffffu, ok);
 }
 
-template <bool kRevOut>
+// kAnti = false: o_t = sum_{u <= t} lambda^(t-u) (q_t . k_u) v_u (the method);
+// kAnti = true: the anti-causal sum over u >= t with lambda^(u-t), for the
+// reversed-time products of the backward pass.  Chunks keep their places
+// (chunk c covers tokens [t0 + c B, t0 + c B + B)) and are walked last to
+// first; inside a chunk the mask is the upper triangle lambda^(l-j), the
+// carried state after chunk c is G_c = sum_{u >= start_c} lambda^(u-start_c)
+// k_u^T v_u (G_c = lambda^{B_c} G_{c+1} + (Lambda_K K_c)^T V_c with
+// Lambda_K = diag(lambda^l)), and row j of a chunk that has a successor gains
+// lambda^(B - j) q_j G_{c+1}.  Every exponent is again >= 0.
+template <bool kAnti>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -200,6 +215,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     const int L = t1 - t0;
     if (L < min_len) return;  // a mixed step's decode launch owns this sequence
     const int nch = (L + BC - 1) / BC;
+    // chunk processed at step i, and the length of chunk c (only the last
+    // chunk of a sequence may be short)
+    auto chunk_of = [&](int i) { return kAnti ? nch - 1 - i : i; };
+    auto len_of = [&](int c) { return min(BC, L - c * BC); };
+    using R = Roles<kAnti>;
     const float lam = __ldg(decay + h);
     // A sequence may continue from a cached state S0 (prefix KV cache,
     // §3.3.1): KV_{-1} = S0 instead of 0.  initial_state may be final_state
@@ -263,7 +283,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
 
     if (!tmem_ok) {
         // leave TMEM alone; the error word is raised below
-    } else if (warp == kMmaWarpA) {
+    } else if (warp == R::mma_a) {
         // ================= MMA stream A: S and P V =================
         // Per chunk i: S_{i+1}, then P_i V_i, so that the mask warps turn
         // S_{i+1} into P_{i+1} while the tensor core runs P_i V_i and stream
@@ -276,7 +296,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             if (!warp_wait(bar(cs.empty_v[st]), ((c >> 1) & 1) ^ 1, abort_flag)) return false;
             if (elect_one()) {
                 mbar_arrive_expect_tx(bar(cs.full_v[st]), kHalf);
-                tma_load_2d(vslot(st), &tmV, bar(cs.full_v[st]), h * D + vs * DV, t0 + c * BC);
+                tma_load_2d(vslot(st), &tmV, bar(cs.full_v[st]), h * D + vs * DV,
+                            t0 + chunk_of(c) * BC);
             }
             __syncwarp();
             ++nv;
@@ -331,7 +352,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         warp_wait(bar(cs.done_a), 0, &no_abort);
         for (int c = max(0, nv - 2); c < nv; ++c)
             warp_wait(bar(cs.full_v[c & 1]), (c >> 1) & 1, &no_abort);
-    } else if (warp == kMmaWarpB) {
+    } else if (warp == R::mma_b) {
         // ================= MMA stream B: dKV and Q KV =================
         const uint32_t vha = sb + kOffVhat, kvb = sb + kOffKVb;
         for (int i = 0; i < nch; ++i) {
@@ -369,7 +390,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         __syncwarp();
         int no_abort = 0;
         warp_wait(bar(cs.done_b), 0, &no_abort);
-    } else if (warp < kStateWarp0 || warp == kMaskHelp2 || warp == kMaskHelp3) {
+    } else if (warp < kStateWarp0 || warp == R::help2 || warp == R::help3) {
         // ================= mask warps: S -> P =================
         // Row j of the chunk is TMEM lane j; the warps of lane quadrant q
         // (rows 32q .. 32q + 31) hold that quadrant's 32-column S blocks
@@ -389,40 +410,65 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         // P block cb lands in TMEM columns [16 cb, 16 cb + 16) of the S
         // buffer, written after every S block of the quadrant has been read
         // (the exchange orders the two warps of a pair).
-        const int q = warp & 3;
+        // Anti-causal: quadrant q holds the blocks cb >= q and
+        // p_jl = S_jl lambda^(l-j) for l >= j; it is the causal quadrant
+        // qm = 3 - q mirrored (block cb <-> 3 - cb), with
+        //     f = lambda^(c - lane) (masked) on the diagonal block,
+        //     f = lambda^(32 (cb - q - 1) + c) above it, row constant lambda^(32 - lane).
+        const int q = warp & 3;                 // TMEM lane quadrant
+        const int qm = kAnti ? 3 - q : q;       // the same quadrant in causal terms
         const bool owner = warp < kStateWarp0;
         const int j = q * 32 + lane;
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-        // Blocks: register set A holds a block below the diagonal (none for
-        // the quadrant-0 owner); set B holds the owner's diagonal block, or
-        // the quadrant-3 helper's second block.
-        const bool has_a = !(owner && q == 0);
-        const int cba = owner ? q - 1 : 0;
-        const bool has_b = owner || q == 3;
-        const int cbb = owner ? q : 1;
-        const int pr = q - 2;  // pair index of a split quadrant
+        // Blocks (causal terms): register set A holds a block below the
+        // diagonal (none for the quadrant-0 owner); set B holds the owner's
+        // diagonal block, or the quadrant-3 helper's second block.
+        const bool has_a = !(owner && qm == 0);
+        const int cba = owner ? qm - 1 : 0;
+        const bool has_b = owner || qm == 3;
+        const int cbb = owner ? qm : 1;
+        const int pba = kAnti ? 3 - cba : cba;  // their blocks in the S buffer
+        const int pbb = kAnti ? 3 - cbb : cbb;
+        const int pr = qm - 2;  // pair index of a split quadrant
         const uint32_t pwt_s = smem_u32(&cs.pwt[32]);  // masked table: lambda^d at pwt_s + 4 d
-        const float rowlam = pw(lane + 1);
-        // p' = S lambda^(32 (q - cb) - 1 - c) for a block below the diagonal;
-        // returns max |p'| over the valid columns.
-        auto decay_below = [&](float(&sv)[32], int cb, int Lc) -> float {
-            const uint32_t tab = pw_s + 4u * (uint32_t)(32 * (q - cb) - 32);
+        const float rowlam = kAnti ? pw(32 - lane) : pw(lane + 1);
+        // p' = S f for a block dd >= 1 blocks off the diagonal (physical
+        // block pb); returns max |p'| over the valid columns.
+        auto decay_below = [&](float(&sv)[32], int dd, int pb, int Lc) -> float {
             float m = 0.f;
+            if constexpr (kAnti) {
+                // lambda^(32 (dd - 1) + c), c = 4g .. 4g + 3: four consecutive entries
+                const uint32_t tab = pw_s + 4u * (uint32_t)(32 * (dd - 1));
 #pragma unroll
-            for (int g = 0; g < 8; ++g) {
-                // lambda^(32 (q - cb) - 1 - c), c = 4g .. 4g + 3: the four
-                // table entries from 32 (q - cb) - 4 - 4g, reversed
-                const uint4 f4 = ld_shared_v4(tab + 16u * (uint32_t)(7 - g));
-                const float2 x0 = f2_mul(make_float2(sv[4 * g], sv[4 * g + 1]),
-                                         make_float2(__uint_as_float(f4.w), __uint_as_float(f4.z)));
-                const float2 x1 = f2_mul(make_float2(sv[4 * g + 2], sv[4 * g + 3]),
-                                         make_float2(__uint_as_float(f4.y), __uint_as_float(f4.x)));
-                sv[4 * g] = x0.x;
-                sv[4 * g + 1] = x0.y;
-                sv[4 * g + 2] = x1.x;
-                sv[4 * g + 3] = x1.y;
+                for (int g = 0; g < 8; ++g) {
+                    const uint4 f4 = ld_shared_v4(tab + 16u * (uint32_t)g);
+                    const float2 x0 = f2_mul(make_float2(sv[4 * g], sv[4 * g + 1]),
+                                             make_float2(__uint_as_float(f4.x), __uint_as_float(f4.y)));
+                    const float2 x1 = f2_mul(make_float2(sv[4 * g + 2], sv[4 * g + 3]),
+                                             make_float2(__uint_as_float(f4.z), __uint_as_float(f4.w)));
+                    sv[4 * g] = x0.x;
+                    sv[4 * g + 1] = x0.y;
+                    sv[4 * g + 2] = x1.x;
+                    sv[4 * g + 3] = x1.y;
+                }
+            } else {
+                const uint32_t tab = pw_s + 4u * (uint32_t)(32 * dd - 32);
+#pragma unroll
+                for (int g = 0; g < 8; ++g) {
+                    // lambda^(32 dd - 1 - c), c = 4g .. 4g + 3: the four
+                    // table entries from 32 dd - 4 - 4g, reversed
+                    const uint4 f4 = ld_shared_v4(tab + 16u * (uint32_t)(7 - g));
+                    const float2 x0 = f2_mul(make_float2(sv[4 * g], sv[4 * g + 1]),
+                                             make_float2(__uint_as_float(f4.w), __uint_as_float(f4.z)));
+                    const float2 x1 = f2_mul(make_float2(sv[4 * g + 2], sv[4 * g + 3]),
+                                             make_float2(__uint_as_float(f4.y), __uint_as_float(f4.x)));
+                    sv[4 * g] = x0.x;
+                    sv[4 * g + 1] = x0.y;
+                    sv[4 * g + 2] = x1.x;
+                    sv[4 * g + 3] = x1.y;
+                }
             }
-            const int lim = Lc - 1 - cb * 32;  // last valid column
+            const int lim = Lc - 1 - pb * 32;  // last valid column
             if (lim < 31) {  // ragged last chunk
 #pragma unroll
                 for (int c = 0; c < 32; ++c) sv[c] = c <= lim ? sv[c] : 0.f;
@@ -431,19 +477,32 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             for (int c = 0; c < 32; ++c) m = fmaxf(m, fabsf(sv[c]));
             return m;
         };
-        // p' = S lambda^(lane - c) for c <= lane (0 above the diagonal).
-        auto decay_diag = [&](float(&sv)[32], int cb, int Lc) -> float {
-            const uint32_t tab = pwt_s + 4u * (uint32_t)lane;
+        // p' = S lambda^(lane - c) for c <= lane, 0 above the diagonal
+        // (anti-causal: lambda^(c - lane) for c >= lane, 0 below).
+        auto decay_diag = [&](float(&sv)[32], int pb, int Lc) -> float {
             float m = 0.f;
+            if constexpr (kAnti) {
+                const uint32_t tab = pwt_s - 4u * (uint32_t)lane;
 #pragma unroll
-            for (int c = 0; c < 32; c += 2) {
-                const float2 x = f2_mul(make_float2(sv[c], sv[c + 1]),
-                                        make_float2(ld_shared_f32(tab - 4u * c),
-                                                    ld_shared_f32(tab - 4u * (c + 1))));
-                sv[c] = x.x;
-                sv[c + 1] = x.y;
+                for (int c = 0; c < 32; c += 2) {
+                    const float2 x = f2_mul(make_float2(sv[c], sv[c + 1]),
+                                            make_float2(ld_shared_f32(tab + 4u * c),
+                                                        ld_shared_f32(tab + 4u * (c + 1))));
+                    sv[c] = x.x;
+                    sv[c + 1] = x.y;
+                }
+            } else {
+                const uint32_t tab = pwt_s + 4u * (uint32_t)lane;
+#pragma unroll
+                for (int c = 0; c < 32; c += 2) {
+                    const float2 x = f2_mul(make_float2(sv[c], sv[c + 1]),
+                                            make_float2(ld_shared_f32(tab - 4u * c),
+                                                        ld_shared_f32(tab - 4u * (c + 1))));
+                    sv[c] = x.x;
+                    sv[c + 1] = x.y;
+                }
             }
-            const int lim = Lc - 1 - cb * 32;
+            const int lim = Lc - 1 - pb * 32;
             if (lim < 31) {
 #pragma unroll
                 for (int c = 0; c < 32; ++c) sv[c] = c <= lim ? sv[c] : 0.f;
@@ -469,21 +528,21 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         for (int i = 0; i < nch; ++i) {
             const int st = i & 1;
             const uint32_t sph = (i >> 1) & 1;
-            const int Lc = min(BC, L - i * BC);
+            const int Lc = len_of(chunk_of(i));
             const uint32_t scol = tmem + lane_off + st * 128;
             if (!warp_wait(bar(cs.s_full[st]), sph, abort_flag)) break;
             tc_fence_after();
             float sa[32], sb2[32];
-            if (has_a) tmem_ld32(scol + cba * 32, sa);
-            if (has_b) tmem_ld32(scol + cbb * 32, sb2);
+            if (has_a) tmem_ld32(scol + pba * 32, sa);
+            if (has_b) tmem_ld32(scol + pbb * 32, sb2);
             tmem_wait_ld();
             // pass 1
-            float mb = 0.f, md = 0.f;  // max |p'| below the diagonal, on it
-            if (has_a) mb = decay_below(sa, cba, Lc);
-            if (owner) md = decay_diag(sb2, cbb, Lc);
-            else if (has_b) mb = fmaxf(mb, decay_below(sb2, cbb, Lc));
+            float mb = 0.f, md = 0.f;  // max |p'| off the diagonal, on it
+            if (has_a) mb = decay_below(sa, qm - cba, pba, Lc);
+            if (owner) md = decay_diag(sb2, pbb, Lc);
+            else if (has_b) mb = fmaxf(mb, decay_below(sb2, qm - cbb, pbb, Lc));
             float bound = fmaxf(mb * rowlam, md);
-            if (q >= 2) {  // exchange with the other warp of the quadrant
+            if (qm >= 2) {  // exchange with the other warp of the quadrant
                 // Only the exponent of the bound matters: pass its top 16 bits
                 // (a nonzero bound stays nonzero), so both warps pick the same e.
                 const uint32_t ub = __float_as_uint(bound);
@@ -498,11 +557,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             const int e = fp16_scale_exp(bound, 11);
             const float inv = exp2i(-e);
             // pass 2
-            if (has_a) store_block(sa, cba, rowlam * inv, scol);
-            if (has_b) store_block(sb2, cbb, owner ? inv : rowlam * inv, scol);
-            if (owner) {
+            if (has_a) store_block(sa, pba, rowlam * inv, scol);
+            if (has_b) store_block(sb2, pbb, owner ? inv : rowlam * inv, scol);
+            if (owner) {  // the blocks on the masked side of the diagonal are zero
 #pragma unroll 1
-                for (int cb = q + 1; cb < 4; ++cb) tmem_st16(scol + cb * 16, zero);
+                for (int cb = qm + 1; cb < 4; ++cb) tmem_st16(scol + (kAnti ? 3 - cb : cb) * 16, zero);
                 cs.rowe[st][j] = (signed char)e;
             }
             tmem_wait_st();
@@ -538,8 +597,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             if (!mbar_wait(bar(cs.empty_q[st]), ((c >> 1) & 1) ^ 1, abort_flag, kTimeoutNs))
                 return false;
             mbar_arrive_expect_tx(bar(cs.full_q[st]), 2 * kHalf);
-            tma_load_2d(qslot(st), &tmQ, bar(cs.full_q[st]), h * D, t0 + c * BC);
-            tma_load_2d(qslot(st) + kHalf, &tmQ, bar(cs.full_q[st]), h * D + 64, t0 + c * BC);
+            const int row = t0 + chunk_of(c) * BC;
+            tma_load_2d(qslot(st), &tmQ, bar(cs.full_q[st]), h * D, row);
+            tma_load_2d(qslot(st) + kHalf, &tmQ, bar(cs.full_q[st]), h * D + 64, row);
             ++nq;
             return true;
         };
@@ -548,8 +608,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             if (!mbar_wait(bar(cs.empty_k[st]), ((c >> 1) & 1) ^ 1, abort_flag, kTimeoutNs))
                 return false;
             mbar_arrive_expect_tx(bar(cs.full_k[st]), 2 * kHalf);
-            tma_load_2d(kslot(st), &tmK, bar(cs.full_k[st]), h * D, t0 + c * BC);
-            tma_load_2d(kslot(st) + kHalf, &tmK, bar(cs.full_k[st]), h * D + 64, t0 + c * BC);
+            const int row = t0 + chunk_of(c) * BC;
+            tma_load_2d(kslot(st), &tmK, bar(cs.full_k[st]), h * D, row);
+            tma_load_2d(kslot(st) + kHalf, &tmK, bar(cs.full_k[st]), h * D + 64, row);
             ++nk;
             return true;
         };
@@ -610,7 +671,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
                               ? reinterpret_cast<float4 *>(
                                     final_state + (((long)s * H + h) * D + r) * D + vs * DV)
                               : nullptr;
-            const float dh = nch > 0 ? 0.5f * pw(min(BC, L)) : 0.f;
+            const float dh = nch > 0 ? 0.5f * pw(len_of(chunk_of(0))) : 0.f;
             const float2 d2 = make_float2(dh, dh);
 #pragma unroll 1
             for (int g = 0; g < 4; ++g) {
@@ -677,7 +738,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         for (int i = 0; i < nch; ++i) {
             const int st = i & 1;
             const uint32_t sph = (i >> 1) & 1, ph = i & 1;
-            const int Lc = min(BC, L - i * BC);
+            const int Lc = len_of(chunk_of(i));
             const bool last = i + 1 == nch;
             // ---- fold ----
             if (!warp_wait(bar(cs.dkv_full), ph, abort_flag)) break;
@@ -700,7 +761,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
                 }
             }
             if (!last) {
-                write_back(kv, pw(min(BC, L - (i + 1) * BC)));
+                write_back(kv, pw(len_of(chunk_of(i + 1))));
             } else if (final_state) {
                 float4 *dst = reinterpret_cast<float4 *>(final_state + (((long)s * H + h) * D + r) * D + vs * DV);
 #pragma unroll
@@ -743,11 +804,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             tc_fence_after();
             const float s1 = exp2i((int)*reinterpret_cast<volatile signed char *>(&cs.rowe[st][r])) *
                              ld_shared_f32(vscale_s + 4u * (uint32_t)(i & 3));
-            const float qf = pw(r + 1);
+            // lambda^(r+1) Q KV_{i-1}; anti-causal: lambda^(B-r) Q G_{c+1}
+            // (G is zero before the first step, when chunk c may be short)
+            const float qf = kAnti ? pw(BC - r) : pw(r + 1);
             const float2 s12 = make_float2(s1, s1), qf2 = make_float2(qf, qf);
-            // token row of o_r; with kRevOut the sequence is written back to
-            // front (the backward pass's reversed-time launches)
-            const long orow_t = kRevOut ? (long)(t1 - 1 - i * BC - r) : (long)(t0 + i * BC + r);
+            const long orow_t = (long)(t0 + chunk_of(i) * BC + r);
             uint4 *orow = reinterpret_cast<uint4 *>(out + (orow_t * H + h) * D +
                                                     vs * DV);
 #pragma unroll
@@ -803,7 +864,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         for (int i = 0; i < nch; ++i) {
             const int st = i & 1;
             if (!warp_wait(bar(cs.full_v[st]), (i >> 1) & 1, abort_flag)) break;
-            const int Lc = min(BC, L - i * BC);
+            const int Lc = len_of(chunk_of(i));
             const bool live = vr < Lc;
             const uint32_t row = vslot(st) + vr * 128;
             // 16-byte pieces in the row's swizzled order (conflict-free)
@@ -830,7 +891,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             // bits.
             if (i > 0 && !warp_wait(bar(cs.dkv_full), (i - 1) & 1, abort_flag)) break;
             {
-                const float g = live ? pw(Lc - 1 - vr) : 0.f;
+                const float g = live ? pw(kAnti ? vr : Lc - 1 - vr) : 0.f;
                 const __nv_bfloat16 ghb = __float2bfloat16_rn(g);
                 const __nv_bfloat16 glb = __float2bfloat16_rn(g - __bfloat162float(ghb));
                 const __nv_bfloat162 gh = __halves2bfloat162(ghb, ghb);
@@ -952,6 +1013,8 @@ __global__ void wait_timeout_selftest_kernel(uint64_t timeout_ns) {
 
 cudaError_t prefill_tc_bf16(const PrefillArgs &a) {
     if (a.head_dim != D || (a.chunk != 0 && a.chunk != BC)) return cudaErrorNotSupported;
+    // rows are written in place; the anti-causal kernel starts from a zero state
+    if (a.reverse_out || (a.anti_causal && a.initial_state)) return cudaErrorNotSupported;
     CUtensorMap mq, mk, mv, mo;
     if (!make_map(&mq, a.q, a.total_tokens, a.num_heads) ||
         !make_map(&mk, a.k, a.total_tokens, a.num_heads) ||
@@ -961,10 +1024,10 @@ cudaError_t prefill_tc_bf16(const PrefillArgs &a) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    static int attr_set_for[64] = {0};  // bit 0: forward kernel, bit 1: reversed-output kernel
-    const int bit = a.reverse_out ? 2 : 1;
+    static int attr_set_for[64] = {0};  // bit 0: causal kernel, bit 1: anti-causal kernel
+    const int bit = a.anti_causal ? 2 : 1;
     if (dev < 64 && !(attr_set_for[dev] & bit)) {
-        e = cudaFuncSetAttribute(a.reverse_out ? prefill_tc_kernel<true> : prefill_tc_kernel<false>,
+        e = cudaFuncSetAttribute(a.anti_causal ? prefill_tc_kernel<true> : prefill_tc_kernel<false>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
         if (e != cudaSuccess) return e;
         attr_set_for[dev] |= bit;
@@ -972,7 +1035,7 @@ cudaError_t prefill_tc_bf16(const PrefillArgs &a) {
     const long grid = (long)(a.rank_limit > 0 ? a.rank_limit : a.nseq) * a.num_heads * NVS;
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffffL) return cudaErrorInvalidConfiguration;
-    auto kern = a.reverse_out ? prefill_tc_kernel<true> : prefill_tc_kernel<false>;
+    auto kern = a.anti_causal ? prefill_tc_kernel<true> : prefill_tc_kernel<false>;
     kern<<<(unsigned)grid, kThreads, kSmemBytes, a.stream>>>(
         mq, mk, mv, mo, a.decay, a.cu_seqlens, a.nseq, a.total_tokens, a.num_heads,
         a.initial_state, static_cast<__nv_bfloat16 *>(a.out), a.final_state, a.min_len);

@@ -354,8 +354,42 @@ def run_ours(args, ws, rank, local):
                 "chunk": 64, "kernel": "prefill_simt_kernel (FFMA), per-channel decay",
                 "roofline": cuda_core_roofline(flops, byts, ms, pk, sms)}
 
+    def time_snapshots(lengths, interval, reps):
+        """Prefill of the layer that also writes the state every `interval`
+        tokens (per-block prefix cache)."""
+        pin = wl.prefill_inputs(lengths, H, d, dtype=torch.bfloat16, seed=0, device=dev)
+        pout = torch.empty_like(pin.q)
+        pfs = torch.empty((len(lengths), H, d, d), dtype=torch.float32, device=dev)
+        nsnap = la.snapshot_count(pin.cu_seqlens, interval)
+        psn = torch.empty((nsnap, H, d, d), dtype=torch.float32, device=dev)
+
+        def run():
+            la.prefill_snapshots(pin.q, pin.k, pin.v, pin.decay, pin.cu_seqlens, interval,
+                                 out=pout, final_state=pfs, snapshots=psn, stream=stream)
+        run()
+        torch.cuda.synchronize()
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(reps):
+            run()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        la.device_status(stream)
+        ms = a0.elapsed_time(a1) / reps
+        Tn = sum(lengths)
+        byts, _ = prefill_alg(Tn, H, d, 128, len(lengths))
+        byts += nsnap * H * d * d * 4
+        return {"ms_per_launch": round(ms, 4), "tokens_per_s": round(Tn / (ms / 1e3), 1),
+                "snapshots": nsnap, "interval": interval,
+                "roofline": {"bound": "hbm", "alg_bytes": byts,
+                             "achieved": round(byts / (ms / 1e3) / 1e9, 1), "peak": pk["hbm"],
+                             "unit": "GB/s", "frac": round(byts / (ms / 1e3) / 1e9 / pk["hbm"], 4)}}
+
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     more = {"prefill_8k_channel_decay": time_channel_decay([8192], 10),
+            "prefill_8k_snapshots_every_1024": time_snapshots([8192], 1024, 10),
+            "prefill_8k_snapshots_every_128": time_snapshots([8192], 128, 10),
             "prefill_8k_chunk64_cuda_cores": time_prefill([8192], 64, 10),
             "prefill_128k": time_prefill([131072], 0, 5),
             "prefill_128k_chunk64_cuda_cores": time_prefill([131072], 64, 3),

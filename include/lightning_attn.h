@@ -126,6 +126,42 @@ la_status lightning_attn_prefill_with_state(const void *q, const void *k, const 
                                             float *final_state, void *stream);
 
 /*
+ * Prefill that also keeps the state at every block boundary: the prefix cache
+ * of a linear-attention layer kept once per block of tokens (K3 report notes
+ * on the inference engine: storing every step's state would give up linear
+ * attention's advantage, storing none gives no prefix reuse, so one cache
+ * entry per block).  Arguments and results are those of
+ * lightning_attn_prefill_with_state, plus
+ *
+ * snapshot_interval  tokens per block, > 0 and a multiple of the block the
+ *                    call computes with: 128 on the tensor-core path (bf16,
+ *                    head_dim 128, chunk 0 or 128), else the chunk (64 for
+ *                    chunk 0); LA_ERR_INVALID_ARG otherwise.
+ * snapshots          [N, num_heads, head_dim, head_dim] fp32 device array,
+ *                    16-byte aligned, N = lightning_attn_snapshot_count(...)
+ *                    of the same cu_seqlens (host copy).  Sequence s owns
+ *                    entries [b_s, b_s + floor(L_s / snapshot_interval)) with
+ *                    b_s = sum_{s' < s} floor(L_s' / snapshot_interval); entry
+ *                    b_s + j holds the state after the first
+ *                    (j + 1) * snapshot_interval tokens of s -- the final_state
+ *                    a prefill of those tokens alone (from the same initial
+ *                    state) returns.  A trailing partial block gets none.
+ */
+la_status lightning_attn_prefill_snapshots(const void *q, const void *k, const void *v,
+                                           const float *decay, const int32_t *cu_seqlens,
+                                           int32_t num_seqs, int32_t total_tokens,
+                                           int32_t num_heads, int32_t head_dim, int32_t chunk,
+                                           la_dtype dtype, const float *initial_state, void *out,
+                                           float *final_state, int32_t snapshot_interval,
+                                           float *snapshots, void *stream);
+
+/* Number of snapshots lightning_attn_prefill_snapshots writes for these
+ * sequences (host copy of cu_seqlens, num_seqs + 1 entries): the sum of
+ * floor(L_s / snapshot_interval).  -1 for invalid arguments. */
+int64_t lightning_attn_snapshot_count(const int32_t *cu_seqlens_host, int32_t num_seqs,
+                                      int32_t snapshot_interval);
+
+/*
  * Prefill with a channel-wise decay: one lambda per head and KEY channel
  * (K3 report reading notes: the scalar decay generalised to a channel-wise
  * one that can fall back to the uniform decay; it acts on the channels Q and
@@ -302,7 +338,7 @@ const char *lightning_attn_last_error(void);
 /* ABI version of this header: (major << 16) | minor. */
 int32_t lightning_attn_version(void);
 
-#define LIGHTNING_ATTN_VERSION ((1 << 16) | 4)
+#define LIGHTNING_ATTN_VERSION ((1 << 16) | 5)
 
 #ifdef __cplusplus
 }

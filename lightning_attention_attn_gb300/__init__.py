@@ -81,6 +81,12 @@ def load(path: str = LIB_PATH):
             lib.lightning_attn_decode_channel_decay.argtypes = [vp, vp, vp, vp, vp, i32, i32,
                                                                 i32, ctypes.c_int, vp, vp]
             lib.lightning_attn_decode_channel_decay.restype = ctypes.c_int
+            lib.lightning_attn_prefill_snapshots.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32,
+                                                             i32, i32, ctypes.c_int, vp, vp, vp,
+                                                             i32, vp, vp]
+            lib.lightning_attn_prefill_snapshots.restype = ctypes.c_int
+            lib.lightning_attn_snapshot_count.argtypes = [vp, i32, i32]
+            lib.lightning_attn_snapshot_count.restype = ctypes.c_int64
             lib.lightning_attn_decode.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32,
                                                   ctypes.c_int, vp, vp]
             lib.lightning_attn_decode.restype = ctypes.c_int
@@ -263,6 +269,60 @@ def mixed_step(q, k, v, decay, cu_seqlens, state, *, out=None, prefill_stream=No
         _dev(out, "out"), None if host_cu is None else ctypes.addressof(host_cu), ps, ds)
     _check(st, "lightning_attn_mixed_step")
     return out
+
+
+def snapshot_count(cu_seqlens, snapshot_interval: int) -> int:
+    """Number of per-block state snapshots :func:`prefill_snapshots` writes:
+    sum over sequences of floor(L_s / snapshot_interval).  ``cu_seqlens`` may
+    live on either device (a host copy is made)."""
+    cu = cu_seqlens.detach().to("cpu", torch.int32).contiguous()
+    n = int(load().lightning_attn_snapshot_count(cu.data_ptr(), cu.numel() - 1,
+                                                 int(snapshot_interval)))
+    if n < 0:
+        raise ValueError("invalid cu_seqlens or snapshot_interval")
+    return n
+
+
+def prefill_snapshots(q, k, v, decay, cu_seqlens, snapshot_interval: int, *, chunk: int = 0,
+                      out=None, final_state=None, snapshots=None, initial_state=None,
+                      stream=None):
+    """Prefill that also returns the state after every ``snapshot_interval``
+    tokens of each sequence (a per-block prefix cache).  Returns ``(out,
+    final_state, snapshots)`` with snapshots fp32 [N, H, d, d] in sequence
+    order (see :func:`snapshot_count`); the interval is a multiple of the
+    block the call computes with (128 on the tensor-core path)."""
+    if q.dim() != 3:
+        raise ValueError("q must be [T, H, d]")
+    T, H, d = q.shape
+    for name, t in (("k", k), ("v", v)):
+        if t.shape != q.shape or t.dtype != q.dtype:
+            raise ValueError(f"{name} must match q in shape and dtype")
+    if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1:
+        raise ValueError("cu_seqlens must be a 1-D int32 tensor")
+    if decay.dtype != torch.float32 or decay.numel() != H:
+        raise ValueError("decay must be fp32 [H]")
+    nseq = cu_seqlens.numel() - 1
+    if snapshots is None:
+        # sizing needs the lengths on the host (one synchronising copy); pass
+        # `snapshots` of snapshot_count() entries to avoid it
+        n = snapshot_count(cu_seqlens, snapshot_interval)
+        snapshots = torch.empty((max(n, 1), H, d, d), dtype=torch.float32,
+                                device=q.device)[:n]
+    elif snapshots.dtype != torch.float32 or snapshots.dim() != 4 or \
+            tuple(snapshots.shape[1:]) != (H, d, d):
+        raise ValueError("snapshots must be fp32 [N, H, d, d] with N = snapshot_count()")
+    if out is None:
+        out = torch.empty_like(q)
+    if final_state is None:
+        final_state = torch.empty((nseq, H, d, d), dtype=torch.float32, device=q.device)
+    st = load().lightning_attn_prefill_snapshots(
+        _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(decay, "decay"),
+        _dev(cu_seqlens, "cu_seqlens"), nseq, T, H, d, int(chunk), _dtype_code(q),
+        None if initial_state is None else _dev(initial_state, "initial_state"),
+        _dev(out, "out"), _dev(final_state, "final_state"), int(snapshot_interval),
+        _dev(snapshots, "snapshots"), _stream_handle(stream))
+    _check(st, "lightning_attn_prefill_snapshots")
+    return out, final_state, snapshots
 
 
 def prefill_channel_decay(q, k, v, decay, cu_seqlens=None, *, chunk: int = 0, out=None,

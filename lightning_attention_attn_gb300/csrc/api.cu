@@ -165,6 +165,52 @@ la_status lightning_attn_prefill_with_state(const void *q, const void *k, const 
     return run_prefill(a, dtype);
 }
 
+la_status lightning_attn_prefill_snapshots(const void *q, const void *k, const void *v,
+                                           const float *decay, const int32_t *cu_seqlens,
+                                           int32_t num_seqs, int32_t total_tokens,
+                                           int32_t num_heads, int32_t head_dim, int32_t chunk,
+                                           la_dtype dtype, const float *initial_state, void *out,
+                                           float *final_state, int32_t snapshot_interval,
+                                           float *snapshots, void *stream) {
+    if (snapshot_interval <= 0)
+        return fail(LA_ERR_INVALID_ARG, "snapshot_interval must be > 0 (got %d)", snapshot_interval);
+    bool work = false;
+    const la_status st = check_prefill(q, k, v, decay, cu_seqlens, num_seqs, total_tokens,
+                                       num_heads, head_dim, chunk, dtype, initial_state, out,
+                                       final_state, stream, &work);
+    if (st != LA_OK || !work) return st;
+    if (!snapshots || !aligned16(snapshots))
+        return fail(LA_ERR_INVALID_ARG, "snapshots must be a 16-byte aligned device array");
+    // the kernel that serves the call and its block
+    const bool tc = dtype == LA_DTYPE_BF16 && head_dim == 128 && (chunk == 0 || chunk == 128);
+    const int block = tc ? 128 : (chunk == 0 ? 64 : chunk);
+    if (!tc && (chunk == 128 || chunk == 256))
+        return fail(LA_ERR_UNSUPPORTED,
+                    "chunk %d needs the tensor-core path (bf16, head_dim 128)", chunk);
+    if (snapshot_interval % block != 0)
+        return fail(LA_ERR_INVALID_ARG,
+                    "snapshot_interval %d is not a multiple of the block (%d tokens) this "
+                    "call runs with", snapshot_interval, block);
+    la::PrefillArgs a{q, k, v, decay, cu_seqlens, num_seqs, total_tokens, num_heads,
+                      head_dim, chunk, out, final_state, static_cast<cudaStream_t>(stream),
+                      initial_state};
+    a.snapshots = snapshots;
+    a.snapshot_interval = snapshot_interval;
+    return run_prefill(a, dtype);
+}
+
+int64_t lightning_attn_snapshot_count(const int32_t *cu_seqlens_host, int32_t num_seqs,
+                                      int32_t snapshot_interval) {
+    if (num_seqs < 0 || snapshot_interval <= 0 || (num_seqs > 0 && !cu_seqlens_host)) return -1;
+    int64_t n = 0;
+    for (int32_t s = 0; s < num_seqs; ++s) {
+        const int64_t L = (int64_t)cu_seqlens_host[s + 1] - cu_seqlens_host[s];
+        if (L < 0) return -1;
+        n += L / snapshot_interval;
+    }
+    return n;
+}
+
 la_status lightning_attn_prefill(const void *q, const void *k, const void *v,
                                  const float *decay, const int32_t *cu_seqlens,
                                  int32_t num_seqs, int32_t total_tokens,

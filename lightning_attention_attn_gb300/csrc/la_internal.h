@@ -27,6 +27,12 @@ struct PrefillArgs {
     // final state is then sum_u lambda^(u - t0) k_u^T v_u.  Tensor-core
     // kernel only, zero initial state.
     bool anti_causal = false;
+    // Per-block state snapshots (nullptr: none): the state after every
+    // snapshot_interval tokens of each sequence, [N, H, D, D] fp32, sequence
+    // s's snapshots from index sum_{s' < s} floor(L_s' / snapshot_interval).
+    // snapshot_interval is a multiple of the kernel's chunk.
+    float *snapshots = nullptr;
+    int snapshot_interval = 0;
 };
 
 struct DecodeArgs {

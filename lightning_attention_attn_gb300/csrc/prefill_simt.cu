@@ -97,6 +97,7 @@ struct SimtSmem {
     // the staging of K_s, whose lanes walk consecutive channels
     float wk[CW ? B + 1 : 1][CW ? D : 1];
     int slot;
+    int snap_base;  // first snapshot of this CTA's sequence
 };
 
 // One CTA per (sequence, head, 64-column value slice); 256 threads.  Every
@@ -112,7 +113,7 @@ prefill_simt_kernel(const T *__restrict__ q, const T *__restrict__ k,
                     const T *__restrict__ v, const float *__restrict__ decay,
                     const int32_t *__restrict__ cu, int nseq, int T_total, int H,
                     const float *initial_state, T *__restrict__ out, float *final_state,
-                    int reverse_out, int min_len) {
+                    int reverse_out, int min_len, float *snapshots, int snap_interval) {
     using Smem = SimtSmem<D, B, CW>;
     using R2 = typename Pair<T>::type;
     constexpr int P = Smem::P, WP = Smem::WP;
@@ -133,6 +134,20 @@ prefill_simt_kernel(const T *__restrict__ q, const T *__restrict__ k,
     if (L < min_len) return;  // a mixed step's decode launch owns this sequence
     const int nv0 = vs * kDV;
     const long row_stride = (long)H * D;
+    if (snapshots) {
+        // per-block snapshots (K3 report notes: one prefix cache per block):
+        // index of this sequence's first one = snapshots of the sequences before it
+        if (tid == 0) sm.snap_base = 0;
+        __syncthreads();
+        int part = 0;
+        for (int s2 = tid; s2 < s; s2 += kThreads) {
+            int a0 = __ldg(cu + s2), a1 = __ldg(cu + s2 + 1);
+            a0 = min(max(a0, 0), T_total);
+            a1 = min(max(a1, a0), T_total);
+            part += (a1 - a0) / snap_interval;
+        }
+        if (part) atomicAdd(&sm.snap_base, part);
+    }
 
     if constexpr (CW) {
         // channel-wise decay (K3 report reading notes): lambda per key
@@ -477,6 +492,16 @@ prefill_simt_kernel(const T *__restrict__ q, const T *__restrict__ k,
             }
         }
         __syncthreads();
+        // the state after the first c0 + Lc tokens closes a block: snapshot
+        if (snapshots && (c0 + Lc) % snap_interval == 0) {
+            float *dst = snapshots +
+                         ((long)(sm.snap_base + (c0 + Lc) / snap_interval - 1) * H + h) * D * D;
+            for (int e = tid; e < D * kDV / 4; e += kThreads) {
+                const int i = e / (kDV / 4), n = 4 * (e % (kDV / 4));
+                *reinterpret_cast<float4 *>(dst + (long)i * D + nv0 + n) =
+                    *reinterpret_cast<const float4 *>(&sm.kv[i][n]);
+            }
+        }
     }
 
     if (final_state) {
@@ -503,13 +528,15 @@ cudaError_t launch(const PrefillArgs &a) {
         static_cast<const T *>(a.q), static_cast<const T *>(a.k),
         static_cast<const T *>(a.v), a.decay, a.cu_seqlens, a.nseq, a.total_tokens,
         a.num_heads, a.initial_state, static_cast<T *>(a.out), a.final_state,
-        a.reverse_out ? 1 : 0, a.min_len);
+        a.reverse_out ? 1 : 0, a.min_len, a.snapshots, a.snapshot_interval);
     return cudaGetLastError();
 }
 
 template <typename T, bool CW>
 cudaError_t dispatch(const PrefillArgs &a) {
     const int B = a.chunk == 0 ? 64 : a.chunk;
+    if (a.snapshots && (a.snapshot_interval <= 0 || a.snapshot_interval % B != 0))
+        return cudaErrorNotSupported;
     if (a.head_dim == 64) {
         if (B == 16) return launch<T, 64, 16, CW>(a);
         if (B == 32) return launch<T, 64, 32, CW>(a);

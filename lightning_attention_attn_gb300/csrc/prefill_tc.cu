@@ -115,6 +115,7 @@ struct Ctrl {
     uint32_t tmem_base;
     int abort;
     int seq_slot;
+    int snap_base;                 // first snapshot of this CTA's sequence
     int pad;
     float vmax[2][4];              // per-warp max |v| of a chunk, double buffered
     float vscale[4];               // 2^f of V's fp16 scale, ring indexed by chunk & 3
@@ -191,13 +192,17 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 // k_u^T v_u (G_c = lambda^{B_c} G_{c+1} + (Lambda_K K_c)^T V_c with
 // Lambda_K = diag(lambda^l)), and row j of a chunk that has a successor gains
 // lambda^(B - j) q_j G_{c+1}.  Every exponent is again >= 0.
-template <bool kAnti>
+// kSnap (causal only): the state after every snap_interval tokens of a
+// sequence (a multiple of B) is also written to `snapshots` (per-block
+// prefix cache, K3 report notes); sequence s's snapshots start at index
+// sum_{s' < s} floor(L_s' / snap_interval).
+template <bool kAnti, bool kSnap>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                   const float *__restrict__ decay, const int32_t *__restrict__ cu, int nseq, int T,
                   int H, const float *initial_state, __nv_bfloat16 *__restrict__ out,
-                  float *final_state, int min_len) {
+                  float *final_state, int min_len, float *snapshots, int snap_interval) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *base = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -262,6 +267,19 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         mbar_init(bar(cs.done_b), 1);
         cs.abort = 0;
         fence_mbar_init();
+    }
+    if constexpr (kSnap) {
+        // snapshots of the sequences before s (lengths clamped as above)
+        if (threadIdx.x == 0) cs.snap_base = 0;
+        __syncthreads();
+        int part = 0;
+        for (int s2 = threadIdx.x; s2 < s; s2 += kThreads) {
+            int a0 = __ldg(cu + s2), a1 = __ldg(cu + s2 + 1);
+            a0 = min(max(a0, 0), T);
+            a1 = min(max(a1, a0), T);
+            part += (a1 - a0) / snap_interval;
+        }
+        if (part) atomicAdd(&cs.snap_base, part);
     }
     for (int e = threadIdx.x; e <= BC; e += kThreads) cs.pw[e] = powf(lam, (float)e);
     if (threadIdx.x < 64) cs.pwt[threadIdx.x] = threadIdx.x < 32 ? 0.f : powf(lam, (float)(threadIdx.x - 32));
@@ -760,6 +778,19 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
                     kv[16 * hh + 2 * c + 1] = x.y;
                 }
             }
+            if constexpr (kSnap) {
+                // the state after the first (i + 1) B tokens closes a block
+                const int end = (i + 1) * BC;
+                if (end <= L && end % snap_interval == 0) {
+                    float4 *dst = reinterpret_cast<float4 *>(
+                        snapshots +
+                        (((long)(cs.snap_base + end / snap_interval - 1) * H + h) * D + r) * D +
+                        vs * DV);
+#pragma unroll
+                    for (int c = 0; c < DV / 4; ++c)
+                        dst[c] = make_float4(kv[4 * c], kv[4 * c + 1], kv[4 * c + 2], kv[4 * c + 3]);
+                }
+            }
             if (!last) {
                 write_back(kv, pw(len_of(chunk_of(i + 1))));
             } else if (final_state) {
@@ -1024,21 +1055,28 @@ cudaError_t prefill_tc_bf16(const PrefillArgs &a) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    static int attr_set_for[64] = {0};  // bit 0: causal kernel, bit 1: anti-causal kernel
-    const int bit = a.anti_causal ? 2 : 1;
+    const bool snap = a.snapshots != nullptr;
+    if (snap && (a.anti_causal || a.snapshot_interval <= 0 || a.snapshot_interval % BC != 0))
+        return cudaErrorNotSupported;
+    auto kern = a.anti_causal ? prefill_tc_kernel<true, false>
+                : snap        ? prefill_tc_kernel<false, true>
+                              : prefill_tc_kernel<false, false>;
+    // bit 0: causal kernel, bit 1: anti-causal, bit 2: causal with snapshots
+    static int attr_set_for[64] = {0};
+    const int bit = a.anti_causal ? 2 : snap ? 4 : 1;
     if (dev < 64 && !(attr_set_for[dev] & bit)) {
-        e = cudaFuncSetAttribute(a.anti_causal ? prefill_tc_kernel<true> : prefill_tc_kernel<false>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kSmemBytes);
         if (e != cudaSuccess) return e;
         attr_set_for[dev] |= bit;
     }
     const long grid = (long)(a.rank_limit > 0 ? a.rank_limit : a.nseq) * a.num_heads * NVS;
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffffL) return cudaErrorInvalidConfiguration;
-    auto kern = a.anti_causal ? prefill_tc_kernel<true> : prefill_tc_kernel<false>;
     kern<<<(unsigned)grid, kThreads, kSmemBytes, a.stream>>>(
         mq, mk, mv, mo, a.decay, a.cu_seqlens, a.nseq, a.total_tokens, a.num_heads,
-        a.initial_state, static_cast<__nv_bfloat16 *>(a.out), a.final_state, a.min_len);
+        a.initial_state, static_cast<__nv_bfloat16 *>(a.out), a.final_state, a.min_len,
+        a.snapshots, a.snapshot_interval);
     return cudaGetLastError();
 }
 

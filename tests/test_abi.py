@@ -23,6 +23,7 @@ def test_header_declares_expected_calls():
               "lightning_attn_backward", "lightning_attn_backward_workspace_bytes",
               "lightning_attn_mixed_step", "lightning_attn_prefill_channel_decay",
               "lightning_attn_decode_channel_decay",
+              "lightning_attn_prefill_snapshots", "lightning_attn_snapshot_count",
               "lightning_attn_decode",
               "lightning_attn_status_string", "lightning_attn_last_error",
               "lightning_attn_version", "lightning_attn_device_status",
@@ -40,7 +41,7 @@ def test_library_exports_every_header_symbol(lib):
 
 
 def test_version(lib):
-    assert la.version() == (1, 4)
+    assert la.version() == (1, 5)
 
 
 def test_status_strings(lib):
@@ -234,3 +235,33 @@ def test_channel_decay_host_validation(lib):
     g = lib.lightning_attn_decode_channel_decay
     assert g(A, A, A, A, A, 4, 2, 96, la.LA_DTYPE_BF16, A, None) == la.LA_ERR_INVALID_ARG
     assert g(A, A, A, A, A, 0, 2, 128, la.LA_DTYPE_BF16, A, None) == la.LA_OK
+
+
+def test_snapshot_host_validation(lib):
+    f = lib.lightning_attn_prefill_snapshots
+    common = (A, A, A, A, A, 1, 8, 2, 128)
+    # interval <= 0, or not a multiple of the block the call computes with
+    assert f(*common, 0, la.LA_DTYPE_BF16, None, A, A, 0, A, None) == la.LA_ERR_INVALID_ARG
+    assert f(*common, 0, la.LA_DTYPE_BF16, None, A, A, 192, A, None) == la.LA_ERR_INVALID_ARG
+    assert f(*common, 0, la.LA_DTYPE_FP32, None, A, A, 96, A, None) == la.LA_ERR_INVALID_ARG
+    assert f(*common, 32, la.LA_DTYPE_FP32, None, A, A, 48, A, None) == la.LA_ERR_INVALID_ARG
+    # missing or misaligned snapshot array
+    assert f(*common, 0, la.LA_DTYPE_BF16, None, A, A, 256, None, None) == la.LA_ERR_INVALID_ARG
+    assert f(*common, 0, la.LA_DTYPE_BF16, None, A, A, 256, A + 8, None) == la.LA_ERR_INVALID_ARG
+    # chunk 256 has no kernel; no sequences: nothing to do
+    assert f(*common, 256, la.LA_DTYPE_FP32, None, A, A, 256, A, None) == la.LA_ERR_UNSUPPORTED
+    assert f(A, A, A, A, A, 0, 8, 2, 128, 0, la.LA_DTYPE_BF16, None, A, A, 128, A, None) == \
+        la.LA_OK
+
+
+def test_snapshot_count(lib):
+    import torch
+    cu = (ctypes.c_int32 * 5)(0, 100, 356, 356, 1000)
+    g = lib.lightning_attn_snapshot_count
+    assert g(cu, 4, 128) == 0 + 2 + 0 + 5
+    assert g(cu, 4, 64) == 1 + 4 + 0 + 10
+    assert g(cu, 4, 0) == -1
+    assert g(None, 4, 64) == -1
+    bad = (ctypes.c_int32 * 3)(0, 10, 5)
+    assert g(bad, 2, 64) == -1
+    assert la.snapshot_count(torch.tensor([0, 100, 356, 356, 1000], dtype=torch.int32), 128) == 7

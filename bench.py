@@ -471,48 +471,87 @@ def run_ours(args, ws, rank, local):
     del dout, dq, dk, dv, bws
 
     # ---------------- mixed serving step (decode + prefill on two streams):
-    # 128 sequences x 64 heads with cached states, two of them with 256 new
-    # tokens, the rest one new token
-    mlen = [256 if s_ in (0, 77) else 1 for s_ in range(128)]
-    minp = wl.prefill_inputs(mlen, H, d, dtype=torch.bfloat16, seed=2, device=dev)
-    mstate = wl.cached_states(len(mlen), H, d, seed=3, device=dev)
-    mcu = minp.cu_seqlens.cpu().tolist()
-    mout = torch.empty_like(minp.q)
-    dstream = torch.cuda.Stream(device=dev)
+    # every sequence continues from a cached state; a few have several new
+    # tokens, the rest one
+    # the decode stream at a higher priority: its small blocks start before
+    # the prefill's large ones take the SMs
+    dstream = torch.cuda.Stream(device=dev, priority=-1)
 
-    def mstep(two):
-        if two:
-            la.mixed_step(minp.q, minp.k, minp.v, minp.decay, minp.cu_seqlens, mstate, out=mout,
-                          prefill_stream=stream, decode_stream=dstream, cu_seqlens_host=mcu)
-        else:  # the same update through one prefill launch for every sequence
-            la.prefill(minp.q, minp.k, minp.v, minp.decay, minp.cu_seqlens, out=mout,
-                       initial_state=mstate, final_state=mstate, stream=stream)
+    def measure_mixed(mlen, label, seed):
+        minp = wl.prefill_inputs(mlen, H, d, dtype=torch.bfloat16, seed=seed, device=dev)
+        mstate = wl.cached_states(len(mlen), H, d, seed=seed + 1, device=dev)
+        mcu = minp.cu_seqlens.cpu().tolist()
+        mout = torch.empty_like(minp.q)
 
-    mixed = {"config": {"workload": "mixed step: 128 sequences x 64 heads, 2 with 256 new "
-                                    "tokens, 126 with 1, cached fp32 states"}}
-    for two in (True, False):
+        def mstep(two):
+            if two:
+                la.mixed_step(minp.q, minp.k, minp.v, minp.decay, minp.cu_seqlens, mstate,
+                              out=mout, prefill_stream=stream, decode_stream=dstream,
+                              cu_seqlens_host=mcu)
+            else:  # the same update through one prefill launch for every sequence
+                la.prefill(minp.q, minp.k, minp.v, minp.decay, minp.cu_seqlens, out=mout,
+                           initial_state=mstate, final_state=mstate, stream=stream)
+
+        res = {"config": {"workload": label}}
+        for two in (True, False):
+            for _ in range(3):
+                mstep(two)
+            torch.cuda.synchronize()
+            m0 = torch.cuda.Event(enable_timing=True)
+            m1 = torch.cuda.Event(enable_timing=True)
+            m0.record(stream)
+            for _ in range(K):
+                mstep(two)
+            m1.record(stream)
+            torch.cuda.synchronize()
+            res["ms_two_streams" if two else "ms_one_prefill_launch"] = round(
+                m0.elapsed_time(m1) / K, 4)
+        la.device_status(stream)
+        mbytes = len(mlen) * H * d * d * 4 * 2 + sum(mlen) * H * d * 2 * 4
+        res["tokens_per_s"] = round(sum(mlen) / (res["ms_two_streams"] / 1e3), 1)
+        res["speedup_vs_one_launch"] = round(res["ms_one_prefill_launch"] /
+                                             res["ms_two_streams"], 2)
+        res["roofline"] = {"bound": "hbm", "alg_bytes_per_step": mbytes,
+                           "achieved": round(mbytes / (res["ms_two_streams"] / 1e3) / 1e9, 1),
+                           "peak": pk["hbm"], "unit": "GB/s"}
+        res["roofline"]["frac"] = round(res["roofline"]["achieved"] / pk["hbm"], 4)
+        return res
+
+    mixed = measure_mixed([256 if s_ in (0, 77) else 1 for s_ in range(128)],
+                          "mixed step: 128 sequences x 64 heads, 2 with 256 new tokens, "
+                          "126 with 1, cached fp32 states", 2)
+    # the serving batch the pages time their two-stream split on: 20 requests,
+    # 2 with 50-token inputs, the rest decoding
+    mixed["pages_batch"] = measure_mixed([50 if s_ in (3, 11) else 1 for s_ in range(20)],
+                                         "20 sequences x 64 heads, 2 with 50 new tokens, "
+                                         "18 with 1, cached fp32 states", 4)
+
+    # short inputs alone: the tensor-core block (one partial 128-token chunk)
+    # against the CUDA-core kernel at chunk 32 and 64
+    sinp = wl.prefill_inputs([50, 50], H, d, dtype=torch.bfloat16, seed=6, device=dev)
+    sst = wl.cached_states(2, H, d, seed=7, device=dev)
+    sout = torch.empty_like(sinp.q)
+    sfs = torch.empty_like(sst)
+    short = {"config": {"workload": "2 sequences x 50 new tokens x 64 heads from cached states"}}
+    for ch in (0, 32, 64):
+        def sstep():
+            la.prefill(sinp.q, sinp.k, sinp.v, sinp.decay, sinp.cu_seqlens, chunk=ch, out=sout,
+                       initial_state=sst, final_state=sfs, stream=stream)
         for _ in range(3):
-            mstep(two)
+            sstep()
         torch.cuda.synchronize()
-        m0 = torch.cuda.Event(enable_timing=True)
-        m1 = torch.cuda.Event(enable_timing=True)
-        m0.record(stream)
+        s0_ = torch.cuda.Event(enable_timing=True)
+        s1_ = torch.cuda.Event(enable_timing=True)
+        s0_.record(stream)
         for _ in range(K):
-            mstep(two)
-        m1.record(stream)
+            sstep()
+        s1_.record(stream)
         torch.cuda.synchronize()
-        mixed["ms_two_streams" if two else "ms_one_prefill_launch"] = round(
-            m0.elapsed_time(m1) / K, 4)
+        short["ms_chunk_%d" % ch if ch else "ms_tensor_core_block_128"] = round(
+            s0_.elapsed_time(s1_) / K, 4)
     la.device_status(stream)
-    mbytes = len(mlen) * H * d * d * 4 * 2 + sum(mlen) * H * d * 2 * 4
-    mixed["tokens_per_s"] = round(sum(mlen) / (mixed["ms_two_streams"] / 1e3), 1)
-    mixed["speedup_vs_one_launch"] = round(mixed["ms_one_prefill_launch"] /
-                                           mixed["ms_two_streams"], 2)
-    mixed["roofline"] = {"bound": "hbm", "alg_bytes_per_step": mbytes,
-                         "achieved": round(mbytes / (mixed["ms_two_streams"] / 1e3) / 1e9, 1),
-                         "peak": pk["hbm"], "unit": "GB/s"}
-    mixed["roofline"]["frac"] = round(mixed["roofline"]["achieved"] / pk["hbm"], 4)
-    del minp, mstate, mout
+    mixed["short_inputs"] = short
+    del sinp, sst, sout, sfs
 
     # ---------------- end to end through the public call, host buffers.
     # Every step copies its inputs from pinned host memory, runs the prefill

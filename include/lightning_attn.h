@@ -295,7 +295,10 @@ int64_t lightning_attn_backward_noalloc_max_bytes(void);
  * device are created on first use for this fork and join; calls from
  * several host threads are serialised while they enqueue).  With
  * decode_stream == prefill_stream the two launches simply run one after the
- * other.  chunk is the path's default; dtype rules as for prefill.
+ * other.  A decode_stream of higher priority than prefill_stream lets the
+ * decode kernel's small blocks start before the prefill's large ones occupy
+ * the SMs (measured: 20 sequences x 64 heads, 2 with 50 new tokens, 45 ->
+ * 37 us).  chunk is the path's default; dtype rules as for prefill.
  *
  * q, k, v, out    [total_tokens, num_heads, head_dim], dtype `dtype`
  * state           [num_seqs, num_heads, head_dim, head_dim] fp32, read and written

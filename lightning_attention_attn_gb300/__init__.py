@@ -242,7 +242,10 @@ def mixed_step(q, k, v, decay, cu_seqlens, state, *, out=None, prefill_stream=No
     [nseq, H, d, d] is updated in place.  Returns out [T, H, d]; the step is
     ordered on ``prefill_stream`` (the current stream when None).
     ``cu_seqlens_host`` (a host sequence of ints, optional) lets the prefill
-    launch cover only the sequences with two or more new tokens."""
+    launch cover only the sequences with two or more new tokens.  A decode
+    stream of higher priority than the prefill stream (e.g.
+    ``torch.cuda.Stream(priority=-1)``) lets the small decode blocks start
+    before the prefill's large ones fill the SMs."""
     if q.dim() != 3:
         raise ValueError("q must be [T, H, d]")
     T, H, d = q.shape

@@ -48,6 +48,8 @@
 //   warps 8-11   V-tile: Vhat hi/lo, fp16 V
 //   warp  12     MMA stream A (one thread): S and P V; TMA loads of the V ring
 //   warp  13     MMA stream B (one thread): dKV and Q KV
+// (the anti-causal instantiation swaps warps 12/13 with 14/15: its heavy
+// mask quadrants are 0 and 1, and a helper must sit on its quadrant)
 // Each ring slot is reloaded, by a role that waits for that event anyway, as
 // soon as the last MMA reading it has finished.
 // Two issuing threads keep the tensor pipe fed while either one waits: the

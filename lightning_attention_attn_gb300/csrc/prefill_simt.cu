@@ -47,6 +47,15 @@ __device__ __forceinline__ void store4(__nv_bfloat16 *p, float a, float b, float
     *reinterpret_cast<uint2 *>(p) = u;
 }
 
+// acc[c] += x b[c] for a row of four accumulators, as two packed fp32 FMAs
+// (each lane of a packed FMA rounds exactly like fmaf)
+__device__ __forceinline__ void fma_row4(float (&acc)[4], float x, const float (&b)[4]) {
+    const float2 xx = make_float2(x, x);
+    const float2 a0 = __ffma2_rn(xx, make_float2(b[0], b[1]), make_float2(acc[0], acc[1]));
+    const float2 a1 = __ffma2_rn(xx, make_float2(b[2], b[3]), make_float2(acc[2], acc[3]));
+    acc[0] = a0.x; acc[1] = a0.y; acc[2] = a1.x; acc[3] = a1.y;
+}
+
 // N consecutive floats of shared memory (N in {1, 2, 4, 8}; p aligned to N floats)
 template <int N> __device__ __forceinline__ void lds(float (&x)[N], const float *p) {
     if constexpr (N == 1) {
@@ -304,9 +313,17 @@ prefill_simt_kernel(const T *__restrict__ q, const T *__restrict__ k,
 #pragma unroll
                             for (int r = 0; r < 4; ++r)
 #pragma unroll
-                                for (int c = 0; c < 4; ++c)
-                                    acc[r][c] = fmaf(st.qa[u][r] * st.w8[u][4 + r - c],
-                                                     st.kb[u][c], acc[r][c]);
+                                for (int c = 0; c < 4; c += 2) {
+                                    // (q_r lambda^(d+r-c), q_r lambda^(d+r-c-1)) (k_c, k_c+1)
+                                    const float2 p = __fmul2_rn(
+                                        make_float2(st.qa[u][r], st.qa[u][r]),
+                                        make_float2(st.w8[u][4 + r - c], st.w8[u][3 + r - c]));
+                                    const float2 x = __ffma2_rn(
+                                        p, make_float2(st.kb[u][c], st.kb[u][c + 1]),
+                                        make_float2(acc[r][c], acc[r][c + 1]));
+                                    acc[r][c] = x.x;
+                                    acc[r][c + 1] = x.y;
+                                }
                     });
             } else {
                 struct St { float qa[2][4], kb[2][4]; };
@@ -324,10 +341,7 @@ prefill_simt_kernel(const T *__restrict__ q, const T *__restrict__ k,
 #pragma unroll
                         for (int u = 0; u < 2; ++u)
 #pragma unroll
-                            for (int r = 0; r < 4; ++r)
-#pragma unroll
-                                for (int c = 0; c < 4; ++c)
-                                    acc[r][c] = fmaf(st.qa[u][r], st.kb[u][c], acc[r][c]);
+                            for (int r = 0; r < 4; ++r) fma_row4(acc[r], st.qa[u][r], st.kb[u]);
                     });
             }
         }
@@ -379,10 +393,7 @@ prefill_simt_kernel(const T *__restrict__ q, const T *__restrict__ k,
 #pragma unroll
                         for (int u = 0; u < 2; ++u)
 #pragma unroll
-                            for (int r = 0; r < TJ; ++r)
-#pragma unroll
-                                for (int c = 0; c < 4; ++c)
-                                    oi[r][c] = fmaf(st.pa[u][r], st.vb[u][c], oi[r][c]);
+                            for (int r = 0; r < TJ; ++r) fma_row4(oi[r], st.pa[u][r], st.vb[u]);
                     });
             }
             if constexpr (CW) {
@@ -408,10 +419,7 @@ prefill_simt_kernel(const T *__restrict__ q, const T *__restrict__ k,
 #pragma unroll
                             for (int c = 0; c < 4; ++c) kl[c] = st.kb[u][c] * st.l1[u];
 #pragma unroll
-                            for (int r = 0; r < TJ; ++r)
-#pragma unroll
-                                for (int c = 0; c < 4; ++c)
-                                    oe[r][c] = fmaf(qw[r], kl[c], oe[r][c]);
+                            for (int r = 0; r < TJ; ++r) fma_row4(oe[r], qw[r], kl);
                         }
                     });
             } else {
@@ -429,10 +437,7 @@ prefill_simt_kernel(const T *__restrict__ q, const T *__restrict__ k,
 #pragma unroll
                         for (int u = 0; u < 2; ++u)
 #pragma unroll
-                            for (int r = 0; r < TJ; ++r)
-#pragma unroll
-                                for (int c = 0; c < 4; ++c)
-                                    oe[r][c] = fmaf(st.qa[u][r], st.kb[u][c], oe[r][c]);
+                            for (int r = 0; r < TJ; ++r) fma_row4(oe[r], st.qa[u][r], st.kb[u]);
                     });
             }
 #pragma unroll
@@ -475,10 +480,7 @@ prefill_simt_kernel(const T *__restrict__ q, const T *__restrict__ k,
 #pragma unroll
                         for (int u = 0; u < 2; ++u)
 #pragma unroll
-                            for (int r = 0; r < TI; ++r)
-#pragma unroll
-                                for (int c = 0; c < 4; ++c)
-                                    a[r][c] = fmaf(st.ka[u][r], st.vb[u][c], a[r][c]);
+                            for (int r = 0; r < TI; ++r) fma_row4(a[r], st.ka[u][r], st.vb[u]);
                     });
             }
 #pragma unroll

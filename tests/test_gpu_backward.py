@@ -68,3 +68,50 @@ def test_backward_layer_sized_sampled_heads():
                           inp.cu_seqlens.cpu(), sub(dout))
     for x, r, name in zip((dq, dk, dv), ref, ("dq", "dk", "dv")):
         assert_close(sub(x), r, TOL_BF16, f"layer-sized {name}")
+
+
+@pytest.mark.parametrize("lam", [1.0, 1e-30, 0.5])
+def test_tensor_core_backward_special_decays(lam):
+    """lambda = 1 (prefix and suffix sums), lambda -> 0 (only the diagonal
+    term) and 1/2 through the causal and anti-causal tensor-core launches."""
+    lengths, H, d = [300, 5, 129], 2, 128
+    inp = wl.prefill_inputs(lengths, H, d, dtype=torch.bfloat16, seed=24, device="cuda")
+    decay = torch.full((H,), lam, dtype=torch.float32, device="cuda")
+    g = torch.Generator(device="cuda")
+    g.manual_seed(1024)
+    dout = torch.randn(inp.q.shape, generator=g, device="cuda").to(torch.bfloat16)
+    got = la.backward(inp.q, inp.k, inp.v, decay, inp.cu_seqlens, dout)
+    torch.cuda.synchronize()
+    ref = oracle.backward(inp.q, inp.k, inp.v, decay.cpu(), inp.cu_seqlens.cpu(), dout)
+    for x, r, name in zip(got, ref, ("dq", "dk", "dv")):
+        assert_close(x, r, TOL_BF16, f"lambda={lam} {name}")
+
+
+def test_tensor_core_backward_many_sequences():
+    """More sequences than the in-kernel length sort handles (natural order)
+    in the anti-causal launches."""
+    g = torch.Generator().manual_seed(25)
+    lengths = torch.randint(0, 260, (150,), generator=g).tolist()
+    got, ref = run(lengths, 2, 128, torch.bfloat16, 0, 26)
+    for x, r, name in zip(got, ref, ("dq", "dk", "dv")):
+        assert_close(x, r, TOL_BF16, f"150 sequences {name}")
+
+
+def test_backward_writes_stay_inside_gradients():
+    """Sentinel guard regions around dq, dk and dv stay untouched."""
+    lengths, H, d = [5, 200, 129], 2, 128
+    inp = wl.prefill_inputs(lengths, H, d, dtype=torch.bfloat16, seed=27, device="cuda")
+    T, G = inp.total_tokens, 4096
+    g = torch.Generator(device="cuda")
+    g.manual_seed(1027)
+    dout = torch.randn(inp.q.shape, generator=g, device="cuda").to(torch.bfloat16)
+    bigs = [torch.full((T * H * d + 2 * G,), 321.0, dtype=torch.bfloat16, device="cuda")
+            for _ in range(3)]
+    dq, dk, dv = (b[G:G + T * H * d].view(T, H, d) for b in bigs)
+    la.backward(inp.q, inp.k, inp.v, inp.decay, inp.cu_seqlens, dout, dq=dq, dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    for b in bigs:
+        assert (b[:G] == 321.0).all() and (b[-G:] == 321.0).all()
+    ref = oracle.backward(inp.q, inp.k, inp.v, inp.decay, inp.cu_seqlens.cpu(), dout)
+    for x, r, name in zip((dq, dk, dv), ref, ("dq", "dk", "dv")):
+        assert_close(x, r, TOL_BF16, f"guarded {name}")

@@ -89,3 +89,18 @@ def test_snapshots_layer_sized():
         _, st = oracle.recurrent(sub(inp.q), sub(inp.k), sub(inp.v), inp.decay[heads],
                                  torch.tensor([0, P], dtype=torch.int32))
         assert_close(snaps[j, heads], st[0], TOL_BF16, f"layer snapshot {j}")
+
+
+def test_snapshots_many_sequences():
+    """150 sequences (more than the in-kernel length sort handles): every
+    CTA finds its sequence's first snapshot by counting those before it."""
+    g = torch.Generator().manual_seed(64)
+    lengths = torch.randint(0, 700, (150,), generator=g).tolist()
+    H, d, interval = 2, 128, 256
+    inp = wl.prefill_inputs(lengths, H, d, dtype=torch.bfloat16, seed=65, device="cuda")
+    out, fs, snaps = la.prefill_snapshots(inp.q, inp.k, inp.v, inp.decay, inp.cu_seqlens,
+                                          interval)
+    torch.cuda.synchronize()
+    assert snaps.shape[0] == sum(L // interval for L in lengths)
+    assert_close(snaps, prefix_states(inp, lengths, interval, None), TOL_BF16,
+                 "150 sequences snapshots")

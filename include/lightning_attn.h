@@ -234,7 +234,9 @@ la_status lightning_attn_decode(const void *q, const void *k, const void *v,
  *                         none of them equal to an input
  * workspace               caller-owned device memory, 256-byte aligned, of at
  *                         least lightning_attn_backward_workspace_bytes(...)
- *                         bytes; its contents are scratch (overwritten)
+ *                         bytes; its contents are scratch (overwritten).  Not
+ *                         used on the tensor-core path, where it may be NULL
+ *                         with workspace_bytes 0.
  * other arguments         as for lightning_attn_prefill.
  * Gradients with respect to decay, to a cached initial state or from a
  * final-state loss are not computed.
@@ -259,8 +261,10 @@ int64_t lightning_attn_backward_workspace_bytes(int32_t total_tokens, int32_t nu
  * must not call cudaMalloc because it can synchronise the device -- the
  * scratch comes from one fixed array of lightning_attn_backward_noalloc_max_bytes()
  * bytes (64 MiB) that every GPU loading the library holds until the process
- * exits.  Arguments and results are those of lightning_attn_backward; a call
- * whose lightning_attn_backward_workspace_bytes() exceeds the array returns
+ * exits.  Arguments and results are those of lightning_attn_backward.  On the
+ * tensor-core path (bf16, head_dim 128, chunk 0 or 128) no scratch is used
+ * and no size limit applies; otherwise a call whose
+ * lightning_attn_backward_workspace_bytes() exceeds the array returns
  * LA_ERR_INVALID_ARG before touching the GPU.  The first call on a device
  * looks up the array's device address (cudaGetSymbolAddress) with that
  * device current; make that first call before any stream capture.  The

@@ -203,7 +203,9 @@ def backward(q, k, v, decay, cu_seqlens, dout, *, chunk: int = 0, dq=None, dk=No
     """Gradients (dq, dk, dv) of sum_t dout_t . o_t for o = prefill(q, k, v,
     decay, cu_seqlens) (zero initial states).  Shapes and dtypes as in
     :func:`prefill`; ``workspace`` is a uint8 CUDA tensor of at least
-    :func:`backward_workspace_bytes` bytes (allocated here when None).
+    :func:`backward_workspace_bytes` bytes, needed on the CUDA-core path
+    only (allocated here when None); the tensor-core path (bf16, d = 128,
+    chunk 0 or 128) runs without one.
     """
     if q.dim() != 3:
         raise ValueError("q must be [T, H, d]")
@@ -221,15 +223,17 @@ def backward(q, k, v, decay, cu_seqlens, dout, *, chunk: int = 0, dq=None, dk=No
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(q) if dk is None else dk
     dv = torch.empty_like(q) if dv is None else dv
-    need = backward_workspace_bytes(T, H, d, q.dtype)
-    if workspace is None:
+    tensor_cores = q.dtype == torch.bfloat16 and d == 128 and int(chunk) in (0, 128)
+    if workspace is None and not tensor_cores:
+        need = backward_workspace_bytes(T, H, d, q.dtype)
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    ws_ptr = None if workspace is None else _dev(workspace, "workspace")
+    ws_bytes = 0 if workspace is None else int(workspace.numel() * workspace.element_size())
     st = load().lightning_attn_backward(
         _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(decay, "decay"),
         _dev(cu_seqlens, "cu_seqlens"), nseq, T, H, d, int(chunk), _dtype_code(q),
         _dev(dout, "dout"), _dev(dq, "dq"), _dev(dk, "dk"), _dev(dv, "dv"),
-        _dev(workspace, "workspace"), int(workspace.numel() * workspace.element_size()),
-        _stream_handle(stream))
+        ws_ptr, ws_bytes, _stream_handle(stream))
     _check(st, "lightning_attn_backward")
     return dq, dk, dv
 

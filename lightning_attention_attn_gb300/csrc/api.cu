@@ -319,9 +319,11 @@ la_status lightning_attn_backward(const void *q, const void *k, const void *v,
         return fail(LA_ERR_INVALID_ARG, "chunk must be 0, 16, 32, 64, 128 or 256 (got %d)", chunk);
     if (num_seqs == 0 || total_tokens == 0) return LA_OK;
     if (!cu_seqlens || !decay) return fail(LA_ERR_INVALID_ARG, "null decay or cu_seqlens");
-    const void *ptrs[] = {q, k, v, d_out, d_q, d_k, d_v, workspace};
+    // the tensor-core path computes dk and dv in place and needs no workspace
+    const bool tc = dtype == LA_DTYPE_BF16 && head_dim == 128 && (chunk == 0 || chunk == 128);
+    const void *ptrs[] = {q, k, v, d_out, d_q, d_k, d_v};
     for (const void *p : ptrs)
-        if (!p) return fail(LA_ERR_INVALID_ARG, "null tensor or workspace pointer");
+        if (!p) return fail(LA_ERR_INVALID_ARG, "null tensor pointer");
     for (const void *p : ptrs)
         if (!aligned16(p)) return fail(LA_ERR_INVALID_ARG, "every pointer must be 16-byte aligned");
     if (!aligned16(decay) || !aligned16(cu_seqlens))
@@ -338,11 +340,14 @@ la_status lightning_attn_backward(const void *q, const void *k, const void *v,
             if (outs[i] == outs[j]) return fail(LA_ERR_INVALID_ARG, "two gradients share an array");
     }
     const size_t slot = backward_slot_bytes(total_tokens, num_heads, head_dim, dtype);
-    if (workspace_bytes < 0 || (size_t)workspace_bytes < 3 * slot)
-        return fail(LA_ERR_INVALID_ARG, "workspace too small: %lld bytes, %zu needed",
-                    (long long)workspace_bytes, 3 * slot);
-    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-        return fail(LA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    if (!tc) {
+        if (!workspace) return fail(LA_ERR_INVALID_ARG, "null workspace (CUDA-core path)");
+        if (workspace_bytes < 0 || (size_t)workspace_bytes < 3 * slot)
+            return fail(LA_ERR_INVALID_ARG, "workspace too small: %lld bytes, %zu needed",
+                        (long long)workspace_bytes, 3 * slot);
+        if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+            return fail(LA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    }
 
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     char *ws = static_cast<char *>(workspace);
@@ -368,7 +373,7 @@ la_status lightning_attn_backward(const void *q, const void *k, const void *v,
     // dq_t = sum_{u<=t} lambda^(t-u) (dout_t . v_u) k_u: the forward form
     // with (q, k, v) -> (dout, v, k)
     if ((r = fwd(d_out, v, k, d_q, false)) != LA_OK) return r;
-    if (dtype == LA_DTYPE_BF16 && head_dim == 128 && (chunk == 0 || chunk == 128)) {
+    if (tc) {
         // tensor-core path: dv_u = sum_{t>=u} lambda^(t-u) (q_t . k_u) dout_t and
         // dk_u = sum_{t>=u} lambda^(t-u) (dout_t . v_u) q_t are anti-causal
         // forms, computed in place (the workspace is not touched)

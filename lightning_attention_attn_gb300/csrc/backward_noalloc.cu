@@ -7,7 +7,8 @@
 // cudaMalloc calls, or a serving or training loop that must not call
 // cudaMalloc in its steady state because cudaMalloc can synchronise the
 // device.  Such callers still pass their inputs and outputs; only the
-// scratch of the time-reversed copies comes from here.
+// scratch of the time-reversed copies of the CUDA-core path comes from here
+// (the tensor-core path needs none).
 //
 // The array lives in device memory of every GPU that loads the library, from
 // module load until the process exits.  Its address is looked up once per
@@ -67,6 +68,12 @@ extern "C" la_status lightning_attn_backward_noalloc(
     const void *q, const void *k, const void *v, const float *decay, const int32_t *cu_seqlens,
     int32_t num_seqs, int32_t total_tokens, int32_t num_heads, int32_t head_dim, int32_t chunk,
     la_dtype dtype, const void *d_out, void *d_q, void *d_k, void *d_v, void *stream) {
+    // the tensor-core path (bf16, head_dim 128, chunk 0 or 128) uses no
+    // scratch: no size limit applies
+    if (dtype == LA_DTYPE_BF16 && head_dim == 128 && (chunk == 0 || chunk == 128))
+        return lightning_attn_backward(q, k, v, decay, cu_seqlens, num_seqs, total_tokens,
+                                       num_heads, head_dim, chunk, dtype, d_out, d_q, d_k, d_v,
+                                       nullptr, 0, stream);
     const int64_t need =
         lightning_attn_backward_workspace_bytes(total_tokens, num_heads, head_dim, dtype);
     if (need > (int64_t)la::kScratchBytes) {

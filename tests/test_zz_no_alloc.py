@@ -27,6 +27,7 @@ def lib():
     lib.lightning_attn_backward_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                                     ctypes.c_int, vp, vp, vp, vp, vp]
     lib.lightning_attn_backward_noalloc.restype = ctypes.c_int
+    lib.lightning_attn_backward_noalloc_max_bytes.restype = ctypes.c_int64
     return lib
 
 
@@ -56,3 +57,20 @@ def test_noalloc_backward_matches_workspace_backward(lib, dtype, chunk, tol):
         torch.cuda.synchronize()
         for x, w, name in zip(got, want, ("dq", "dk", "dv")):
             assert_close(x, w, tol, f"no-alloc call {call + 1} {name}")
+
+
+def test_noalloc_tensor_core_path_has_no_size_limit(lib):
+    """bf16, d = 128: the anti-causal launches need no scratch, so a problem
+    whose workspace would exceed the built-in array is still accepted."""
+    lengths = [1500, 700]
+    inp = wl.prefill_inputs(lengths, 64, 128, dtype=torch.bfloat16, seed=33, device="cuda")
+    T, H, d = inp.q.shape
+    assert la.backward_workspace_bytes(T, H, d) > lib.lightning_attn_backward_noalloc_max_bytes()
+    g = torch.Generator(device="cuda")
+    g.manual_seed(34)
+    dout = torch.randn(inp.q.shape, generator=g, device="cuda").to(torch.bfloat16)
+    got = noalloc_backward(lib, inp, dout, 0)
+    want = la.backward(inp.q, inp.k, inp.v, inp.decay, inp.cu_seqlens, dout)
+    torch.cuda.synchronize()
+    for x, w, name in zip(got, want, ("dq", "dk", "dv")):
+        assert torch.equal(x, w), name

@@ -360,11 +360,19 @@ prefill_simt_kernel(const T *__restrict__ q, const T *__restrict__ k,
                 if (l > j) acc[r][c] = 0.f;
                 else if constexpr (!CW) acc[r][c] *= sm.pw[j - l];
             }
-        __syncthreads();  // every read of K_i^T is done
+        __syncthreads();  // every read of K_i^T and Q_i^T for the scores is done
         if (ks == 0) {
 #pragma unroll
             for (int c = 0; c < 4; ++c)
                 store4(&pT[sl0 + c][sj0], acc[0][c], acc[1][c], acc[2][c], acc[3][c]);
+        }
+        if constexpr (CW) {
+            // Q_i^T is only read by the inter-chunk product from here on:
+            // scale it in place, q_j[i] -> q_j[i] lambda_i^(j+1)
+            for (int e = tid; e < D * B; e += kThreads) {
+                const int i = e / B, j = e % B;
+                sm.qT[i][j] *= sm.wz[i][5 + j];
+            }
         }
         __syncthreads();
 
@@ -396,33 +404,8 @@ prefill_simt_kernel(const T *__restrict__ q, const T *__restrict__ k,
                             for (int r = 0; r < TJ; ++r) fma_row4(oi[r], st.pa[u][r], st.vb[u]);
                     });
             }
-            if constexpr (CW) {
-                // q_j[i] lambda_i^(j+1) = (q_j[i] lambda_i^j) lambda_i
-                struct St { float qa[2][TJ], wq[2][TJ], kb[2][4], l1[2]; };
-                pipelined<St, 2>(
-                    D,
-                    [&](St &st, int i) {
-#pragma unroll
-                        for (int u = 0; u < 2; ++u) {
-                            lds<TJ>(st.qa[u], &sm.qT[i + u][jo]);
-                            lds<TJ>(st.wq[u], &sm.wz[i + u][4 + jo]);
-                            lds<4>(st.kb[u], &sm.kv[i + u][n0]);
-                            st.l1[u] = sm.wz[i + u][5];
-                        }
-                    },
-                    [&](const St &st) {
-#pragma unroll
-                        for (int u = 0; u < 2; ++u) {
-                            float qw[TJ], kl[4];
-#pragma unroll
-                            for (int r = 0; r < TJ; ++r) qw[r] = st.qa[u][r] * st.wq[u][r];
-#pragma unroll
-                            for (int c = 0; c < 4; ++c) kl[c] = st.kb[u][c] * st.l1[u];
-#pragma unroll
-                            for (int r = 0; r < TJ; ++r) fma_row4(oe[r], qw[r], kl);
-                        }
-                    });
-            } else {
+            {
+                // Q_i KV_{i-1} (with channel-wise decay Q_i already carries lambda_i^(j+1))
                 struct St { float qa[2][TJ], kb[2][4]; };
                 pipelined<St, 2>(
                     D,

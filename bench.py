@@ -430,6 +430,28 @@ def run_ours(args, ws, rank, local):
                            "unit": "GB/s", "frac": round(dgbs / pk["hbm"], 4),
                            "traffic": ncu_traffic("decode_kernel", DECODE_KERNEL_SRC),
                            "kernel": "decode_kernel", "alg_bytes_per_launch": dbytes}}
+    # the channel-wise decay step on the same batch (one lambda per head and
+    # key channel, read per state row): 200 consecutive steps
+    lam_cw = dinp.decay[:, None].repeat(1, dcfg["head_dim"]).contiguous()
+    lam_cw = lam_cw * (1.0 - 0.01 * torch.linspace(0, 1, dcfg["head_dim"], device=dev))[None, :]
+    csteps = 200
+    for t in range(5):
+        la.decode_channel_decay(dinp.q[t], dinp.k[t], dinp.v[t], lam_cw, dinp.state, out=dout,
+                                stream=stream)
+    torch.cuda.synchronize()
+    d0.record(stream)
+    for t in range(csteps):
+        la.decode_channel_decay(dinp.q[t], dinp.k[t], dinp.v[t], lam_cw, dinp.state, out=dout,
+                                stream=stream)
+    d1.record(stream)
+    torch.cuda.synchronize()
+    cms = d0.elapsed_time(d1) / csteps
+    cgbs = dbytes / (cms / 1e3) / 1e9
+    decode["channel_decay"] = {"ms_per_step": round(cms, 5), "steps": csteps,
+                               "roofline": {"bound": "hbm", "achieved": round(cgbs, 1),
+                                            "peak": pk["hbm"], "unit": "GB/s",
+                                            "frac": round(cgbs / pk["hbm"], 4)}}
+    la.device_status(stream)
     del dinp
 
     # ---------------- backward on the same 8K-token layer (training step of
@@ -438,12 +460,10 @@ def run_ours(args, ws, rank, local):
     g.manual_seed(1)
     dout = torch.randn(inp.q.shape, generator=g, device=dev).to(torch.bfloat16)
     dq, dk, dv = (torch.empty_like(inp.q) for _ in range(3))
-    bws = torch.empty(la.backward_workspace_bytes(T, H, d, torch.bfloat16), dtype=torch.uint8,
-                      device=dev)
 
-    def bstep():
+    def bstep():  # the tensor-core path needs no workspace
         la.backward(inp.q, inp.k, inp.v, inp.decay, inp.cu_seqlens, dout, dq=dq, dk=dk, dv=dv,
-                    workspace=bws, stream=stream)
+                    stream=stream)
 
     for _ in range(3):
         bstep()
@@ -468,7 +488,7 @@ def run_ours(args, ws, rank, local):
                              "note": "algorithmic bytes of the gradients; the implementation "
                                      "runs 3 tensor-core launches, each reading 3 inputs and "
                                      "writing 1 (12 x T x H x d x 2 bytes moved)"}}
-    del dout, dq, dk, dv, bws
+    del dout, dq, dk, dv
 
     # ---------------- mixed serving step (decode + prefill on two streams):
     # every sequence continues from a cached state; a few have several new

@@ -47,7 +47,7 @@ extern "C" {
 typedef enum la_status {
     LA_OK = 0,
     LA_ERR_INVALID_ARG = 1,   /* null / misaligned pointer, bad size or dtype */
-    LA_ERR_UNSUPPORTED = 2,   /* valid request this build has no kernel for   */
+    LA_ERR_UNSUPPORTED = 2,   /* valid request the library has no kernel for */
     LA_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed          */
     LA_ERR_TIMEOUT = 4        /* reserved: a bounded device-side wait gave up  */
 } la_status;

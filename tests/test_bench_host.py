@@ -59,7 +59,7 @@ def test_single_rank_helpers_are_identity():
     assert bench.sum_over_ranks(7.0, 1) == 7.0
 
 
-def test_algorithmic_model_matches_survey_numbers():
+def test_algorithmic_model_matches_the_hand_counts():
     byts, flops = bench.prefill_alg(8192, 64, 128, 128, 1)
     assert byts == 541_065_216                     # 8d per token-head + H d^2 4
     assert flops == 8192 * 64 * (4 * 128 * 128 + 2 * 129 * 128)

@@ -1,12 +1,15 @@
 // CUDA-core (FFMA) chunkwise lightning-attention prefill.
 //
 // This is the fp32 path (tensor-core tf32 would not meet a 1e-4 relative
-// bound) and the path for head_dim 64.  One CTA owns one (sequence, head)
-// and walks its chunks in order, keeping the d x d state in shared memory:
+// bound), the path for head_dim 64 and chunks 16-64, and the channel-wise
+// decay.  One CTA owns one (sequence, head, 64-column value slice) and walks
+// its chunks in order, keeping its d x 64 slice of the state in shared memory:
 //   MiniMax-01 report (CSDN translation) §2.2.1 -- intra-block left product
 //   [(Q_i K_i^T) (.) M] V_i, inter-block right product Q_i KV_{i-1} and the
 //   recursive state update KV_i = lambda^{B_i} KV_{i-1} + (Lambda_K K_i)^T V_i,
 //   with the decay values (§3.3.1) computed in the kernel.
+// With channel-wise decay (K3 report reading notes, gated DeltaNet) every
+// lambda becomes lambda_i of key channel i.
 // A sequence may continue from a cached state (initial_state): KV_{-1} = S0.
 // Exponents of lambda are never negative (lambda^(j-l) for j >= l,
 // lambda^(j+1), lambda^(B_i-1-l), lambda^(B_i)), so no factor can overflow;
@@ -99,8 +102,9 @@ struct SimtSmem {
     float kv[D][kDV];                 // the CTA's value slice of the state KV
     float pw[B + 4];                  // lambda^e, e = 0..B (scalar decay)
     // channel-wise decay: wz[i][4 + e] = lambda_i^e for e = 0..B, zero elsewhere,
-    // so that an 8-wide window starting at 4 (j - l) - 4 below a 4 x 4 tile
-    // reads zero for every l > j
+    // so that the 4 x 4 score tile at tile distance d = (j0 - l0) / 4 finds
+    // lambda_i^(4d + r - c) at element 4 + r - c of the window wz[i][4d .. 4d + 7]
+    // (zero for r < c on the diagonal tile)
     float wz[CW ? D : 1][CW ? WP : 1];
     // the same powers exponent-major, wk[e][i] = lambda_i^e (e = 0..B), for
     // the staging of K_s, whose lanes walk consecutive channels

@@ -297,8 +297,8 @@ def run_ours(args, ws, rank, local):
     # ---------------- the other prefill workloads of the benchmark set:
     # 128K-token context (chunk 128 on tensor cores; chunk 64 on the
     # CUDA-core kernel timed once) and the 16-sequence varlen batch
-    def time_prefill(lengths, chunk, reps):
-        pin = wl.prefill_inputs(lengths, H, d, dtype=torch.bfloat16, seed=0, device=dev)
+    def time_prefill(lengths, chunk, reps, dtype=torch.bfloat16):
+        pin = wl.prefill_inputs(lengths, H, d, dtype=dtype, seed=0, device=dev)
         pout = torch.empty_like(pin.q)
         pfs = torch.empty((len(lengths), H, d, d), dtype=torch.float32, device=dev)
 
@@ -317,14 +317,18 @@ def run_ours(args, ws, rank, local):
         la.device_status(stream)
         ms = a0.elapsed_time(a1) / reps
         Tn = sum(lengths)
-        if chunk not in (0, 128):
+        if dtype == torch.float32:  # the CUDA-core (FFMA) kernel
             byts, flops = prefill_alg(Tn, H, d, chunk, len(lengths))
+            byts += Tn * H * d * 8  # fp32 inputs and output: twice the bf16 bytes
             return {"ms_per_launch": round(ms, 4), "tokens_per_s": round(Tn / (ms / 1e3), 1),
-                    "tokens": Tn, "chunk": chunk, "kernel": "prefill_simt_kernel (FFMA)",
+                    "tokens": Tn, "chunk": chunk, "dtype": "f32",
+                    "kernel": "prefill_simt_kernel (FFMA)",
                     "roofline": cuda_core_roofline(flops, byts, ms, pk, sms)}
-        byts, flops = prefill_alg(Tn, H, d, 128, len(lengths))
+        B = chunk if chunk else 128
+        byts, flops = prefill_alg(Tn, H, d, B, len(lengths))
         return {"ms_per_launch": round(ms, 4), "tokens_per_s": round(Tn / (ms / 1e3), 1),
-                "tokens": Tn, "chunk": chunk,
+                "tokens": Tn, "chunk": chunk, "kernel": "prefill_tc_kernel",
+                "tensor_tiles_per_block": 128 // B,
                 "roofline": {"bound": "hbm", "alg_bytes": byts,
                              "achieved": round(byts / (ms / 1e3) / 1e9, 1), "peak": pk["hbm"],
                              "unit": "GB/s", "frac": round(byts / (ms / 1e3) / 1e9 / pk["hbm"], 4)}}
@@ -390,11 +394,13 @@ def run_ours(args, ws, rank, local):
     more = {"prefill_8k_channel_decay": time_channel_decay([8192], 10),
             "prefill_8k_snapshots_every_1024": time_snapshots([8192], 1024, 10),
             "prefill_8k_snapshots_every_128": time_snapshots([8192], 128, 10),
-            "prefill_8k_chunk64_cuda_cores": time_prefill([8192], 64, 10),
+            "prefill_8k_chunk64": time_prefill([8192], 64, 10),
+            "prefill_8k_chunk32": time_prefill([8192], 32, 10),
+            "prefill_8k_fp32_cuda_cores": time_prefill([8192], 64, 5, torch.float32),
             "prefill_128k": time_prefill([131072], 0, 5),
-            "prefill_128k_chunk64_cuda_cores": time_prefill([131072], 64, 3),
-            "prefill_128k_chunk256": "not run: the tensor-core block is 128 (chunk 256 returns "
-                                     "LA_ERR_UNSUPPORTED)",
+            "prefill_128k_chunk64": time_prefill([131072], 64, 3),
+            "prefill_128k_chunk256": "not run: the tensor-core tile is 128 tokens (chunk 256 "
+                                     "returns LA_ERR_UNSUPPORTED)",
             "varlen_16": time_prefill(wl.varlen_lengths().tolist(), 0, 5)}
     torch.cuda.empty_cache()
 
@@ -688,13 +694,15 @@ def run_only(args):
         fs = torch.empty((1, cfg["num_heads"], 128, 128), device="cuda")
         for _ in range(args.warmup + args.steps):
             la.prefill(inp.q, inp.k, inp.v, inp.decay, inp.cu_seqlens, out=out, final_state=fs)
-    elif args.only in ("channel_decay", "prefill_chunk64"):
-        # the CUDA-core kernel on the 8K-token layer: per-channel decay
-        # (lambda_h scaled by 1 - 0.01 i / (d - 1) for key channel i), or the
-        # scalar decay at chunk 64
+    elif args.only in ("channel_decay", "prefill_chunk64", "prefill_fp32"):
+        # the 8K-token layer: per-channel decay on the CUDA-core kernel
+        # (lambda_h scaled by 1 - 0.01 i / (d - 1) for key channel i), the
+        # scalar decay with 64-token blocks on the tensor cores, or fp32
+        # inputs (chunk 64) on the CUDA-core kernel
         cfg = wl.PREFILL_8K
         inp = wl.prefill_inputs(cfg["lengths"], cfg["num_heads"], cfg["head_dim"],
-                                dtype=torch.bfloat16, seed=0, device="cuda")
+                                dtype=torch.float32 if args.only == "prefill_fp32"
+                                else torch.bfloat16, seed=0, device="cuda")
         d = cfg["head_dim"]
         lam_cw = inp.decay[:, None].repeat(1, d).contiguous()
         lam_cw = lam_cw * (1.0 - 0.01 * torch.linspace(0, 1, d, device="cuda"))[None, :]
@@ -768,7 +776,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--only", choices=["prefill", "decode", "backward", "channel_decay",
-                                       "prefill_chunk64"], default=None,
+                                       "prefill_chunk64", "prefill_fp32"], default=None,
                     help="profiling aid: run just W + K launches of one kernel on its "
                          "workload and print nothing else")
     args = ap.parse_args(argv)

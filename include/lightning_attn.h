@@ -77,11 +77,15 @@ typedef enum la_dtype {
  * num_heads    >= 1.
  * head_dim     64 or 128.
  * chunk        block size B: 0 picks the default for the path
- *              (128 on the tensor-core path, 64 otherwise); the tensor-core
- *              path (bf16, head_dim 128) takes 128; the fp32 / CUDA-core path
- *              takes 16, 32 or 64.  The result does not depend on B beyond
- *              rounding (K3 report reading notes, CP for linear attention:
- *              any chunk split is mathematically equivalent).
+ *              (128 on the tensor-core path, 64 otherwise).  The
+ *              tensor-core path (bf16, head_dim 128) takes 16, 32, 64 or 128
+ *              (its tiles are 128 tokens; a smaller block runs as masked
+ *              tiles advancing B tokens, at 128 / B times the tensor-core
+ *              work); the fp32 / head_dim 64 CUDA-core path takes 16, 32 or
+ *              64; 256 has no kernel (LA_ERR_UNSUPPORTED).  The result does
+ *              not depend on B beyond rounding (K3 report reading notes, CP
+ *              for linear attention: any chunk split is mathematically
+ *              equivalent).
  * dtype        LA_DTYPE_BF16 or LA_DTYPE_FP32.
  * out          [total_tokens, num_heads, head_dim], dtype `dtype`: o_t.
  * final_state  nullable; [num_seqs, num_heads, head_dim, head_dim] fp32:
@@ -134,9 +138,9 @@ la_status lightning_attn_prefill_with_state(const void *q, const void *k, const 
  * lightning_attn_prefill_with_state, plus
  *
  * snapshot_interval  tokens per block, > 0 and a multiple of the block the
- *                    call computes with: 128 on the tensor-core path (bf16,
- *                    head_dim 128, chunk 0 or 128), else the chunk (64 for
- *                    chunk 0); LA_ERR_INVALID_ARG otherwise.
+ *                    call computes with (the chunk; for chunk 0, 128 on the
+ *                    tensor-core path -- bf16, head_dim 128 -- and 64
+ *                    otherwise); LA_ERR_INVALID_ARG otherwise.
  * snapshots          [N, num_heads, head_dim, head_dim] fp32 device array,
  *                    16-byte aligned, N = lightning_attn_snapshot_count(...)
  *                    of the same cu_seqlens (host copy).  Sequence s owns
@@ -223,7 +227,7 @@ la_status lightning_attn_decode(const void *q, const void *k, const void *v,
  *
  * per sequence and head.  dq is the forward form applied to (dout, v, k);
  * dk and dv are anti-causal forms (sums over t >= u).  On the tensor-core
- * path (bf16, head_dim 128, chunk 0/128) the call makes three launches of
+ * path (bf16, head_dim 128, chunk 0-128) the call makes three launches of
  * the prefill kernel, one causal and two anti-causal, and does not touch
  * `workspace`; on the CUDA-core path it runs the forward form in reversed
  * time, with four time-reversal copies through `workspace`.  Same dtype /
@@ -262,7 +266,7 @@ int64_t lightning_attn_backward_workspace_bytes(int32_t total_tokens, int32_t nu
  * scratch comes from one fixed array of lightning_attn_backward_noalloc_max_bytes()
  * bytes (64 MiB) that every GPU loading the library holds until the process
  * exits.  Arguments and results are those of lightning_attn_backward.  On the
- * tensor-core path (bf16, head_dim 128, chunk 0 or 128) no scratch is used
+ * tensor-core path (bf16, head_dim 128, chunk 0-128) no scratch is used
  * and no size limit applies; otherwise a call whose
  * lightning_attn_backward_workspace_bytes() exceeds the array returns
  * LA_ERR_INVALID_ARG before touching the GPU.  The first call on a device

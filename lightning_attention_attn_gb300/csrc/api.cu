@@ -40,13 +40,14 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // Runs the forward kernel that serves (dtype, head_dim, chunk); arguments
 // already validated.
 la_status run_prefill(const la::PrefillArgs &a, la_dtype dtype) {
-    const bool tc = dtype == LA_DTYPE_BF16 && a.head_dim == 128 && (a.chunk == 0 || a.chunk == 128);
+    const bool tc = la::uses_tensor_cores(dtype == LA_DTYPE_BF16, a.head_dim, a.chunk);
     if (tc) return from_cuda(la::prefill_tc_bf16(a), "prefill (tcgen05)");
     if (a.anti_causal)
         return fail(LA_ERR_UNSUPPORTED, "the anti-causal form runs on the tensor-core path only");
-    if (a.chunk == 128 || a.chunk == 256)
-        return fail(LA_ERR_UNSUPPORTED,
-                    "chunk %d needs the tensor-core path (bf16, head_dim 128)", a.chunk);
+    if (a.chunk == 256)
+        return fail(LA_ERR_UNSUPPORTED, "chunk 256: no kernel (the tensor-core tile is 128 tokens)");
+    if (a.chunk == 128)
+        return fail(LA_ERR_UNSUPPORTED, "chunk 128 needs the tensor-core path (bf16, head_dim 128)");
     if (dtype == LA_DTYPE_FP32) return from_cuda(la::prefill_simt_f32(a), "prefill (fp32)");
     return from_cuda(la::prefill_simt_bf16(a), "prefill (bf16, CUDA cores)");
 }
@@ -182,11 +183,12 @@ la_status lightning_attn_prefill_snapshots(const void *q, const void *k, const v
     if (!snapshots || !aligned16(snapshots))
         return fail(LA_ERR_INVALID_ARG, "snapshots must be a 16-byte aligned device array");
     // the kernel that serves the call and its block
-    const bool tc = dtype == LA_DTYPE_BF16 && head_dim == 128 && (chunk == 0 || chunk == 128);
-    const int block = tc ? 128 : (chunk == 0 ? 64 : chunk);
-    if (!tc && (chunk == 128 || chunk == 256))
-        return fail(LA_ERR_UNSUPPORTED,
-                    "chunk %d needs the tensor-core path (bf16, head_dim 128)", chunk);
+    const bool tc = la::uses_tensor_cores(dtype == LA_DTYPE_BF16, head_dim, chunk);
+    const int block = chunk != 0 ? chunk : tc ? 128 : 64;
+    if (chunk == 256)
+        return fail(LA_ERR_UNSUPPORTED, "chunk 256: no kernel (the tensor-core tile is 128 tokens)");
+    if (!tc && chunk == 128)
+        return fail(LA_ERR_UNSUPPORTED, "chunk 128 needs the tensor-core path (bf16, head_dim 128)");
     if (snapshot_interval % block != 0)
         return fail(LA_ERR_INVALID_ARG,
                     "snapshot_interval %d is not a multiple of the block (%d tokens) this "
@@ -320,7 +322,7 @@ la_status lightning_attn_backward(const void *q, const void *k, const void *v,
     if (num_seqs == 0 || total_tokens == 0) return LA_OK;
     if (!cu_seqlens || !decay) return fail(LA_ERR_INVALID_ARG, "null decay or cu_seqlens");
     // the tensor-core path computes dk and dv in place and needs no workspace
-    const bool tc = dtype == LA_DTYPE_BF16 && head_dim == 128 && (chunk == 0 || chunk == 128);
+    const bool tc = la::uses_tensor_cores(dtype == LA_DTYPE_BF16, head_dim, chunk);
     const void *ptrs[] = {q, k, v, d_out, d_q, d_k, d_v};
     for (const void *p : ptrs)
         if (!p) return fail(LA_ERR_INVALID_ARG, "null tensor pointer");

@@ -68,9 +68,9 @@ extern "C" la_status lightning_attn_backward_noalloc(
     const void *q, const void *k, const void *v, const float *decay, const int32_t *cu_seqlens,
     int32_t num_seqs, int32_t total_tokens, int32_t num_heads, int32_t head_dim, int32_t chunk,
     la_dtype dtype, const void *d_out, void *d_q, void *d_k, void *d_v, void *stream) {
-    // the tensor-core path (bf16, head_dim 128, chunk 0 or 128) uses no
+    // the tensor-core path (bf16, head_dim 128, block size 16-128) uses no
     // scratch: no size limit applies
-    if (dtype == LA_DTYPE_BF16 && head_dim == 128 && (chunk == 0 || chunk == 128))
+    if (la::uses_tensor_cores(dtype == LA_DTYPE_BF16, head_dim, chunk))
         return lightning_attn_backward(q, k, v, decay, cu_seqlens, num_seqs, total_tokens,
                                        num_heads, head_dim, chunk, dtype, d_out, d_q, d_k, d_v,
                                        nullptr, 0, stream);

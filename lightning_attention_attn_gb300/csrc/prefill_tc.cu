@@ -198,7 +198,11 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 // sequence (a multiple of B) is also written to `snapshots` (per-block
 // prefix cache, K3 report notes); sequence s's snapshots start at index
 // sum_{s' < s} floor(L_s' / snap_interval).
-template <bool kAnti, bool kSnap>
+// kCS: the block size B of the method (128, 64, 32 or 16).  Tiles are always
+// 128 rows; a block of B < 128 tokens is a tile whose rows past B are masked
+// exactly like the short last block of a sequence, and the next block's tile
+// starts B tokens later (128 / B times the tensor-core work per token).
+template <bool kAnti, bool kSnap, int kCS>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -221,11 +225,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     t1 = min(max(t1, t0), T);
     const int L = t1 - t0;
     if (L < min_len) return;  // a mixed step's decode launch owns this sequence
-    const int nch = (L + BC - 1) / BC;
+    static_assert(kCS == 128 || kCS == 64 || kCS == 32 || kCS == 16, "block size");
+    const int nch = (L + kCS - 1) / kCS;
     // chunk processed at step i, and the length of chunk c (only the last
     // chunk of a sequence may be short)
     auto chunk_of = [&](int i) { return kAnti ? nch - 1 - i : i; };
-    auto len_of = [&](int c) { return min(BC, L - c * BC); };
+    auto len_of = [&](int c) { return min(kCS, L - c * kCS); };
     using R = Roles<kAnti>;
     const float lam = __ldg(decay + h);
     // A sequence may continue from a cached state S0 (prefix KV cache,
@@ -317,7 +322,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             if (elect_one()) {
                 mbar_arrive_expect_tx(bar(cs.full_v[st]), kHalf);
                 tma_load_2d(vslot(st), &tmV, bar(cs.full_v[st]), h * D + vs * DV,
-                            t0 + chunk_of(c) * BC);
+                            t0 + chunk_of(c) * kCS);
             }
             __syncwarp();
             ++nv;
@@ -617,7 +622,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             if (!mbar_wait(bar(cs.empty_q[st]), ((c >> 1) & 1) ^ 1, abort_flag, kTimeoutNs))
                 return false;
             mbar_arrive_expect_tx(bar(cs.full_q[st]), 2 * kHalf);
-            const int row = t0 + chunk_of(c) * BC;
+            const int row = t0 + chunk_of(c) * kCS;
             tma_load_2d(qslot(st), &tmQ, bar(cs.full_q[st]), h * D, row);
             tma_load_2d(qslot(st) + kHalf, &tmQ, bar(cs.full_q[st]), h * D + 64, row);
             ++nq;
@@ -628,7 +633,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             if (!mbar_wait(bar(cs.empty_k[st]), ((c >> 1) & 1) ^ 1, abort_flag, kTimeoutNs))
                 return false;
             mbar_arrive_expect_tx(bar(cs.full_k[st]), 2 * kHalf);
-            const int row = t0 + chunk_of(c) * BC;
+            const int row = t0 + chunk_of(c) * kCS;
             tma_load_2d(kslot(st), &tmK, bar(cs.full_k[st]), h * D, row);
             tma_load_2d(kslot(st) + kHalf, &tmK, bar(cs.full_k[st]), h * D + 64, row);
             ++nk;
@@ -782,7 +787,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             }
             if constexpr (kSnap) {
                 // the state after the first (i + 1) B tokens closes a block
-                const int end = (i + 1) * BC;
+                const int end = (i + 1) * kCS;
                 if (end <= L && end % snap_interval == 0) {
                     float4 *dst = reinterpret_cast<float4 *>(
                         snapshots +
@@ -839,9 +844,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
                              ld_shared_f32(vscale_s + 4u * (uint32_t)(i & 3));
             // lambda^(r+1) Q KV_{i-1}; anti-causal: lambda^(B-r) Q G_{c+1}
             // (G is zero before the first step, when chunk c may be short)
-            const float qf = kAnti ? pw(BC - r) : pw(r + 1);
+            const float qf = kAnti ? pw(kCS - r) : pw(r + 1);
             const float2 s12 = make_float2(s1, s1), qf2 = make_float2(qf, qf);
-            const long orow_t = (long)(t0 + chunk_of(i) * BC + r);
+            const long orow_t = (long)(t0 + chunk_of(i) * kCS + r);
             uint4 *orow = reinterpret_cast<uint4 *>(out + (orow_t * H + h) * D +
                                                     vs * DV);
 #pragma unroll
@@ -1042,10 +1047,21 @@ __global__ void wait_timeout_selftest_kernel(uint64_t timeout_ns) {
         atomicOr(&g_tc_error, 1u);
 }
 
+using TcKernel = decltype(&prefill_tc_kernel<false, false, BC>);
+
+template <int CS>
+TcKernel pick_kernel(bool anti, bool snap) {
+    return anti ? prefill_tc_kernel<true, false, CS>
+           : snap ? prefill_tc_kernel<false, true, CS>
+                  : prefill_tc_kernel<false, false, CS>;
+}
+
 }  // namespace
 
 cudaError_t prefill_tc_bf16(const PrefillArgs &a) {
-    if (a.head_dim != D || (a.chunk != 0 && a.chunk != BC)) return cudaErrorNotSupported;
+    const int cs = a.chunk == 0 ? BC : a.chunk;  // the method's block size
+    if (a.head_dim != D || (cs != 128 && cs != 64 && cs != 32 && cs != 16))
+        return cudaErrorNotSupported;
     // rows are written in place; the anti-causal kernel starts from a zero state
     if (a.reverse_out || (a.anti_causal && a.initial_state)) return cudaErrorNotSupported;
     CUtensorMap mq, mk, mv, mo;
@@ -1058,14 +1074,16 @@ cudaError_t prefill_tc_bf16(const PrefillArgs &a) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const bool snap = a.snapshots != nullptr;
-    if (snap && (a.anti_causal || a.snapshot_interval <= 0 || a.snapshot_interval % BC != 0))
+    if (snap && (a.anti_causal || a.snapshot_interval <= 0 || a.snapshot_interval % cs != 0))
         return cudaErrorNotSupported;
-    auto kern = a.anti_causal ? prefill_tc_kernel<true, false>
-                : snap        ? prefill_tc_kernel<false, true>
-                              : prefill_tc_kernel<false, false>;
-    // bit 0: causal kernel, bit 1: anti-causal, bit 2: causal with snapshots
+    const int csi = cs == 128 ? 0 : cs == 64 ? 1 : cs == 32 ? 2 : 3;
+    const TcKernel kern = csi == 0   ? pick_kernel<128>(a.anti_causal, snap)
+                          : csi == 1 ? pick_kernel<64>(a.anti_causal, snap)
+                          : csi == 2 ? pick_kernel<32>(a.anti_causal, snap)
+                                     : pick_kernel<16>(a.anti_causal, snap);
+    // one bit per instantiation: (causal, anti-causal, causal with snapshots) x block size
     static int attr_set_for[64] = {0};
-    const int bit = a.anti_causal ? 2 : snap ? 4 : 1;
+    const int bit = 1 << ((a.anti_causal ? 1 : snap ? 2 : 0) * 4 + csi);
     if (dev < 64 && !(attr_set_for[dev] & bit)) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)kSmemBytes);

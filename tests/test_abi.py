@@ -177,10 +177,10 @@ def _backward(lib, **kw):
 
 
 @pytest.mark.parametrize("kw, status", [
-    # the workspace is checked on the CUDA-core path (chunk 64), which uses it
-    (dict(ws=None, chunk=64), la.LA_ERR_INVALID_ARG),
-    (dict(wsb=100, chunk=64), la.LA_ERR_INVALID_ARG),       # workspace too small
-    (dict(ws=W + 16, chunk=64), la.LA_ERR_INVALID_ARG),     # workspace not 256-aligned
+    # the workspace is checked on the CUDA-core path (fp32), which uses it
+    (dict(ws=None, dtype=la.LA_DTYPE_FP32), la.LA_ERR_INVALID_ARG),
+    (dict(wsb=100, dtype=la.LA_DTYPE_FP32), la.LA_ERR_INVALID_ARG),    # workspace too small
+    (dict(ws=W + 16, dtype=la.LA_DTYPE_FP32), la.LA_ERR_INVALID_ARG),  # not 256-aligned
     (dict(ws=None, dq=A), la.LA_ERR_INVALID_ARG),           # tensor-core path, no workspace:
                                                             # the other checks still apply
     (dict(dq=A), la.LA_ERR_INVALID_ARG),                    # gradient aliases q
@@ -202,9 +202,9 @@ def test_backward_noalloc_rejects_sizes_beyond_its_array(lib):
     lib.lightning_attn_backward_noalloc_max_bytes.restype = ctypes.c_int64
     cap = lib.lightning_attn_backward_noalloc_max_bytes()
     assert cap == 64 << 20
-    # chunk 64: the CUDA-core path, whose time reversals need the scratch
-    T = cap // (3 * 64 * 128 * 2) + 1  # one token more than the array holds (bf16)
-    st = f(A, A, A, A, A, 1, T, 64, 128, 64, la.LA_DTYPE_BF16, A, A + 0x40000, A + 0x50000,
+    # fp32: the CUDA-core path, whose time reversals need the scratch
+    T = cap // (3 * 64 * 128 * 4) + 1  # one token more than the array holds (fp32)
+    st = f(A, A, A, A, A, 1, T, 64, 128, 64, la.LA_DTYPE_FP32, A, A + 0x40000, A + 0x50000,
            A + 0x60000, None)
     assert st == la.LA_ERR_INVALID_ARG
     assert "scratch" in lib.lightning_attn_last_error().decode()

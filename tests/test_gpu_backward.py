@@ -115,3 +115,12 @@ def test_backward_writes_stay_inside_gradients():
     ref = oracle.backward(inp.q, inp.k, inp.v, inp.decay, inp.cu_seqlens.cpu(), dout)
     for x, r, name in zip((dq, dk, dv), ref, ("dq", "dk", "dv")):
         assert_close(x, r, TOL_BF16, f"guarded {name}")
+
+
+@pytest.mark.parametrize("chunk", [32, 64])
+def test_tensor_core_backward_block_sizes(chunk):
+    """The anti-causal launches with 32- and 64-token blocks (128-row tiles
+    advancing one block at a time, walked last to first)."""
+    got, ref = run([1, 0, 31, 33, 64, 65, 200, 129], 3, 128, torch.bfloat16, chunk, 28)
+    for x, r, name in zip(got, ref, ("dq", "dk", "dv")):
+        assert_close(x, r, TOL_BF16, f"tc B={chunk} {name}")

@@ -88,10 +88,34 @@ def test_bf16_cuda_core_d64(chunk):
 
 @pytest.mark.parametrize("chunk", [0, 64])
 def test_bf16_d128_paths(chunk):
-    """chunk 0 (tensor cores, 128) and chunk 64 (CUDA cores) both match."""
+    """chunk 0 (tensor cores, block 128) and chunk 64 (tensor cores, 64-token
+    blocks in 128-row tiles) both match."""
     inp, out, st, ref, ref_st = run_case([1000, 1, 2049], 8, 128, torch.bfloat16,
                                          chunk=chunk, seed=4)
     check(out, st, ref, ref_st, TOL_BF16, what=f"bf16 d=128 chunk={chunk}")
+
+
+@pytest.mark.parametrize("chunk", [16, 32, 64])
+def test_tensor_core_block_sizes_ragged_varlen(chunk):
+    """Blocks of 16, 32 and 64 tokens on the tensor cores: every block is a
+    128-row tile whose rows past the block are masked, the next tile starting
+    one block later; ragged lengths put the short last block everywhere."""
+    lengths = [1, 0, 15, 16, 17, 31, 33, 63, 64, 65, 127, 129, 300, 0, 513]
+    inp, out, st, ref, ref_st = run_case(lengths, 3, 128, torch.bfloat16, chunk=chunk, seed=40)
+    check(out, st, ref, ref_st, TOL_BF16, what=f"tc B={chunk}")
+
+
+@pytest.mark.parametrize("chunk", [16, 64])
+def test_tensor_core_block_sizes_with_state(chunk):
+    lengths = [0, 40, 200, 77]
+    inp = wl.prefill_inputs(lengths, 2, 128, dtype=torch.bfloat16, seed=41, device="cuda")
+    s0 = wl.cached_states(len(lengths), 2, 128, seed=42, device="cuda")
+    out, st = la.prefill(inp.q, inp.k, inp.v, inp.decay, inp.cu_seqlens, chunk=chunk,
+                         initial_state=s0)
+    torch.cuda.synchronize()
+    ref, ref_st = oracle.recurrent(inp.q, inp.k, inp.v, inp.decay, inp.cu_seqlens.cpu(),
+                                   initial_state=s0.cpu())
+    check(out, st, ref, ref_st, TOL_BF16, what=f"tc B={chunk} from cached states")
 
 
 def test_chunk_invariance():
@@ -104,10 +128,11 @@ def test_chunk_invariance():
         assert rel_err(o, outs[0][0]) < 1e-5
         assert rel_err(s, outs[0][1]) < 1e-5
     qb, kb, vb = (t.to(torch.bfloat16) for t in (inp.q, inp.k, inp.v))
-    ob, sb = la.prefill(qb, kb, vb, inp.decay, inp.cu_seqlens, chunk=128)
     of, sf = la.prefill(qb.float(), kb.float(), vb.float(), inp.decay, inp.cu_seqlens, chunk=64)
-    assert_close(ob, of, TOL_BF16, "tc B=128 vs fp32 B=64")
-    assert_close(sb, sf, TOL_BF16, "tc B=128 vs fp32 B=64 state")
+    for c in (128, 64, 32, 16):  # the tensor-core kernel at every block size
+        ob, sb = la.prefill(qb, kb, vb, inp.decay, inp.cu_seqlens, chunk=c)
+        assert_close(ob, of, TOL_BF16, f"tc B={c} vs fp32 B=64")
+        assert_close(sb, sf, TOL_BF16, f"tc B={c} vs fp32 B=64 state")
 
 
 # ------------------------------------------------------------- special decays

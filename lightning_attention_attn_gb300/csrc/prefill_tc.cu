@@ -64,6 +64,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "la_internal.h"
@@ -1081,14 +1082,16 @@ cudaError_t prefill_tc_bf16(const PrefillArgs &a) {
                           : csi == 1 ? pick_kernel<64>(a.anti_causal, snap)
                           : csi == 2 ? pick_kernel<32>(a.anti_causal, snap)
                                      : pick_kernel<16>(a.anti_causal, snap);
-    // one bit per instantiation: (causal, anti-causal, causal with snapshots) x block size
-    static int attr_set_for[64] = {0};
+    // The shared-memory opt-in is set once per device and instantiation (one
+    // bit each: (causal, anti-causal, causal with snapshots) x block size);
+    // concurrent first calls may both set it, which is harmless.
+    static std::atomic<int> attr_set_for[64];
     const int bit = 1 << ((a.anti_causal ? 1 : snap ? 2 : 0) * 4 + csi);
-    if (dev < 64 && !(attr_set_for[dev] & bit)) {
+    if (dev >= 64 || !(attr_set_for[dev].load(std::memory_order_acquire) & bit)) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)kSmemBytes);
         if (e != cudaSuccess) return e;
-        attr_set_for[dev] |= bit;
+        if (dev < 64) attr_set_for[dev].fetch_or(bit, std::memory_order_release);
     }
     const long grid = (long)(a.rank_limit > 0 ? a.rank_limit : a.nseq) * a.num_heads * NVS;
     if (grid <= 0) return cudaSuccess;

@@ -267,6 +267,25 @@ def run_ours(args, ws, rank, local):
     torch.cuda.synchronize()
     g_start = torch.cuda.Event(enable_timing=True)
     g_end = torch.cuda.Event(enable_timing=True)
+
+    def graph_ms(fn, n):
+        """Mean ms per call of fn(stream), n calls captured as one CUDA graph
+        and replayed (after one untimed replay)."""
+        gstream.wait_stream(stream)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=gstream):
+            for _ in range(n):
+                fn(gstream)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(gstream):
+            g.replay()
+            e0.record(gstream)
+            g.replay()
+            e1.record(gstream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
     barrier(ws)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
@@ -531,11 +550,16 @@ def run_ours(args, ws, rank, local):
     b1.record(stream)
     torch.cuda.synchronize()
     la.device_status(stream)
-    bms = b0.elapsed_time(b1) / K
+    bms_eager = b0.elapsed_time(b1) / K
+    bms = graph_ms(lambda s_: la.backward(inp.q, inp.k, inp.v, inp.decay, inp.cu_seqlens, dout,
+                                          dq=dq, dk=dk, dv=dv, stream=s_), K)
+    la.device_status(stream)
     bbytes = T * H * d * 2 * 7  # q, k, v, dout read; dq, dk, dv written (bf16)
     bgbs = bbytes / (bms / 1e3) / 1e9
     backward = {"value": round(T / (bms / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(bms, 4),
-                "config": {"workload": "prefill_8k backward (dq, dk, dv)"},
+                "config": {"workload": "prefill_8k backward (dq, dk, dv)",
+                           "issue": "K steps replayed as one CUDA graph"},
+                "eager_ms_per_step": round(bms_eager, 4),
                 "launches_per_step": 3,
                 "roofline": {"bound": "hbm", "achieved": round(bgbs, 1), "peak": pk["hbm"],
                              "unit": "GB/s", "frac": round(bgbs / pk["hbm"], 4),
@@ -579,8 +603,17 @@ def run_ours(args, ws, rank, local):
                 mstep(two)
             m1.record(stream)
             torch.cuda.synchronize()
-            res["ms_two_streams" if two else "ms_one_prefill_launch"] = round(
+            res[("ms_two_streams" if two else "ms_one_prefill_launch") + "_eager"] = round(
                 m0.elapsed_time(m1) / K, 4)
+        # the same steps replayed as CUDA graphs (the decode stream joins the
+        # capture through the step's fork and join events)
+        res["ms_two_streams"] = round(graph_ms(
+            lambda s_: la.mixed_step(minp.q, minp.k, minp.v, minp.decay, minp.cu_seqlens, mstate,
+                                     out=mout, prefill_stream=s_, decode_stream=dstream,
+                                     cu_seqlens_host=mcu), K), 4)
+        res["ms_one_prefill_launch"] = round(graph_ms(
+            lambda s_: la.prefill(minp.q, minp.k, minp.v, minp.decay, minp.cu_seqlens, out=mout,
+                                  initial_state=mstate, final_state=mstate, stream=s_), K), 4)
         la.device_status(stream)
         mbytes = len(mlen) * H * d * d * 4 * 2 + sum(mlen) * H * d * 2 * 4
         res["tokens_per_s"] = round(sum(mlen) / (res["ms_two_streams"] / 1e3), 1)

@@ -758,6 +758,26 @@ def run_ours(args, ws, rank, local):
         host = wl.PrefillInputs(inp.q.cpu(), inp.k.cpu(), inp.v.cpu(), inp.decay.cpu(),
                                 inp.cu_seqlens.cpu())
         line["cpu_baseline"] = cpu_baseline(host)
+    # Compact copies of the secondary measurements, last in the line so that
+    # a reader of only the line's tail still sees them.
+    def frac(x):
+        return x.get("roofline", {}).get("frac") if isinstance(x, dict) else x
+    line["summary"] = {
+        "decode_128": {"ms_per_step": decode["ms_per_step"], "tokens_per_s": decode["value"],
+                       "hbm_frac": decode["roofline"]["frac"],
+                       "eager_hbm_frac": decode["roofline"]["eager"]["frac"]},
+        "backward_8k": {"ms_per_step": backward["ms_per_step"],
+                        "tokens_per_s": backward["value"],
+                        "hbm_frac": backward["roofline"]["frac"],
+                        "launches_per_step": backward["launches_per_step"]},
+        "prefill_8k": {"ms_per_launch": round(total_ms / K, 5), "hbm_frac": roofline["frac"],
+                       "eager_hbm_frac": roofline["eager"]["frac"]},
+        "chunk_sweep_hbm_frac": {k_: frac(more.get(k_)) for k_ in
+                                 ("prefill_8k_chunk32", "prefill_8k_chunk64",
+                                  "prefill_128k_chunk64", "prefill_128k",
+                                  "prefill_128k_chunk256")},
+        "varlen_16_hbm_frac": frac(more.get("varlen_16")),
+    }
     return line
 
 

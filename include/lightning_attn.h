@@ -269,9 +269,12 @@ int64_t lightning_attn_backward_workspace_bytes(int32_t total_tokens, int32_t nu
  * tensor-core path (bf16, head_dim 128, chunk 0-128) no scratch is used
  * and no size limit applies; otherwise a call whose
  * lightning_attn_backward_workspace_bytes() exceeds the array returns
- * LA_ERR_INVALID_ARG before touching the GPU.  The first call on a device
- * looks up the array's device address (cudaGetSymbolAddress) with that
- * device current; make that first call before any stream capture.  The
+ * LA_ERR_INVALID_ARG before touching the GPU (argument errors, empty calls
+ * and unsupported block sizes are reported first, exactly as by
+ * lightning_attn_backward).  The first call on a device looks up the array's
+ * device address (cudaGetSymbolAddress) with that device current, and so does
+ * the first call after the device's context has been destroyed and made
+ * again (cudaDeviceReset); make such a call before any stream capture.  The
  * array is shared by all calls: calls that overlap on the GPU race on it;
  * calls ordered on one stream do not.  Nothing is allocated.
  */

@@ -304,12 +304,17 @@ int64_t lightning_attn_backward_workspace_bytes(int32_t total_tokens, int32_t nu
     return (int64_t)(3 * backward_slot_bytes(total_tokens, num_heads, head_dim, dtype));
 }
 
-la_status lightning_attn_backward(const void *q, const void *k, const void *v,
-                                  const float *decay, const int32_t *cu_seqlens,
-                                  int32_t num_seqs, int32_t total_tokens, int32_t num_heads,
-                                  int32_t head_dim, int32_t chunk, la_dtype dtype,
-                                  const void *d_out, void *d_q, void *d_k, void *d_v,
-                                  void *workspace, int64_t workspace_bytes, void *stream) {
+}  // extern "C"
+
+namespace la {
+
+la_status backward_check(const void *q, const void *k, const void *v, const float *decay,
+                         const int32_t *cu_seqlens, int32_t num_seqs, int32_t total_tokens,
+                         int32_t num_heads, int32_t head_dim, int32_t chunk, la_dtype dtype,
+                         const void *d_out, void *d_q, void *d_k, void *d_v, bool *work,
+                         bool *needs_workspace) {
+    *work = false;
+    *needs_workspace = false;
     if (num_seqs < 0) return fail(LA_ERR_INVALID_ARG, "num_seqs < 0 (%d)", num_seqs);
     if (total_tokens < 0) return fail(LA_ERR_INVALID_ARG, "total_tokens < 0 (%d)", total_tokens);
     if (num_heads < 1) return fail(LA_ERR_INVALID_ARG, "num_heads < 1 (%d)", num_heads);
@@ -321,8 +326,6 @@ la_status lightning_attn_backward(const void *q, const void *k, const void *v,
         return fail(LA_ERR_INVALID_ARG, "chunk must be 0, 16, 32, 64, 128 or 256 (got %d)", chunk);
     if (num_seqs == 0 || total_tokens == 0) return LA_OK;
     if (!cu_seqlens || !decay) return fail(LA_ERR_INVALID_ARG, "null decay or cu_seqlens");
-    // the tensor-core path computes dk and dv in place and needs no workspace
-    const bool tc = la::uses_tensor_cores(dtype == LA_DTYPE_BF16, head_dim, chunk);
     const void *ptrs[] = {q, k, v, d_out, d_q, d_k, d_v};
     for (const void *p : ptrs)
         if (!p) return fail(LA_ERR_INVALID_ARG, "null tensor pointer");
@@ -341,6 +344,33 @@ la_status lightning_attn_backward(const void *q, const void *k, const void *v,
         for (int j = i + 1; j < 3; ++j)
             if (outs[i] == outs[j]) return fail(LA_ERR_INVALID_ARG, "two gradients share an array");
     }
+    // the tensor-core path computes dk and dv in place and needs no
+    // workspace; off it, blocks of 128 and 256 tokens have no kernel
+    const bool tc = uses_tensor_cores(dtype == LA_DTYPE_BF16, head_dim, chunk);
+    if (!tc && (chunk == 128 || chunk == 256))
+        return fail(LA_ERR_UNSUPPORTED,
+                    "chunk %d needs the tensor-core path (bf16, head_dim 128)", chunk);
+    *work = true;
+    *needs_workspace = !tc;
+    return LA_OK;
+}
+
+}  // namespace la
+
+extern "C" {
+
+la_status lightning_attn_backward(const void *q, const void *k, const void *v,
+                                  const float *decay, const int32_t *cu_seqlens,
+                                  int32_t num_seqs, int32_t total_tokens, int32_t num_heads,
+                                  int32_t head_dim, int32_t chunk, la_dtype dtype,
+                                  const void *d_out, void *d_q, void *d_k, void *d_v,
+                                  void *workspace, int64_t workspace_bytes, void *stream) {
+    bool work = false, needs_ws = false;
+    const la_status chk = la::backward_check(q, k, v, decay, cu_seqlens, num_seqs, total_tokens,
+                                             num_heads, head_dim, chunk, dtype, d_out, d_q, d_k,
+                                             d_v, &work, &needs_ws);
+    if (chk != LA_OK || !work) return chk;
+    const bool tc = !needs_ws;
     const size_t slot = backward_slot_bytes(total_tokens, num_heads, head_dim, dtype);
     if (!tc) {
         if (!workspace) return fail(LA_ERR_INVALID_ARG, "null workspace (CUDA-core path)");

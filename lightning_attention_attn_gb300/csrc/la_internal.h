@@ -5,6 +5,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "lightning_attn.h"
+
 namespace la {
 
 struct PrefillArgs {
@@ -75,6 +77,16 @@ cudaError_t selftest_wait_timeout(uint64_t timeout_ns, cudaStream_t stream);
 // sequence s; rows are row_bytes long (a multiple of 16).  in != out.
 cudaError_t reverse_sequences(const void *in, void *out, const int32_t *cu_seqlens, int nseq,
                               int total_tokens, size_t row_bytes, cudaStream_t stream);
+
+// Every host-side check of lightning_attn_backward except those of the
+// workspace.  Returns an error status, or LA_OK with *work = false when there
+// is nothing to compute, or LA_OK with *work = true and *needs_workspace
+// telling whether the path that serves the call reads a workspace.
+la_status backward_check(const void *q, const void *k, const void *v, const float *decay,
+                         const int32_t *cu_seqlens, int32_t num_seqs, int32_t total_tokens,
+                         int32_t num_heads, int32_t head_dim, int32_t chunk, la_dtype dtype,
+                         const void *d_out, void *d_q, void *d_k, void *d_v, bool *work,
+                         bool *needs_workspace);
 
 // Sets the message lightning_attn_last_error() returns on this host thread.
 void set_last_error(const char *fmt, ...) __attribute__((format(printf, 1, 2)));

@@ -206,7 +206,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 template <bool kAnti, bool kSnap, int kCS>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                  const __grid_constant__ CUtensorMap tmV,
                   const float *__restrict__ decay, const int32_t *__restrict__ cu, int nseq, int T,
                   int H, const float *initial_state, __nv_bfloat16 *__restrict__ out,
                   float *final_state, int min_len, float *snapshots, int snap_interval) {
@@ -1065,11 +1065,10 @@ cudaError_t prefill_tc_bf16(const PrefillArgs &a) {
         return cudaErrorNotSupported;
     // rows are written in place; the anti-causal kernel starts from a zero state
     if (a.reverse_out || (a.anti_causal && a.initial_state)) return cudaErrorNotSupported;
-    CUtensorMap mq, mk, mv, mo;
+    CUtensorMap mq, mk, mv;
     if (!make_map(&mq, a.q, a.total_tokens, a.num_heads) ||
         !make_map(&mk, a.k, a.total_tokens, a.num_heads) ||
-        !make_map(&mv, a.v, a.total_tokens, a.num_heads) ||
-        !make_map(&mo, a.out, a.total_tokens, a.num_heads))
+        !make_map(&mv, a.v, a.total_tokens, a.num_heads))
         return cudaErrorInvalidValue;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -1097,7 +1096,7 @@ cudaError_t prefill_tc_bf16(const PrefillArgs &a) {
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffffL) return cudaErrorInvalidConfiguration;
     kern<<<(unsigned)grid, kThreads, kSmemBytes, a.stream>>>(
-        mq, mk, mv, mo, a.decay, a.cu_seqlens, a.nseq, a.total_tokens, a.num_heads,
+        mq, mk, mv, a.decay, a.cu_seqlens, a.nseq, a.total_tokens, a.num_heads,
         a.initial_state, static_cast<__nv_bfloat16 *>(a.out), a.final_state, a.min_len,
         a.snapshots, a.snapshot_interval);
     return cudaGetLastError();

@@ -140,27 +140,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, uint
         : "memory");
 }
 
-// 2-D tiled store of one box from shared memory (bulk async-group).
-__device__ __forceinline__ void tma_store_2d(const void *tmap, uint32_t src, int x, int y) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-            reinterpret_cast<uint64_t>(tmap)),
-        "r"(src), "r"(x), "r"(y)
-        : "memory");
-}
-__device__ __forceinline__ void bulk_commit_group() {
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-// Waits until the shared-memory sources of all committed bulk groups have
-// been read (the global writes may still be in flight).
-__device__ __forceinline__ void bulk_wait_read_all() {
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-// Waits until all committed bulk groups have completed.
-__device__ __forceinline__ void bulk_wait_all() {
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
 // Barrier among `count` threads (a multiple of 32) of the CTA, id 1..15.
 __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

@@ -216,36 +216,46 @@ def test_prefill_8k_layer_full_parity():
     assert worst <= TOL_BF16, worst
 
 
+def check_all_heads(inp, out, st, what, group=8):
+    """Every head of a large case against the oracle's recurrent form, a
+    group of heads at a time (bounded host memory): all tokens, all value
+    columns and every final state.  Each group is held to its own RMS, which
+    is stricter than the whole-tensor RMS for the fast-decay heads."""
+    H = inp.q.shape[1]
+    cu = inp.cu_seqlens.cpu()
+    worst_o = worst_s = 0.0
+    for h0 in range(0, H, group):
+        heads = list(range(h0, min(H, h0 + group)))
+        sel = lambda t: t[:, heads].contiguous()
+        ref, ref_st = oracle.recurrent(sel(inp.q), sel(inp.k), sel(inp.v), inp.decay[heads], cu)
+        worst_o = max(worst_o, assert_close(out[:, heads], ref, TOL_BF16,
+                                            f"{what} out heads {h0}..{heads[-1]}"))
+        worst_s = max(worst_s, assert_close(st[:, heads], ref_st, TOL_BF16,
+                                            f"{what} state heads {h0}..{heads[-1]}"))
+        del ref, ref_st
+    print(f"[parity] {what}: worst group error out {worst_o:.3e}, state {worst_s:.3e}")
+
+
 @pytest.mark.slow
-def test_prefill_128k_sampled_heads():
-    """B=1, H=64, N=131072: heads 0, 31, 63 in full (all tokens, final state)."""
+def test_prefill_128k_all_heads():
+    """B=1, H=64, N=131072: every head in full (all tokens, final states)."""
     cfg = wl.PREFILL_128K
-    heads = [0, 31, 63]
     inp = wl.prefill_inputs(cfg["lengths"], 64, 128, dtype=torch.bfloat16, seed=0, device="cuda")
     out, st = la.prefill(inp.q, inp.k, inp.v, inp.decay, inp.cu_seqlens)
     torch.cuda.synchronize()
-    sel = lambda t: t[:, heads].contiguous()
-    ref, ref_st = oracle.recurrent(sel(inp.q), sel(inp.k), sel(inp.v), inp.decay[heads],
-                                   inp.cu_seqlens.cpu())
-    assert_close(out[:, heads], ref, TOL_BF16, "128k out")
-    assert_close(st[:, heads], ref_st, TOL_BF16, "128k state")
+    check_all_heads(inp, out, st, "128k")
 
 
 @pytest.mark.slow
-def test_prefill_varlen_16_sampled_heads():
+def test_prefill_varlen_16_all_heads():
     """16 packed sequences, lengths uniform in [1024, 32768] (seed 0), H=64:
-    heads 0 and 63 of every sequence in full."""
+    every head of every sequence in full."""
     cfg = wl.VARLEN_16
     lengths = wl.varlen_lengths(cfg["num_seqs"], cfg["lo"], cfg["hi"], seed=0)
-    heads = [0, 63]
     inp = wl.prefill_inputs(lengths, 64, 128, dtype=torch.bfloat16, seed=0, device="cuda")
     out, st = la.prefill(inp.q, inp.k, inp.v, inp.decay, inp.cu_seqlens)
     torch.cuda.synchronize()
-    sel = lambda t: t[:, heads].contiguous()
-    ref, ref_st = oracle.recurrent(sel(inp.q), sel(inp.k), sel(inp.v), inp.decay[heads],
-                                   inp.cu_seqlens.cpu())
-    assert_close(out[:, heads], ref, TOL_BF16, "varlen out")
-    assert_close(st[:, heads], ref_st, TOL_BF16, "varlen state")
+    check_all_heads(inp, out, st, "varlen_16")
 
 
 # ------------------------------------------------------- failure detection

@@ -43,9 +43,10 @@
 //   warps 0-3    mask: S -> P = fp16(2^-e_j S (.) M) into TMEM, one lane
 //                quadrant each, helped by warps 14 and 15 on the two
 //                quadrants with the most blocks below the diagonal
-//   warps 4-7    state: KV fold + write-back, KV copy, output; its thread 0
-//                also issues the TMA loads of the Q and K rings
-//   warps 8-11   V-tile: Vhat hi/lo, fp16 V
+//   warps 4-11   workers, two threads per row (token / state row), each with
+//                32 of the 64 value columns: KV fold + write-back, the V tile
+//                (Vhat hi/lo, fp16 V), KV copy, output; worker thread 0 also
+//                issues the TMA loads of the Q and K rings
 //   warp  12     MMA stream A (one thread): S and P V; TMA loads of the V ring
 //   warp  13     MMA stream B (one thread): dKV and Q KV
 // (the anti-causal instantiation swaps warps 12/13 with 14/15: its heavy
@@ -84,8 +85,9 @@ constexpr int DV = 64;       // value columns per CTA
 constexpr int NVS = D / DV;  // value slices per head
 constexpr int BC = 128;      // chunk (block) size
 constexpr int kThreads = 512;  // 16 warps: 4 per SM sub-partition, 128 registers
-constexpr int kStateWarp0 = 4;
-constexpr int kVWarp0 = 8;
+constexpr int kMaskWarps = 4;   // warps 0-3: one per TMEM lane quadrant
+constexpr int kWorkWarp0 = 4;   // warps 4-11: fold, V tile, copy, output
+constexpr int kWorkWarps = 8;
 // Warps 12-15: two MMA issuers and two mask helpers.  A helper must sit on
 // the TMEM lane quadrant it helps (a warp reads lanes 32 (warp % 4) ..), and
 // the quadrants with the most mask blocks are 2 and 3 in the causal
@@ -120,7 +122,7 @@ struct Ctrl {
     int seq_slot;
     int snap_base;                 // first snapshot of this CTA's sequence
     int pad;
-    float vmax[2][4];              // per-warp max |v| of a chunk, double buffered
+    alignas(16) float vmax[2][8];  // per-warp max |v| of a chunk, double buffered
     float vscale[4];               // 2^f of V's fp16 scale, ring indexed by chunk & 3
     signed char rowe[2][BC];       // e_j of P's rows (scale 2^-e_j), per S buffer
     uint16_t mpart[2][2][2][32];   // [pair][chunk & 1][owner, helper][lane]: partial
@@ -158,6 +160,19 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
                  : "r"(addr)
                  : "memory");
     return v;
+}
+// 32 bytes to global memory: one 256-bit store when the address is 32-byte
+// aligned (aligned32), else two 128-bit stores.
+__device__ __forceinline__ void st_global_32B(void *p, const uint32_t *w, bool aligned32) {
+    if (aligned32) {
+        asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]),
+                     "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                     : "memory");
+    } else {
+        uint4 *q = reinterpret_cast<uint4 *>(p);
+        q[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        q[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    }
 }
 __device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
     float v;
@@ -238,6 +253,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     // §3.3.1): KV_{-1} = S0 instead of 0.  initial_state may be final_state
     // itself: every CTA reads its slice of S0 before it writes that slice.
     const bool has_init = initial_state != nullptr;
+    const bool out32 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
 
     auto bar = [&](const uint64_t &b) { return smem_u32(&b); };
     const uint32_t pw_s = smem_u32(&cs.pw[0]);          // lambda^e at pw_s + 4 e
@@ -259,18 +275,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             mbar_init(bar(cs.empty_k[i]), 2);  // S_i (stream A) and dKV_i (stream B)
             mbar_init(bar(cs.empty_v[i]), 1);
             mbar_init(bar(cs.s_full[i]), 1);
-            mbar_init(bar(cs.s_free[i]), 128);
-            mbar_init(bar(cs.pv_ready[i]), 6 * 32 + 128);  // mask warps + V-tile warpgroup
-            mbar_init(bar(cs.vmax_ready[i]), 128);
+            mbar_init(bar(cs.s_free[i]), kWorkWarps * 32);
+            mbar_init(bar(cs.pv_ready[i]), 6 * 32 + kWorkWarps * 32);  // mask + worker warps
+            mbar_init(bar(cs.vmax_ready[i]), kWorkWarps * 32);
             mbar_init(bar(cs.pair[i]), 64);
             // by chunk parity: near the end of a sequence stream A may finish
             // two P V groups before the state warps wait for the first
             mbar_init(bar(cs.o_full[i]), 1);
         }
         mbar_init(bar(cs.o2_full), 1);
-        mbar_init(bar(cs.o2_ready), 128);
+        mbar_init(bar(cs.o2_ready), kWorkWarps * 32);
         mbar_init(bar(cs.dkv_full), 1);
-        mbar_init(bar(cs.dkv_ready), 256);  // V-tile (Vhat) + state (write-back)
+        mbar_init(bar(cs.dkv_ready), kWorkWarps * 32);  // Vhat and write-back, per worker
         mbar_init(bar(cs.done_a), 1);
         mbar_init(bar(cs.done_b), 1);
         cs.abort = 0;
@@ -416,7 +432,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         __syncwarp();
         int no_abort = 0;
         warp_wait(bar(cs.done_b), 0, &no_abort);
-    } else if (warp < kStateWarp0 || warp == R::help2 || warp == R::help3) {
+    } else if (warp < kMaskWarps || warp == R::help2 || warp == R::help3) {
         // ================= mask warps: S -> P =================
         // Row j of the chunk is TMEM lane j; the warps of lane quadrant q
         // (rows 32q .. 32q + 31) hold that quadrant's 32-column S blocks
@@ -443,7 +459,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         //     f = lambda^(32 (cb - q - 1) + c) above it, row constant lambda^(32 - lane).
         const int q = warp & 3;                 // TMEM lane quadrant
         const int qm = kAnti ? 3 - q : q;       // the same quadrant in causal terms
-        const bool owner = warp < kStateWarp0;
+        const bool owner = warp < kMaskWarps;
         const int j = q * 32 + lane;
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         // Blocks (causal terms): register set A holds a block below the
@@ -594,29 +610,44 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             tc_fence_before();
             mbar_arrive(bar(cs.pv_ready[st]));
         }
-    } else if (warp < kVWarp0) {
-        // ================= state warpgroup =================
-        // Thread r owns TMEM lane r: row r of the d_k x 64 state and token r
-        // of the chunk.  The fp32 state lives in the dKV accumulator as the
-        // sum of its two 64-column halves.  Per chunk:
-        //   fold: KV_i = sum of the halves; lambda^{B_{i+1}} KV_i / 2 is
-        //         written back into both halves for dKV_{i+1} to accumulate
-        //         onto (dKV_{i+1} may start right after);
-        //   copy: once Q_i KV_{i-1} has finished, a hi/lo bf16 copy of KV_i
-        //         for Q_{i+1} KV_i;
-        //   O2:   Q_i KV_{i-1} (hi + lo) into registers, freeing its columns;
-        //   out:  once P_i V_i has finished, o = 2^(e + f) O1 + lambda^(r+1) O2.
-        const int w4 = warp - kStateWarp0;
-        const int r = w4 * 32 + lane;
-        const uint32_t lane_off = (uint32_t)(w4 * 32) << 16;
-        const uint32_t kvb = sb + kOffKVb;
-        const uint32_t tkv = tmem + lane_off + kColDKV;
-        const uint32_t to2 = tmem + lane_off + kColO2;
-        // Q and K rings (thread 0 of the warpgroup): slot c & 1 is reloaded
-        // for chunk c once S and dKV (K) or S and Q KV (Q) of chunk c - 2
-        // have finished; the fold and copy steps of chunk c - 2 wait for dKV
-        // and Q KV anyway, and S was issued before.
-        const bool loader = threadIdx.x == kStateWarp0 * 32;
+    } else if (warp < kWorkWarp0 + kWorkWarps) {
+        // ================= worker warps =================
+        // Thread (warp, lane) owns TMEM lane r = 32 (warp % 4) + lane -- token
+        // r of the chunk and row r (a d_k index) of the state -- and the 32
+        // value columns [c0, c0 + 32) of the CTA's 64-wide slice, c0 = 0 for
+        // warps 4-7 and 32 for warps 8-11.  The fp32 state lives in the dKV
+        // accumulator as the sum of its two 64-column halves.  Per chunk i:
+        //   fold:   KV_i = sum of the halves; lambda^{B_{i+1}} KV_i / 2 is
+        //           written back into both halves for dKV_{i+1} to accumulate
+        //           onto;
+        //   V tile: chunk i+1's V row segment, read from shared memory once:
+        //           max |v| (for the tile's fp16 scale, exchanged among the
+        //           eight warps), Vhat = lambda^(Lc-1-l) v as a hi/lo bf16 pair
+        //           (dKV_{i+1} may go once every worker has written its part
+        //           and its write-back), then V in place as fp16 with the
+        //           tile's power-of-two scale (for P V);
+        //   copy:   once Q_i KV_{i-1} has finished, a hi/lo bf16 copy of KV_i
+        //           for Q_{i+1} KV_i, and Q_i KV_{i-1} (hi + lo) into registers;
+        //   out:    once P_i V_i has finished, o = 2^(e + f) O1 + lambda^(r+1) O2.
+        // Splitting the value columns between two threads per row halves the
+        // latency of each step; the steps that gate the next MMA come first.
+        // Worker thread 0 also issues the TMA loads of the Q and K rings.
+        const int wq = warp & 3;
+        const int half = (warp - kWorkWarp0) >> 2;
+        const int r = wq * 32 + lane;
+        const int c0 = 32 * half;
+        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        const uint32_t kvb = sb + kOffKVb, vha = sb + kOffVhat;
+        const uint32_t tkv = tmem + lane_off + kColDKV + c0;  // hi half; lo half at + 64
+        const uint32_t to2 = tmem + lane_off + kColO2 + c0;   // hi half; lo half at + 64
+        // byte offset of the row's 16-byte piece 4 half + m (value columns
+        // c0 + 8m .. c0 + 8m + 7) in a 128-byte swizzled row
+        auto piece = [&](int m) { return (uint32_t)(((4 * half + m) ^ (r & 7)) * 16); };
+        // Q and K rings (worker thread 0): slot c & 1 is reloaded for chunk c
+        // once S and dKV (K) or S and Q KV (Q) of chunk c - 2 have finished;
+        // the fold and copy steps of chunk c - 2 wait for dKV and Q KV anyway,
+        // and S was issued before.
+        const bool loader = threadIdx.x == kWorkWarp0 * 32;
         int nq = 0, nk = 0;
         auto load_q = [&](int c) -> bool {
             const int st = c & 1;
@@ -647,121 +678,186 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
                 if (!load_k(c) || !load_q(c)) break;
         }
         __syncwarp();
-        // hi/lo bf16 copy of a state row for the Q KV MMA: hi = x with the
-        // low 16 bits cleared (a bf16, exact); lo = x - hi (exact in fp32),
-        // also truncated: hi + lo = x to about 2^-14 relative
-        auto store_kv_copy = [&](const float(&kv)[DV]) {
+        // hi/lo bf16 copy of 8 state values: hi = x with the low 16 bits
+        // cleared (a bf16, exact); lo = x - hi (exact in fp32), also
+        // truncated: hi + lo = x to about 2^-14 relative
+        auto split8 = [&](const float *x, uint32_t(&hi)[4], uint32_t(&lo)[4]) {
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const uint32_t phys = (uint32_t)(c ^ (r & 7));
+            for (int m = 0; m < 4; ++m) {
+                const uint32_t ua = __float_as_uint(x[2 * m]);
+                const uint32_t ub = __float_as_uint(x[2 * m + 1]);
+                hi[m] = __byte_perm(ua, ub, 0x7632);
+                const float2 l2 = f2_sub(make_float2(__uint_as_float(ua), __uint_as_float(ub)),
+                                         make_float2(__uint_as_float(ua & 0xffff0000u),
+                                                     __uint_as_float(ub & 0xffff0000u)));
+                lo[m] = __byte_perm(__float_as_uint(l2.x), __float_as_uint(l2.y), 0x7632);
+            }
+        };
+        // the copy of this thread's 32 state values for the Q KV MMA
+        auto store_kv_copy = [&](const float(&kv)[32]) {
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
                 uint32_t hi[4], lo[4];
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const uint32_t ua = __float_as_uint(kv[8 * c + 2 * m]);
-                    const uint32_t ub = __float_as_uint(kv[8 * c + 2 * m + 1]);
-                    hi[m] = __byte_perm(ua, ub, 0x7632);
-                    const float2 l2 = f2_sub(make_float2(__uint_as_float(ua), __uint_as_float(ub)),
-                                             make_float2(__uint_as_float(ua & 0xffff0000u),
-                                                         __uint_as_float(ub & 0xffff0000u)));
-                    lo[m] = __byte_perm(__float_as_uint(l2.x), __float_as_uint(l2.y), 0x7632);
-                }
-                st_shared_v4(kvb + r * 128 + phys * 16, hi[0], hi[1], hi[2], hi[3]);
-                st_shared_v4(kvb + kHalf + r * 128 + phys * 16, lo[0], lo[1], lo[2], lo[3]);
+                split8(&kv[8 * m], hi, lo);
+                st_shared_v4(kvb + r * 128 + piece(m), hi[0], hi[1], hi[2], hi[3]);
+                st_shared_v4(kvb + kHalf + r * 128 + piece(m), lo[0], lo[1], lo[2], lo[3]);
             }
             fence_proxy_async_smem();
         };
-        // lambda^{Lc} KV / 2 into both halves of the dKV accumulator, for
-        // the next dKV MMA to accumulate onto
-        auto write_back = [&](const float(&kv)[DV], float decay_to_next) {
+        // lambda^{Lc} KV / 2 into both halves of the dKV accumulator, for the
+        // next dKV MMA to accumulate onto
+        auto write_back = [&](const float(&kv)[32], float decay_to_next) {
             const float dh = 0.5f * decay_to_next;
             const float2 d2 = make_float2(dh, dh);
+            uint32_t w[32];
 #pragma unroll
-            for (int hh = 0; hh < 4; ++hh) {
-                uint32_t w[16];
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const float2 x = f2_mul(make_float2(kv[16 * hh + 2 * c], kv[16 * hh + 2 * c + 1]), d2);
-                    w[2 * c] = __float_as_uint(x.x);
-                    w[2 * c + 1] = __float_as_uint(x.y);
-                }
-                tmem_st16(tkv + 16 * hh, w);
-                tmem_st16(tkv + 64 + 16 * hh, w);
+            for (int c = 0; c < 16; ++c) {
+                const float2 x = f2_mul(make_float2(kv[2 * c], kv[2 * c + 1]), d2);
+                w[2 * c] = __float_as_uint(x.x);
+                w[2 * c + 1] = __float_as_uint(x.y);
             }
+            tmem_st32(tkv, w);
+            tmem_st32(tkv + 64, w);
             tmem_wait_st();
         };
-        if (has_init) {
-            // KV_{-1} = S0: row r, this CTA's 64 value columns, 16 at a time
-            const float4 *src = reinterpret_cast<const float4 *>(
-                initial_state + (((long)s * H + h) * D + r) * D + vs * DV);
-            float4 *dst = (nch == 0 && final_state)
-                              ? reinterpret_cast<float4 *>(
-                                    final_state + (((long)s * H + h) * D + r) * D + vs * DV)
-                              : nullptr;
-            const float dh = nch > 0 ? 0.5f * pw(len_of(chunk_of(0))) : 0.f;
-            const float2 d2 = make_float2(dh, dh);
-#pragma unroll 1
-            for (int g = 0; g < 4; ++g) {
-                float x[16];
+        auto state_row = [&](float *base, long idx) {  // this thread's 32 values of a state
+            return reinterpret_cast<float4 *>(base + ((idx * H + h) * D + r) * D + vs * DV + c0);
+        };
+        // V tile of the chunk processed at step j, part 1: max |v| of the
+        // row segment (published for the tile's scale), Vhat hi/lo.  Keeps the
+        // bf16 values in xv for part 2.
+        uint4 xv[4];
+        auto vtile_hat = [&](int j) -> bool {
+            const int st = j & 1;
+            if (!warp_wait(bar(cs.full_v[st]), (j >> 1) & 1, abort_flag)) return false;
+            const int Lc = len_of(chunk_of(j));
+            const bool live = r < Lc;
+            const uint32_t row = vslot(st) + r * 128;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const float4 f = src[4 * g + c];
-                    x[4 * c] = f.x;
-                    x[4 * c + 1] = f.y;
-                    x[4 * c + 2] = f.z;
-                    x[4 * c + 3] = f.w;
+            for (int m = 0; m < 4; ++m) xv[m] = ld_shared_v4(row + piece(m));
+            {  // max |v| (bf16 magnitudes, packed)
+                uint32_t mbits = 0;
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    mbits = __vmaxu2(__vmaxu2(mbits, xv[m].x & 0x7fff7fffu), xv[m].y & 0x7fff7fffu);
+                    mbits = __vmaxu2(__vmaxu2(mbits, xv[m].z & 0x7fff7fffu), xv[m].w & 0x7fff7fffu);
                 }
-                if (dst) {  // empty sequence: the state is the cached one
+                if (!live) mbits = 0;
+                float mx = fmaxf(__uint_as_float(mbits << 16), __uint_as_float(mbits & 0xffff0000u));
 #pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        dst[4 * g + c] = make_float4(x[4 * c], x[4 * c + 1], x[4 * c + 2], x[4 * c + 3]);
+                for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                if (lane == 0)
+                    st_shared_f32(vmax_s + 4u * (uint32_t)((j & 1) * kWorkWarps + warp - kWorkWarp0),
+                                  mx);
+                mbar_arrive(bar(cs.vmax_ready[j & 1]));
+            }
+            // Vhat: lambda^(Lc-1-l) split as g_hi + g_lo (bf16 each) so that
+            // the packed bf16 FMAs give hi + lo = v g to about 16 bits
+            const float g = live ? pw(kAnti ? r : Lc - 1 - r) : 0.f;
+            const __nv_bfloat16 ghb = __float2bfloat16_rn(g);
+            const __nv_bfloat16 glb = __float2bfloat16_rn(g - __bfloat162float(ghb));
+            const __nv_bfloat162 gh = __halves2bfloat162(ghb, ghb);
+            const __nv_bfloat162 gl = __halves2bfloat162(glb, glb);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const uint32_t w[4] = {xv[m].x, xv[m].y, xv[m].z, xv[m].w};
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const __nv_bfloat162 v2 = *reinterpret_cast<const __nv_bfloat162 *>(&w[q]);
+                    const __nv_bfloat162 h2 = __hmul2(v2, gh);
+                    // exact residual of the rounded product, plus the g_lo term
+                    __nv_bfloat162 l2 = __hfma2(v2, gh, __hneg2(h2));
+                    l2 = __hfma2(v2, gl, l2);
+                    hi[q] = *reinterpret_cast<const uint32_t *>(&h2);
+                    lo[q] = *reinterpret_cast<const uint32_t *>(&l2);
                 }
-#pragma unroll
-                for (int c2 = 0; c2 < 2; ++c2) {  // smem 16-byte chunks 2g, 2g + 1
-                    const int c = 2 * g + c2;
-                    const uint32_t phys = (uint32_t)(c ^ (r & 7));
-                    uint32_t hi[4], lo[4];
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        const uint32_t ua = __float_as_uint(x[8 * c2 + 2 * m]);
-                        const uint32_t ub = __float_as_uint(x[8 * c2 + 2 * m + 1]);
-                        hi[m] = __byte_perm(ua, ub, 0x7632);
-                        const float2 l2 =
-                            f2_sub(make_float2(__uint_as_float(ua), __uint_as_float(ub)),
-                                   make_float2(__uint_as_float(ua & 0xffff0000u),
-                                               __uint_as_float(ub & 0xffff0000u)));
-                        lo[m] = __byte_perm(__float_as_uint(l2.x), __float_as_uint(l2.y), 0x7632);
-                    }
-                    st_shared_v4(kvb + r * 128 + phys * 16, hi[0], hi[1], hi[2], hi[3]);
-                    st_shared_v4(kvb + kHalf + r * 128 + phys * 16, lo[0], lo[1], lo[2], lo[3]);
-                }
-                if (nch > 0) {
-                    uint32_t w[16];
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const float2 y = f2_mul(make_float2(x[2 * c], x[2 * c + 1]), d2);
-                        w[2 * c] = __float_as_uint(y.x);
-                        w[2 * c + 1] = __float_as_uint(y.y);
-                    }
-                    tmem_st16(tkv + 16 * g, w);
-                    tmem_st16(tkv + 64 + 16 * g, w);
-                }
+                st_shared_v4(vha + r * 128 + piece(m), hi[0], hi[1], hi[2], hi[3]);
+                st_shared_v4(vha + kHalf + r * 128 + piece(m), lo[0], lo[1], lo[2], lo[3]);
             }
             fence_proxy_async_smem();
-            tmem_wait_st();
+            return true;
+        };
+        // part 2: V itself, written back in place as fp16 with the tile's
+        // power-of-two scale; rows past the chunk end become zero
+        auto vtile_f16 = [&](int j) -> bool {
+            if (!warp_wait(bar(cs.vmax_ready[j & 1]), (j >> 1) & 1, abort_flag)) return false;
+            const uint32_t vm = vmax_s + 4u * (uint32_t)((j & 1) * kWorkWarps);
+            const uint4 ma = ld_shared_v4(vm), mb = ld_shared_v4(vm + 16);
+            const float mt = fmaxf(
+                fmaxf(fmaxf(__uint_as_float(ma.x), __uint_as_float(ma.y)),
+                      fmaxf(__uint_as_float(ma.z), __uint_as_float(ma.w))),
+                fmaxf(fmaxf(__uint_as_float(mb.x), __uint_as_float(mb.y)),
+                      fmaxf(__uint_as_float(mb.z), __uint_as_float(mb.w))));
+            // no scale when the tile is comfortably inside fp16's normal
+            // range, else 2^-f with max |v| 2^-f in [2^14, 2^15)
+            const int f = (mt <= 1024.f && mt >= 0.0625f) ? 0 : fp16_scale_exp(mt, 14);
+            if (threadIdx.x == kWorkWarp0 * 32) st_shared_f32(vscale_s + 4u * (uint32_t)(j & 3), exp2i(f));
+            const bool live = r < len_of(chunk_of(j));
+            const float sc = live ? exp2i(-f) : 0.f;
+            const float2 sc2 = make_float2(sc, sc);
+            const uint32_t row = vslot(j & 1) + r * 128;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const uint32_t w[4] = {xv[m].x, xv[m].y, xv[m].z, xv[m].w};
+                uint32_t hv[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float2 y = f2_mul(make_float2(__uint_as_float(w[q] << 16),
+                                                        __uint_as_float(w[q] & 0xffff0000u)),
+                                            sc2);
+                    hv[q] = pack_f16(y.x, y.y);
+                }
+                st_shared_v4(row + piece(m), hv[0], hv[1], hv[2], hv[3]);
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(bar(cs.pv_ready[j & 1]));
+            return true;
+        };
+
+        // ---- prologue: the initial state, chunk 0's V tile ----
+        if (has_init) {
+            // KV_{-1} = S0: row r, this thread's 32 value columns
+            const float4 *src = state_row(const_cast<float *>(initial_state), s);
+            float4 *dst = (nch == 0 && final_state) ? state_row(final_state, s) : nullptr;
+            float x[32];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const float4 f = src[c];
+                x[4 * c] = f.x;
+                x[4 * c + 1] = f.y;
+                x[4 * c + 2] = f.z;
+                x[4 * c + 3] = f.w;
+            }
+            if (dst) {  // empty sequence: the state is the cached one
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    dst[c] = make_float4(x[4 * c], x[4 * c + 1], x[4 * c + 2], x[4 * c + 3]);
+            }
+            store_kv_copy(x);
+            if (nch > 0) write_back(x, pw(len_of(chunk_of(0))));
         } else {
             // KV_{-1} = 0
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                st_shared_v4(kvb + r * 128 + c * 16, 0u, 0u, 0u, 0u);
-                st_shared_v4(kvb + kHalf + r * 128 + c * 16, 0u, 0u, 0u, 0u);
+            for (int m = 0; m < 4; ++m) {
+                st_shared_v4(kvb + r * 128 + piece(m), 0u, 0u, 0u, 0u);
+                st_shared_v4(kvb + kHalf + r * 128 + piece(m), 0u, 0u, 0u, 0u);
             }
             fence_proxy_async_smem();
         }
         tc_fence_before();
-        mbar_arrive(bar(cs.o2_ready));   // Q_0 KV_{-1} may go
-        mbar_arrive(bar(cs.dkv_ready));  // dKV_0 accumulates onto lambda^{B_0} S0 (or overwrites)
+        mbar_arrive(bar(cs.o2_ready));  // Q_0 KV_{-1} may go
+        bool ok = true;
+        if (nch > 0) {
+            ok = vtile_hat(0);
+            if (ok) {
+                tc_fence_before();
+                mbar_arrive(bar(cs.dkv_ready));  // dKV_0 accumulates onto lambda^{B_0} S0 (or overwrites)
+                ok = vtile_f16(0);
+            }
+        }
 
-        for (int i = 0; i < nch; ++i) {
+        for (int i = 0; ok && i < nch; ++i) {
             const int st = i & 1;
             const uint32_t sph = (i >> 1) & 1, ph = i & 1;
             const int Lc = len_of(chunk_of(i));
@@ -769,70 +865,66 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             // ---- fold ----
             if (!warp_wait(bar(cs.dkv_full), ph, abort_flag)) break;
             tc_fence_after();
-            float kv[DV];
-            tmem_ld32(tkv, *reinterpret_cast<float(*)[32]>(&kv[0]));
-            tmem_ld32(tkv + 32, *reinterpret_cast<float(*)[32]>(&kv[32]));
-            tmem_wait_ld();
-#pragma unroll
-            for (int hh = 0; hh < 4; ++hh) {
-                float b[16];
-                tmem_ld16(tkv + 64 + 16 * hh, b);
+            float kv[32];
+            {
+                float b[32];
+                tmem_ld32(tkv, kv);
+                tmem_ld32(tkv + 64, b);
                 tmem_wait_ld();
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const float2 x = f2_add(make_float2(kv[16 * hh + 2 * c], kv[16 * hh + 2 * c + 1]),
+                for (int c = 0; c < 16; ++c) {
+                    const float2 x = f2_add(make_float2(kv[2 * c], kv[2 * c + 1]),
                                             make_float2(b[2 * c], b[2 * c + 1]));
-                    kv[16 * hh + 2 * c] = x.x;
-                    kv[16 * hh + 2 * c + 1] = x.y;
+                    kv[2 * c] = x.x;
+                    kv[2 * c + 1] = x.y;
                 }
             }
             if constexpr (kSnap) {
                 // the state after the first (i + 1) B tokens closes a block
                 const int end = (i + 1) * kCS;
                 if (end <= L && end % snap_interval == 0) {
-                    float4 *dst = reinterpret_cast<float4 *>(
-                        snapshots +
-                        (((long)(cs.snap_base + end / snap_interval - 1) * H + h) * D + r) * D +
-                        vs * DV);
+                    float4 *dst = state_row(snapshots, cs.snap_base + end / snap_interval - 1);
 #pragma unroll
-                    for (int c = 0; c < DV / 4; ++c)
+                    for (int c = 0; c < 8; ++c)
                         dst[c] = make_float4(kv[4 * c], kv[4 * c + 1], kv[4 * c + 2], kv[4 * c + 3]);
                 }
             }
             if (!last) {
                 write_back(kv, pw(len_of(chunk_of(i + 1))));
             } else if (final_state) {
-                float4 *dst = reinterpret_cast<float4 *>(final_state + (((long)s * H + h) * D + r) * D + vs * DV);
+                float4 *dst = state_row(final_state, s);
 #pragma unroll
-                for (int c = 0; c < DV / 4; ++c)
+                for (int c = 0; c < 8; ++c)
                     dst[c] = make_float4(kv[4 * c], kv[4 * c + 1], kv[4 * c + 2], kv[4 * c + 3]);
             }
-            tc_fence_before();
-            mbar_arrive(bar(cs.dkv_ready));
             if (loader && i + 2 < nch) load_k(i + 2);
             __syncwarp();
-            // ---- copy ----
+            // ---- V tile of the next chunk ----
+            if (!last) {
+                // Vhat_{i+1} may overwrite Vhat_i: dKV_i has finished
+                if (!vtile_hat(i + 1)) break;
+                tc_fence_before();
+                mbar_arrive(bar(cs.dkv_ready));
+                if (!vtile_f16(i + 1)) break;
+            }
+            // ---- copy, O2 ----
             if (!warp_wait(bar(cs.o2_full), ph, abort_flag)) break;
             tc_fence_after();
             if (!last) store_kv_copy(kv);
             if (loader && i + 2 < nch) load_q(i + 2);
             __syncwarp();
-            // ---- O2 ----
-            float o2[DV];
-            tmem_ld32(to2, *reinterpret_cast<float(*)[32]>(&o2[0]));
-            tmem_ld32(to2 + 32, *reinterpret_cast<float(*)[32]>(&o2[32]));
-            tmem_wait_ld();
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
+            float o2[32];
+            {
                 float b[32];
-                tmem_ld32(to2 + 64 + 32 * hh, b);
+                tmem_ld32(to2, o2);
+                tmem_ld32(to2 + 64, b);
                 tmem_wait_ld();
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
-                    const float2 x = f2_add(make_float2(o2[32 * hh + 2 * c], o2[32 * hh + 2 * c + 1]),
+                    const float2 x = f2_add(make_float2(o2[2 * c], o2[2 * c + 1]),
                                             make_float2(b[2 * c], b[2 * c + 1]));
-                    o2[32 * hh + 2 * c] = x.x;
-                    o2[32 * hh + 2 * c + 1] = x.y;
+                    o2[2 * c] = x.x;
+                    o2[2 * c + 1] = x.y;
                 }
             }
             tc_fence_before();
@@ -847,31 +939,41 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             // (G is zero before the first step, when chunk c may be short)
             const float qf = kAnti ? pw(kCS - r) : pw(r + 1);
             const float2 s12 = make_float2(s1, s1), qf2 = make_float2(qf, qf);
-            const long orow_t = (long)(t0 + chunk_of(i) * kCS + r);
-            uint4 *orow = reinterpret_cast<uint4 *>(out + (orow_t * H + h) * D +
-                                                    vs * DV);
+            float a[32];
+            tmem_ld32(tmem + lane_off + st * 128 + 64 + c0, a);
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(bar(cs.s_free[st]));  // all TMEM reads of this chunk are done
+            uint32_t w[16];
 #pragma unroll
-            for (int hh = 0; hh < 4; ++hh) {
-                float a[16];
-                tmem_ld16(tmem + lane_off + st * 128 + 64 + 16 * hh, a);
-                tmem_wait_ld();
-                if (hh == 3) {  // all TMEM reads of this chunk are done
-                    tc_fence_before();
-                    mbar_arrive(bar(cs.s_free[st]));
-                }
-                uint32_t w[8];
-#pragma unroll
-                for (int m = 0; m < 8; ++m) {
-                    const float2 y = f2_fma(
-                        qf2, make_float2(o2[16 * hh + 2 * m], o2[16 * hh + 2 * m + 1]),
-                        f2_mul(s12, make_float2(a[2 * m], a[2 * m + 1])));
-                    w[m] = pack_bf16(y.x, y.y);
-                }
-                if (r < Lc) {
-                    orow[2 * hh] = make_uint4(w[0], w[1], w[2], w[3]);
-                    orow[2 * hh + 1] = make_uint4(w[4], w[5], w[6], w[7]);
-                }
+            for (int m = 0; m < 16; ++m) {
+                const float2 y = f2_fma(qf2, make_float2(o2[2 * m], o2[2 * m + 1]),
+                                        f2_mul(s12, make_float2(a[2 * m], a[2 * m + 1])));
+                w[m] = pack_bf16(y.x, y.y);
             }
+            // Lanes 2k and 2k+1 (rows r and r+1) swap halves so that each
+            // store instruction writes whole 64-byte row pieces: the first
+            // writes row 2k (the even lane its bytes 0-31, the odd lane the
+            // even lane's bytes 32-63), the second row 2k+1; 16 rows per
+            // instruction instead of 32 half sectors.
+            const bool odd = lane & 1;
+            uint32_t mine[8], other[8];
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                const uint32_t send = odd ? w[m] : w[8 + m];  // even: bytes 32-63; odd: 0-31
+                other[m] = __shfl_xor_sync(0xffffffffu, send, 1);
+                mine[m] = odd ? w[8 + m] : w[m];
+            }
+            const int rbase = wq * 32 + (lane & ~1);
+            const long trow = (long)(t0 + chunk_of(i) * kCS + rbase);
+            __nv_bfloat16 *o0 = out + (trow * H + h) * D + vs * DV + c0 + (odd ? 16 : 0);
+            __nv_bfloat16 *o1 = o0 + (long)H * D;
+            // row rbase: even lane's own low half, odd lane the received high half;
+            // row rbase + 1: even lane the received low half, odd lane its own high half
+            const uint32_t *r0 = odd ? other : mine;
+            const uint32_t *r1 = odd ? mine : other;
+            if (rbase < Lc) st_global_32B(o0, r0, out32);
+            if (rbase + 1 < Lc) st_global_32B(o1, r1, out32);
         }
         if (loader) {  // never leave with a load still landing in shared memory
             int no_abort = 0;
@@ -882,109 +984,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         }
         __syncwarp();
         if (nch == 0 && final_state && !has_init) {  // empty sequence: the state stays zero
-            float4 *dst = reinterpret_cast<float4 *>(final_state + (((long)s * H + h) * D + r) * D + vs * DV);
+            float4 *dst = state_row(final_state, s);
 #pragma unroll
-            for (int c = 0; c < DV / 4; ++c) dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-    } else if (warp < kVWarp0 + 4) {
-        // ================= V-tile warpgroup =================
-        // Chunk i's V tile, one row (token) per thread, read from shared
-        // memory once into registers, then:
-        //  0. max |v| of the row, exchanged among the four warps (for the
-        //     tile's fp16 scale) while step 1 runs;
-        //  1. Vhat = Lambda_K V as a hi/lo bf16 pair for the dKV MMA (Vhat_i
-        //     may be written once dKV_{i-1} has read Vhat_{i-1});
-        //  2. V itself, written back in place as fp16 with the chunk's
-        //     power-of-two scale, for the P V MMA.
-        // Rows past the chunk end are zero in both.
-        const int w4 = warp - kVWarp0;
-        const int vr = w4 * 32 + lane;
-        const uint32_t vha = sb + kOffVhat;
-        for (int i = 0; i < nch; ++i) {
-            const int st = i & 1;
-            if (!warp_wait(bar(cs.full_v[st]), (i >> 1) & 1, abort_flag)) break;
-            const int Lc = len_of(chunk_of(i));
-            const bool live = vr < Lc;
-            const uint32_t row = vslot(st) + vr * 128;
-            // 16-byte pieces in the row's swizzled order (conflict-free)
-            uint4 x[8];
-#pragma unroll
-            for (int c = 0; c < 8; ++c) x[c] = ld_shared_v4(row + (uint32_t)((c + vr) & 7) * 16);
-            // ---- 0: max |v| (bf16 magnitudes, packed)
-            {
-                uint32_t mbits = 0;
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    mbits = __vmaxu2(__vmaxu2(mbits, x[c].x & 0x7fff7fffu), x[c].y & 0x7fff7fffu);
-                    mbits = __vmaxu2(__vmaxu2(mbits, x[c].z & 0x7fff7fffu), x[c].w & 0x7fff7fffu);
-                }
-                if (!live) mbits = 0;
-                float m = fmaxf(__uint_as_float(mbits << 16), __uint_as_float(mbits & 0xffff0000u));
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-                if (lane == 0) st_shared_f32(vmax_s + 4u * (uint32_t)((i & 1) * 4 + w4), m);
-                mbar_arrive(bar(cs.vmax_ready[i & 1]));
-            }
-            // ---- 1: Vhat.  lambda^(Lc-1-l) split as g_hi + g_lo (bf16
-            // each) so that the packed bf16 FMAs give hi + lo = v g to ~16
-            // bits.
-            if (i > 0 && !warp_wait(bar(cs.dkv_full), (i - 1) & 1, abort_flag)) break;
-            {
-                const float g = live ? pw(kAnti ? vr : Lc - 1 - vr) : 0.f;
-                const __nv_bfloat16 ghb = __float2bfloat16_rn(g);
-                const __nv_bfloat16 glb = __float2bfloat16_rn(g - __bfloat162float(ghb));
-                const __nv_bfloat162 gh = __halves2bfloat162(ghb, ghb);
-                const __nv_bfloat162 gl = __halves2bfloat162(glb, glb);
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const uint32_t ch = (uint32_t)((c + vr) & 7) * 16;
-                    const uint32_t w[4] = {x[c].x, x[c].y, x[c].z, x[c].w};
-                    uint32_t hi[4], lo[4];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const __nv_bfloat162 v2 = *reinterpret_cast<const __nv_bfloat162 *>(&w[q]);
-                        const __nv_bfloat162 h2 = __hmul2(v2, gh);
-                        // exact residual of the rounded product, plus the g_lo term
-                        __nv_bfloat162 l2 = __hfma2(v2, gh, __hneg2(h2));
-                        l2 = __hfma2(v2, gl, l2);
-                        hi[q] = *reinterpret_cast<const uint32_t *>(&h2);
-                        lo[q] = *reinterpret_cast<const uint32_t *>(&l2);
-                    }
-                    st_shared_v4(vha + vr * 128 + ch, hi[0], hi[1], hi[2], hi[3]);
-                    st_shared_v4(vha + kHalf + vr * 128 + ch, lo[0], lo[1], lo[2], lo[3]);
-                }
-                fence_proxy_async_smem();
-                mbar_arrive(bar(cs.dkv_ready));
-            }
-            // ---- 2: fp16 V for P V
-            if (!warp_wait(bar(cs.vmax_ready[i & 1]), (i >> 1) & 1, abort_flag)) break;
-            const uint32_t vm = vmax_s + 16u * (uint32_t)(i & 1);
-            const float mt = fmaxf(fmaxf(ld_shared_f32(vm), ld_shared_f32(vm + 4)),
-                                   fmaxf(ld_shared_f32(vm + 8), ld_shared_f32(vm + 12)));
-            // no scale when the tile is comfortably inside fp16's normal
-            // range, else 2^-f with max |v| 2^-f in [2^14, 2^15); rows past
-            // the chunk end become zero
-            const int f = (mt <= 1024.f && mt >= 0.0625f) ? 0 : fp16_scale_exp(mt, 14);
-            if (threadIdx.x == kVWarp0 * 32)
-                st_shared_f32(vscale_s + 4u * (uint32_t)(i & 3), exp2i(f));
-            const float sc = live ? exp2i(-f) : 0.f;
-            const float2 sc2 = make_float2(sc, sc);
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const uint32_t ch = (uint32_t)((c + vr) & 7) * 16;
-                const uint32_t w[4] = {x[c].x, x[c].y, x[c].z, x[c].w};
-                uint32_t hv[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float2 y = f2_mul(make_float2(__uint_as_float(w[q] << 16),
-                                                        __uint_as_float(w[q] & 0xffff0000u)),
-                                            sc2);
-                    hv[q] = pack_f16(y.x, y.y);
-                }
-                st_shared_v4(row + ch, hv[0], hv[1], hv[2], hv[3]);
-            }
-            fence_proxy_async_smem();
-            mbar_arrive(bar(cs.pv_ready[st]));
+            for (int c = 0; c < 8; ++c) dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
     }
 

@@ -45,10 +45,10 @@
 //                quadrants with the most blocks below the diagonal
 //   warps 4-11   workers, two threads per row (token / state row), each with
 //                32 of the 64 value columns: KV fold + write-back, the V tile
-//                (Vhat hi/lo, fp16 V), KV copy, output; worker thread 0 also
-//                issues the TMA loads of the K ring
+//                (Vhat hi/lo, fp16 V), KV copy, output
 //   warp  12     MMA stream A (one thread): S and P V; TMA loads of the V ring
-//   warp  13     MMA stream B (one thread): dKV and Q KV; TMA loads of the Q ring
+//   warp  13     MMA stream B (one thread): dKV and Q KV; TMA loads of the Q
+//                and K rings
 // (the anti-causal instantiation swaps warps 12/13 with 14/15: its heavy
 // mask quadrants are 0 and 1, and a helper must sit on its quadrant)
 // Each ring slot is reloaded, by a role that waits for that event anyway, as
@@ -396,13 +396,22 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             warp_wait(bar(cs.full_v[c & 1]), (c >> 1) & 1, &no_abort);
     } else if (warp == R::mma_b) {
         // ================= MMA stream B: dKV and Q KV =================
-        // Also the Q ring: slot c & 1 is reloaded for chunk c as soon as
-        // S_{c-2} and Q_{c-2} KV_{c-3} (issued here) have finished, a whole
-        // chunk before S_c needs it.
+        // Also the Q and K rings: slot c & 1 is reloaded for chunk c as soon
+        // as the MMAs of chunk c - 2 reading it have finished (S and Q KV for
+        // Q, S and dKV for K; dKV and Q KV are issued here, Q KV last), a
+        // whole chunk before S_c needs it.
         const uint32_t vha = sb + kOffVhat, kvb = sb + kOffKVb;
         int nq = 0;
-        auto load_q = [&](int c) -> bool {
+        auto load_qk = [&](int c) -> bool {
             const int st = c & 1;
+            if (!warp_wait(bar(cs.empty_k[st]), ((c >> 1) & 1) ^ 1, abort_flag)) return false;
+            if (elect_one()) {
+                mbar_arrive_expect_tx(bar(cs.full_k[st]), 2 * kHalf);
+                const int row = t0 + chunk_of(c) * kCS;
+                tma_load_2d(kslot(st), &tmK, bar(cs.full_k[st]), h * D, row);
+                tma_load_2d(kslot(st) + kHalf, &tmK, bar(cs.full_k[st]), h * D + 64, row);
+            }
+            __syncwarp();
             if (!warp_wait(bar(cs.empty_q[st]), ((c >> 1) & 1) ^ 1, abort_flag)) return false;
             if (elect_one()) {
                 mbar_arrive_expect_tx(bar(cs.full_q[st]), 2 * kHalf);
@@ -414,9 +423,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             ++nq;
             return true;
         };
-        if (elect_one()) tma_prefetch_desc(&tmQ);
+        if (elect_one()) {
+            tma_prefetch_desc(&tmQ);
+            tma_prefetch_desc(&tmK);
+        }
         __syncwarp();
-        for (int c = 0; c < min(nch, 2); ++c) load_q(c);
+        for (int c = 0; c < min(nch, 2); ++c) load_qk(c);
         for (int i = 0; i < nch; ++i) {
             const int st = i & 1;
             const uint32_t sph = (i >> 1) & 1, ph = i & 1;
@@ -447,14 +459,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
                 mma_commit(bar(cs.empty_q[st]));
             }
             __syncwarp();
-            if (i + 2 < nch && !load_q(i + 2)) break;
+            if (i + 2 < nch && !load_qk(i + 2)) break;
         }
         if (elect_one()) mma_commit(bar(cs.done_b));
         __syncwarp();
         int no_abort = 0;
         warp_wait(bar(cs.done_b), 0, &no_abort);
-        for (int c = max(0, nq - 2); c < nq; ++c)  // no load may still be landing
+        for (int c = max(0, nq - 2); c < nq; ++c) {  // no load may still be landing
+            warp_wait(bar(cs.full_k[c & 1]), (c >> 1) & 1, &no_abort);
             warp_wait(bar(cs.full_q[c & 1]), (c >> 1) & 1, &no_abort);
+        }
     } else if (warp < kMaskWarps || warp == R::help2 || warp == R::help3) {
         // ================= mask warps: S -> P =================
         // Row j of the chunk is TMEM lane j; the warps of lane quadrant q
@@ -654,7 +668,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         //   out:    once P_i V_i has finished, o = 2^(e + f) O1 + lambda^(r+1) O2.
         // Splitting the value columns between two threads per row halves the
         // latency of each step; the steps that gate the next MMA come first.
-        // Worker thread 0 also issues the TMA loads of the K ring.
         const int wq = warp & 3;
         const int half = (warp - kWorkWarp0) >> 2;
         const int r = wq * 32 + lane;
@@ -666,28 +679,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         // byte offset of the row's 16-byte piece 4 half + m (value columns
         // c0 + 8m .. c0 + 8m + 7) in a 128-byte swizzled row
         auto piece = [&](int m) { return (uint32_t)(((4 * half + m) ^ (r & 7)) * 16); };
-        // K ring (worker thread 0): slot c & 1 is reloaded for chunk c once S
-        // and dKV of chunk c - 2 have finished; the fold step of chunk c - 2
-        // waits for dKV anyway, and S was issued before.
-        const bool loader = threadIdx.x == kWorkWarp0 * 32;
-        int nk = 0;
-        auto load_k = [&](int c) -> bool {
-            const int st = c & 1;
-            if (!mbar_wait(bar(cs.empty_k[st]), ((c >> 1) & 1) ^ 1, abort_flag, kTimeoutNs))
-                return false;
-            mbar_arrive_expect_tx(bar(cs.full_k[st]), 2 * kHalf);
-            const int row = t0 + chunk_of(c) * kCS;
-            tma_load_2d(kslot(st), &tmK, bar(cs.full_k[st]), h * D, row);
-            tma_load_2d(kslot(st) + kHalf, &tmK, bar(cs.full_k[st]), h * D + 64, row);
-            ++nk;
-            return true;
-        };
-        if (loader) {
-            tma_prefetch_desc(&tmK);
-            for (int c = 0; c < min(nch, 2); ++c)
-                if (!load_k(c)) break;
-        }
-        __syncwarp();
         // hi/lo bf16 copy of 8 state values: hi = x with the low 16 bits
         // cleared (a bf16, exact); lo = x - hi (exact in fp32), also
         // truncated: hi + lo = x to about 2^-14 relative
@@ -907,8 +898,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
                 for (int c = 0; c < 8; ++c)
                     dst[c] = make_float4(kv[4 * c], kv[4 * c + 1], kv[4 * c + 2], kv[4 * c + 3]);
             }
-            if (loader && i + 2 < nch) load_k(i + 2);
-            __syncwarp();
             // ---- V tile of the next chunk ----
             if (!last) {
                 // Vhat_{i+1} may overwrite Vhat_i: dKV_i has finished
@@ -983,12 +972,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             if (rbase < Lc) st_global_32B(o0, r0, out32);
             if (rbase + 1 < Lc) st_global_32B(o1, r1, out32);
         }
-        if (loader) {  // never leave with a load still landing in shared memory
-            int no_abort = 0;
-            for (int c = max(0, nk - 2); c < nk; ++c)
-                mbar_wait(bar(cs.full_k[c & 1]), (c >> 1) & 1, &no_abort, kTimeoutNs);
-        }
-        __syncwarp();
         if (nch == 0 && final_state && !has_init) {  // empty sequence: the state stays zero
             float4 *dst = state_row(final_state, s);
 #pragma unroll

@@ -78,11 +78,14 @@ typedef enum la_dtype {
  * head_dim     64 or 128.
  * chunk        block size B: 0 picks the default for the path
  *              (128 on the tensor-core path, 64 otherwise).  The
- *              tensor-core path (bf16, head_dim 128) takes 16, 32, 64 or 128
- *              (its tiles are 128 tokens; a smaller block runs as masked
- *              tiles advancing B tokens, at 128 / B times the tensor-core
- *              work); the fp32 / head_dim 64 CUDA-core path takes 16, 32 or
- *              64; 256 has no kernel (LA_ERR_UNSUPPORTED).  The result does
+ *              tensor-core path (bf16, head_dim 128) takes 16, 32, 64, 128
+ *              or 256 (its tiles are 128 tokens; a smaller block runs as
+ *              masked tiles advancing B tokens, at 128 / B times the
+ *              tensor-core work; a 256-token block as two tiles whose
+ *              coupling term goes through the state after the first, the
+ *              same sum regrouped); the fp32 / head_dim 64 CUDA-core path
+ *              takes 16, 32 or 64 (128 and 256: LA_ERR_UNSUPPORTED).  The
+ *              result does
  *              not depend on B beyond rounding (K3 report reading notes, CP
  *              for linear attention: any chunk split is mathematically
  *              equivalent).

@@ -205,7 +205,7 @@ def backward(q, k, v, decay, cu_seqlens, dout, *, chunk: int = 0, dq=None, dk=No
     :func:`prefill`; ``workspace`` is a uint8 CUDA tensor of at least
     :func:`backward_workspace_bytes` bytes, needed on the CUDA-core path
     only (allocated here when None); the tensor-core path (bf16, d = 128,
-    chunk 0, 16, 32, 64 or 128) runs without one.
+    chunk 0, 16, 32, 64, 128 or 256) runs without one.
     """
     if q.dim() != 3:
         raise ValueError("q must be [T, H, d]")
@@ -223,7 +223,7 @@ def backward(q, k, v, decay, cu_seqlens, dout, *, chunk: int = 0, dq=None, dk=No
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(q) if dk is None else dk
     dv = torch.empty_like(q) if dv is None else dv
-    tensor_cores = q.dtype == torch.bfloat16 and d == 128 and int(chunk) in (0, 16, 32, 64, 128)
+    tensor_cores = q.dtype == torch.bfloat16 and d == 128 and int(chunk) in (0, 16, 32, 64, 128, 256)
     if workspace is None and not tensor_cores:
         need = backward_workspace_bytes(T, H, d, q.dtype)
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)

@@ -44,10 +44,9 @@ la_status run_prefill(const la::PrefillArgs &a, la_dtype dtype) {
     if (tc) return from_cuda(la::prefill_tc_bf16(a), "prefill (tcgen05)");
     if (a.anti_causal)
         return fail(LA_ERR_UNSUPPORTED, "the anti-causal form runs on the tensor-core path only");
-    if (a.chunk == 256)
-        return fail(LA_ERR_UNSUPPORTED, "chunk 256: no kernel (the tensor-core tile is 128 tokens)");
-    if (a.chunk == 128)
-        return fail(LA_ERR_UNSUPPORTED, "chunk 128 needs the tensor-core path (bf16, head_dim 128)");
+    if (a.chunk == 128 || a.chunk == 256)
+        return fail(LA_ERR_UNSUPPORTED, "chunk %d needs the tensor-core path (bf16, head_dim 128)",
+                    a.chunk);
     if (dtype == LA_DTYPE_FP32) return from_cuda(la::prefill_simt_f32(a), "prefill (fp32)");
     return from_cuda(la::prefill_simt_bf16(a), "prefill (bf16, CUDA cores)");
 }
@@ -185,10 +184,9 @@ la_status lightning_attn_prefill_snapshots(const void *q, const void *k, const v
     // the kernel that serves the call and its block
     const bool tc = la::uses_tensor_cores(dtype == LA_DTYPE_BF16, head_dim, chunk);
     const int block = chunk != 0 ? chunk : tc ? 128 : 64;
-    if (chunk == 256)
-        return fail(LA_ERR_UNSUPPORTED, "chunk 256: no kernel (the tensor-core tile is 128 tokens)");
-    if (!tc && chunk == 128)
-        return fail(LA_ERR_UNSUPPORTED, "chunk 128 needs the tensor-core path (bf16, head_dim 128)");
+    if (!tc && (chunk == 128 || chunk == 256))
+        return fail(LA_ERR_UNSUPPORTED, "chunk %d needs the tensor-core path (bf16, head_dim 128)",
+                    chunk);
     if (snapshot_interval % block != 0)
         return fail(LA_ERR_INVALID_ARG,
                     "snapshot_interval %d is not a multiple of the block (%d tokens) this "

@@ -53,10 +53,11 @@ struct DecodeArgs {
 };
 
 // Whether a (scalar-decay) call runs on the tensor-core kernel: bf16,
-// head_dim 128 and a block size of 16, 32, 64 or 128 (chunk 0 = 128).
+// head_dim 128 and a block size of 16, 32, 64, 128 or 256 (chunk 0 = 128).
 inline bool uses_tensor_cores(bool bf16, int head_dim, int chunk) {
     return bf16 && head_dim == 128 &&
-           (chunk == 0 || chunk == 16 || chunk == 32 || chunk == 64 || chunk == 128);
+           (chunk == 0 || chunk == 16 || chunk == 32 || chunk == 64 || chunk == 128 ||
+            chunk == 256);
 }
 
 // CUDA-core chunkwise prefill; chunk in {16, 32, 64}, head_dim in {64, 128};
@@ -64,7 +65,7 @@ inline bool uses_tensor_cores(bool bf16, int head_dim, int chunk) {
 cudaError_t prefill_simt_f32(const PrefillArgs &a);
 cudaError_t prefill_simt_bf16(const PrefillArgs &a);
 
-// tcgen05 / TMEM / TMA prefill; bf16, head_dim 128, block size 16-128.
+// tcgen05 / TMEM / TMA prefill; bf16, head_dim 128, block size 16-256.
 // Returns cudaErrorNotSupported when the tensor-map encoder is unavailable.
 cudaError_t prefill_tc_bf16(const PrefillArgs &a);
 

@@ -1050,9 +1050,18 @@ TcKernel pick_kernel(bool anti, bool snap) {
 
 }  // namespace
 
+// A block of 256 tokens (the MiniMax-01 report's block, §3.2 and §3.3.3) is
+// computed as two 128-row tiles: the term that couples its halves,
+// [(Q_b K_a^T) (.) M] V_a for the second half b and the first half a, is
+// taken through the state carried after a, Lambda_Q Q_b (Lambda_K K_a)^T V_a,
+// which is the same sum regrouped (equal in exact arithmetic), and the
+// block's state update lambda^256 KV + (Lambda_K K)^T V is the two tile
+// updates composed.  A 256-row left product in one piece would need a third
+// 128-column S tile in TMEM, whose 512 columns already hold two S tiles, O2
+// and the state.
 cudaError_t prefill_tc_bf16(const PrefillArgs &a) {
     const int cs = a.chunk == 0 ? BC : a.chunk;  // the method's block size
-    if (a.head_dim != D || (cs != 128 && cs != 64 && cs != 32 && cs != 16))
+    if (a.head_dim != D || (cs != 256 && cs != 128 && cs != 64 && cs != 32 && cs != 16))
         return cudaErrorNotSupported;
     // rows are written in place; the anti-causal kernel starts from a zero state
     if (a.reverse_out || (a.anti_causal && a.initial_state)) return cudaErrorNotSupported;
@@ -1067,7 +1076,7 @@ cudaError_t prefill_tc_bf16(const PrefillArgs &a) {
     const bool snap = a.snapshots != nullptr;
     if (snap && (a.anti_causal || a.snapshot_interval <= 0 || a.snapshot_interval % cs != 0))
         return cudaErrorNotSupported;
-    const int csi = cs == 128 ? 0 : cs == 64 ? 1 : cs == 32 ? 2 : 3;
+    const int csi = cs >= 128 ? 0 : cs == 64 ? 1 : cs == 32 ? 2 : 3;
     const TcKernel kern = csi == 0   ? pick_kernel<128>(a.anti_causal, snap)
                           : csi == 1 ? pick_kernel<64>(a.anti_causal, snap)
                           : csi == 2 ? pick_kernel<32>(a.anti_causal, snap)

@@ -117,10 +117,11 @@ def test_backward_writes_stay_inside_gradients():
         assert_close(x, r, TOL_BF16, f"guarded {name}")
 
 
-@pytest.mark.parametrize("chunk", [32, 64])
+@pytest.mark.parametrize("chunk", [32, 64, 256])
 def test_tensor_core_backward_block_sizes(chunk):
     """The anti-causal launches with 32- and 64-token blocks (128-row tiles
-    advancing one block at a time, walked last to first)."""
+    advancing one block at a time, walked last to first) and 256-token blocks
+    (two tiles each)."""
     got, ref = run([1, 0, 31, 33, 64, 65, 200, 129], 3, 128, torch.bfloat16, chunk, 28)
     for x, r, name in zip(got, ref, ("dq", "dk", "dv")):
         assert_close(x, r, TOL_BF16, f"tc B={chunk} {name}")

@@ -86,10 +86,10 @@ def test_bf16_cuda_core_d64(chunk):
     check(out, st, ref, ref_st, TOL_BF16, what=f"bf16 d=64 B={chunk}")
 
 
-@pytest.mark.parametrize("chunk", [0, 64])
+@pytest.mark.parametrize("chunk", [0, 64, 256])
 def test_bf16_d128_paths(chunk):
-    """chunk 0 (tensor cores, block 128) and chunk 64 (tensor cores, 64-token
-    blocks in 128-row tiles) both match."""
+    """chunk 0 (tensor cores, block 128), chunk 64 (64-token blocks in
+    128-row tiles) and chunk 256 (256-token blocks as two tiles) all match."""
     inp, out, st, ref, ref_st = run_case([1000, 1, 2049], 8, 128, torch.bfloat16,
                                          chunk=chunk, seed=4)
     check(out, st, ref, ref_st, TOL_BF16, what=f"bf16 d=128 chunk={chunk}")
@@ -129,7 +129,7 @@ def test_chunk_invariance():
         assert rel_err(s, outs[0][1]) < 1e-5
     qb, kb, vb = (t.to(torch.bfloat16) for t in (inp.q, inp.k, inp.v))
     of, sf = la.prefill(qb.float(), kb.float(), vb.float(), inp.decay, inp.cu_seqlens, chunk=64)
-    for c in (128, 64, 32, 16):  # the tensor-core kernel at every block size
+    for c in (256, 128, 64, 32, 16):  # the tensor-core kernel at every block size
         ob, sb = la.prefill(qb, kb, vb, inp.decay, inp.cu_seqlens, chunk=c)
         assert_close(ob, of, TOL_BF16, f"tc B={c} vs fp32 B=64")
         assert_close(sb, sf, TOL_BF16, f"tc B={c} vs fp32 B=64 state")

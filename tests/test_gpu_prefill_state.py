@@ -68,6 +68,7 @@ def test_quadratic_form_agrees_with_state():
 
 
 @pytest.mark.parametrize("dtype, chunk, tol", [(torch.bfloat16, 128, TOL_BF16),
+                                               (torch.bfloat16, 256, TOL_BF16),
                                                (torch.float32, 64, TOL_FP32)])
 def test_two_segment_continuation(dtype, chunk, tol):
     """prefill(A) then prefill(B | final state of A) == one pass over A + B."""

@@ -52,6 +52,7 @@ def prefix_states(inp, lengths, interval, s0):
 @pytest.mark.parametrize("dtype, d, chunk, interval, with_state, tol", [
     (torch.bfloat16, 128, 0, 128, True, TOL_BF16),    # tensor cores, every block
     (torch.bfloat16, 128, 128, 256, False, TOL_BF16),  # tensor cores, every second block
+    (torch.bfloat16, 128, 256, 256, True, TOL_BF16),   # tensor cores, 256-token blocks
     (torch.bfloat16, 128, 64, 64, True, TOL_BF16),     # tensor cores, 64-token blocks
     (torch.float32, 128, 64, 128, True, TOL_FP32),     # CUDA cores
     (torch.float32, 64, 32, 64, False, TOL_FP32),

@@ -66,15 +66,10 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
     return ok != 0;
 }
 
-// Waits for the phase with the given parity to complete.  Gives up (returns
-// false) when *abort becomes non-zero or after timeout_ns; on a timeout it
-// sets *abort so the other roles of the CTA stop too.
-// Waiting threads sleep in try_wait (woken when the phase completes), so a
-// waiting warp does not take issue slots from working warps of its SM
-// sub-partition; they wake at least every 0.2 ms to check the deadline.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
-                                          uint64_t timeout_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
+// The waiting part of mbar_wait, out of line: the timer loop appears once in
+// the kernel instead of at every wait, which keeps the hot loops compact.
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int *abort,
+                                           uint64_t timeout_ns) {
     const uint64_t t0 = globaltimer_ns();
 #pragma unroll 1
     while (true) {
@@ -85,6 +80,17 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
             return false;
         }
     }
+}
+// Waits for the phase with the given parity to complete.  Gives up (returns
+// false) when *abort becomes non-zero or after timeout_ns; on a timeout it
+// sets *abort so the other roles of the CTA stop too.
+// Waiting threads sleep in try_wait (woken when the phase completes), so a
+// waiting warp does not take issue slots from working warps of its SM
+// sub-partition; they wake at least every 0.2 ms to check the deadline.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
+                                          uint64_t timeout_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, abort, timeout_ns);
 }
 
 // ------------------------------------------------------- packed fp32 pairs

@@ -34,8 +34,10 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = ("prefill tokens/s + % bf16 tensor peak; decode tokens/s + % HBM BW (1×GB300)")
-PREFILL_KERNEL_SRC = os.path.join(ROOT, "lightning_attention_attn_gb300", "csrc", "prefill_tc.cu")
-DECODE_KERNEL_SRC = os.path.join(ROOT, "lightning_attention_attn_gb300", "csrc", "decode.cu")
+# the files a kernel's code comes from (its traffic record is void once any changes)
+_CSRC = os.path.join(ROOT, "lightning_attention_attn_gb300", "csrc")
+PREFILL_KERNEL_SRC = [os.path.join(_CSRC, f) for f in ("prefill_tc.cu", "sm100_ptx.cuh")]
+DECODE_KERNEL_SRC = [os.path.join(_CSRC, "decode.cu")]
 
 
 # ---------------------------------------------------------------- helpers
@@ -66,9 +68,12 @@ def cuda_core_roofline(flops, byts, ms, pk, sms):
             "hbm_frac": round(byts / (ms / 1e3) / 1e9 / pk["hbm"], 4)}
 
 
-def src_hash(path):
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def src_hash(paths):
+    h = hashlib.sha256()
+    for path in paths:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def ncu_traffic(kernel_key, src):

@@ -184,6 +184,26 @@ def test_writes_stay_inside_outputs(dtype, chunk):
     assert_close(fs, ref_st, tol)
 
 
+@pytest.mark.parametrize("offset_elems", [0, 8])
+def test_tensor_core_output_alignment(offset_elems):
+    """The tensor-core kernel writes output rows with 256-bit stores when out
+    is 32-byte aligned and with 128-bit stores when it is only 16-byte
+    aligned (offset 8 bf16 elements); both give the same bits, inside guard
+    regions."""
+    lengths, H, d = [5, 200, 129, 300], 4, 128
+    inp = wl.prefill_inputs(lengths, H, d, dtype=torch.bfloat16, seed=14, device="cuda")
+    T, G = inp.total_tokens, 4096
+    big = torch.full((T * H * d + 2 * G + 64,), 12345.0, dtype=torch.bfloat16, device="cuda")
+    base = G + offset_elems
+    out = big[base:base + T * H * d].view(T, H, d)
+    assert (out.data_ptr() % 32 == 0) == (offset_elems == 0)
+    ref_out, _ = la.prefill(inp.q, inp.k, inp.v, inp.decay, inp.cu_seqlens)
+    la.prefill(inp.q, inp.k, inp.v, inp.decay, inp.cu_seqlens, out=out)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref_out)
+    assert (big[:base] == 12345.0).all() and (big[base + T * H * d:] == 12345.0).all()
+
+
 def test_many_sequences_natural_order():
     """More sequences than the in-kernel length sort handles (natural order)."""
     g = torch.Generator().manual_seed(9)

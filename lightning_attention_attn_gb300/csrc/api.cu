@@ -240,6 +240,9 @@ la_status lightning_attn_prefill_channel_decay(const void *q, const void *k, con
                       head_dim, chunk, out, final_state, static_cast<cudaStream_t>(stream),
                       initial_state};
     a.channel_decay = true;
+    // bf16 with head_dim 128 and 64-token blocks: the tensor-core kernel
+    if (dtype == LA_DTYPE_BF16 && head_dim == 128 && (chunk == 0 || chunk == 64))
+        return from_cuda(la::prefill_cw_tc_bf16(a), "prefill (channel-wise decay, tcgen05)");
     if (dtype == LA_DTYPE_FP32)
         return from_cuda(la::prefill_simt_f32(a), "prefill (channel-wise decay, fp32)");
     return from_cuda(la::prefill_simt_bf16(a), "prefill (channel-wise decay, bf16)");
@@ -498,10 +501,13 @@ la_status lightning_attn_mixed_step(const void *q, const void *k, const void *v,
 }
 
 la_status lightning_attn_device_status(void *stream) {
-    unsigned int err = 0;
-    const la_status st =
+    unsigned int err = 0, err_cw = 0;
+    la_status st =
         from_cuda(la::take_device_error(static_cast<cudaStream_t>(stream), &err), "device_status");
     if (st != LA_OK) return st;
+    st = from_cuda(la::take_cw_device_error(&err_cw), "device_status");
+    if (st != LA_OK) return st;
+    err |= err_cw;
     if (err) return fail(LA_ERR_TIMEOUT, "a bounded device-side wait gave up");
     return LA_OK;
 }

@@ -69,6 +69,14 @@ cudaError_t prefill_simt_bf16(const PrefillArgs &a);
 // Returns cudaErrorNotSupported when the tensor-map encoder is unavailable.
 cudaError_t prefill_tc_bf16(const PrefillArgs &a);
 
+// tcgen05 / TMEM / TMA prefill with the channel-wise decay; bf16, head_dim
+// 128, block size 64 (chunk 0 or 64), scalar-decay features (snapshots,
+// anti-causal, mixed-step ranks) excluded.
+cudaError_t prefill_cw_tc_bf16(const PrefillArgs &a);
+// Reads and clears the channel-wise kernel's device error word (the caller
+// has synchronised the stream).
+cudaError_t take_cw_device_error(unsigned int *err);
+
 // Synchronises `stream`, then reads and clears the device error word.
 cudaError_t take_device_error(cudaStream_t stream, unsigned int *err);
 // Launches a kernel whose bounded wait must time out after timeout_ns.

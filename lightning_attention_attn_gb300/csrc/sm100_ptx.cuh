@@ -68,7 +68,7 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
 
 // The waiting part of mbar_wait, out of line: the timer loop appears once in
 // the kernel instead of at every wait, which keeps the hot loops compact.
-__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int *abort,
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int *abort,
                                            uint64_t timeout_ns) {
     const uint64_t t0 = globaltimer_ns();
 #pragma unroll 1

@@ -69,6 +69,83 @@ def test_channel_decay_extreme_decays(chunk):
     assert_close(st, ref_st, TOL_FP32, f"extreme channel decays B={chunk} state")
 
 
+# ---------------------------------------- the tensor-core kernel (bf16, d=128, B=64)
+RAGGED_TC = [1, 0, 15, 16, 17, 31, 33, 63, 64, 65, 127, 129, 200, 0, 513]
+
+
+@pytest.mark.parametrize("with_state", [False, True])
+def test_channel_decay_tensor_core_ragged(with_state):
+    """Ragged packed sequences (empty, shorter than a sub-block, across
+    sub-block and block edges) through the tcgen05 kernel, with and without
+    cached states."""
+    H, d = 4, 128
+    inp = wl.prefill_inputs(RAGGED_TC, H, d, dtype=torch.bfloat16, seed=57, device="cuda")
+    lam = channel_decays(H, d, 58)
+    s0 = wl.cached_states(len(RAGGED_TC), H, d, seed=59, device="cuda") if with_state else None
+    out, st = la.prefill_channel_decay(inp.q, inp.k, inp.v, lam.cuda(), inp.cu_seqlens,
+                                       initial_state=s0)
+    torch.cuda.synchronize()
+    la.device_status()
+    ref, ref_st = oracle.recurrent_cw(inp.q, inp.k, inp.v, lam, inp.cu_seqlens.cpu(),
+                                      initial_state=None if s0 is None else s0.cpu())
+    assert_close(out, ref, TOL_BF16, f"tc channel decay state={with_state} out")
+    assert_close(st, ref_st, TOL_BF16, f"tc channel decay state={with_state} state")
+
+
+@pytest.mark.parametrize("pattern", ["one_and_tiny", "near_one", "spread_small"])
+def test_channel_decay_tensor_core_extreme_decays(pattern):
+    """Channel decays at the extremes on the tcgen05 kernel: lambda = 1 next to
+    lambda = 1e-30 (every power above the first underflows), all near 1 (long
+    memory, the largest state), and spread down to 1e-3.  Only non-negative
+    exponents are formed, so nothing overflows and no NaN appears."""
+    H, d = 2, 128
+    inp = wl.prefill_inputs([300, 3, 64, 129], H, d, dtype=torch.bfloat16, seed=60, device="cuda")
+    lam = channel_decays(H, d, 61)
+    if pattern == "one_and_tiny":
+        lam[:, 0::3] = 1.0
+        lam[:, 1::3] = 1e-30
+    elif pattern == "near_one":
+        lam = 1.0 - 1e-3 * torch.rand((H, d), generator=torch.Generator().manual_seed(62))
+    else:
+        lam = 10.0 ** (-3.0 * torch.rand((H, d), generator=torch.Generator().manual_seed(63)))
+    lam = lam.to(torch.float32)
+    out, st = la.prefill_channel_decay(inp.q, inp.k, inp.v, lam.cuda(), inp.cu_seqlens)
+    torch.cuda.synchronize()
+    la.device_status()
+    assert torch.isfinite(out.float()).all() and torch.isfinite(st).all()
+    ref, ref_st = oracle.recurrent_cw(inp.q, inp.k, inp.v, lam, inp.cu_seqlens.cpu())
+    assert_close(out, ref, TOL_BF16, f"tc extreme channel decays ({pattern}) out")
+    assert_close(st, ref_st, TOL_BF16, f"tc extreme channel decays ({pattern}) state")
+
+
+def test_channel_decay_tensor_core_layer_heads():
+    """A 64-head, 4096-token layer (the measured layer's shape, shorter): every
+    head, every token and the final states."""
+    H, d = 64, 128
+    inp = wl.prefill_inputs([4096], H, d, dtype=torch.bfloat16, seed=64, device="cuda")
+    lam = inp.decay.cpu()[:, None].repeat(1, d)
+    lam = (lam * (1.0 - 0.01 * torch.linspace(0, 1, d))[None, :]).to(torch.float32)
+    out, st = la.prefill_channel_decay(inp.q, inp.k, inp.v, lam.cuda(), inp.cu_seqlens)
+    torch.cuda.synchronize()
+    la.device_status()
+    ref, ref_st = oracle.recurrent_cw(inp.q, inp.k, inp.v, lam, inp.cu_seqlens.cpu())
+    assert_close(out, ref, TOL_BF16, "tc channel decay 64 heads out")
+    assert_close(st, ref_st, TOL_BF16, "tc channel decay 64 heads state")
+
+
+def test_channel_decay_tensor_core_matches_cuda_cores():
+    """The tcgen05 kernel (chunk 64) and the CUDA-core kernel (chunk 32) agree
+    to the bf16 bound on the same inputs."""
+    H, d = 3, 128
+    inp = wl.prefill_inputs([700, 129], H, d, dtype=torch.bfloat16, seed=65, device="cuda")
+    lam = channel_decays(H, d, 66).cuda()
+    a, sa = la.prefill_channel_decay(inp.q, inp.k, inp.v, lam, inp.cu_seqlens, chunk=64)
+    b, sb = la.prefill_channel_decay(inp.q, inp.k, inp.v, lam, inp.cu_seqlens, chunk=32)
+    torch.cuda.synchronize()
+    assert_close(a, b.double(), TOL_BF16, "tc vs cuda-core channel decay out", u=2.0 ** -7)
+    assert_close(sa, sb.double(), TOL_BF16, "tc vs cuda-core channel decay state")
+
+
 def test_channel_decay_uniform_equals_scalar_kernel():
     """Equal channel decays give the scalar-decay result (CUDA-core path)."""
     H, d = 4, 128

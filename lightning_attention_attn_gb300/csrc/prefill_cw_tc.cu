@@ -68,7 +68,13 @@ constexpr int NVS = D / DV;  // value slices per head
 constexpr int BC = 64;       // block size
 constexpr int kThreads = 512;
 constexpr int kMaxExp = 64;  // largest exponent of lambda used
+// Diagonal sub-blocks factor around their middle (exponents -8 .. 8) with
+// mu = max(lambda, 2^-12): every factor stays below 2^96 in magnitude.
+constexpr float kMuMin = 1.0f / 4096.0f;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
+// Issuing warps, both idle during the diagonal sums: warp 12 (lane quadrant
+// 0) issues S, P V and the TMA loads; warp 14 issues Q~ KV and the state update.
+constexpr int kWarpS = 12, kWarpKV = 14;
 
 // Shared memory (offsets from a 1024-byte aligned base).  Every operand uses
 // 128-byte swizzled rows of 64 16-bit values in 8-row, 1024-byte atoms; a
@@ -85,9 +91,13 @@ constexpr uint32_t kOffKt = kOffKh + 2 * kKhHalf;    // K~ hi, then K~ lo (MN-ma
 constexpr uint32_t kOffKVb = kOffKt + 4 * kPiece;    // state copy: hi atom, lo atom (16 KB each)
 constexpr uint32_t kKVAtom = D * 128;
 constexpr uint32_t kOffPw = kOffKVb + 2 * kKVAtom;   // pw[e][i] = lambda_i^e, fp32
-constexpr uint32_t kPwBytes = (kMaxExp + 1) * D * 4;
-constexpr uint32_t kOffDg = kOffPw + kPwBytes;       // diagonal scores [4][16][16] fp32
-constexpr uint32_t kOffCtrl = kOffDg + 4 * 16 * 16 * 4;
+constexpr uint32_t kPwRow = D;
+constexpr uint32_t kPwBytes = (kMaxExp + 1) * kPwRow * 4;
+// pd[e + 8][i] = mu_i^e, e = -8 .. 8, mu_i = max(lambda_i, 2^-12): the factors
+// of the diagonal sub-blocks (rows padded so that rows start on different banks)
+constexpr uint32_t kOffPd = kOffPw + kPwBytes;
+constexpr uint32_t kPdRow = D + 4;
+constexpr uint32_t kOffCtrl = kOffPd + 17 * kPdRow * 4;
 // The Q^ and Q~ MMAs read 128 rows of which only 0..63 are the block's; rows
 // 64..127 of each half fall on the next 8 KB, which is always inside the
 // buffers above (results of those rows are never used).
@@ -108,10 +118,12 @@ constexpr uint32_t kColPl = 128;  // 32: P lo
 constexpr uint32_t kColO1 = 160;  // 64: P V
 constexpr uint32_t kColO2 = 224;  // 128: Q~ [KV_hi | KV_lo]
 constexpr uint32_t kColKV = 352;  // 64: state
+constexpr uint32_t kColSd = 416;  // 64: scores of the diagonal sub-blocks
 constexpr uint32_t kTmemCols = 512;
 __host__ __device__ constexpr uint32_t slab_col(int m) { return m == 0 ? 0u : m == 1 ? 48u : 80u; }
 
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 96, 0, 0);   // Q^ (K-major) x K^ (K-major)
+constexpr uint32_t kIdescSd = idesc_bf16_f32(128, 64, 0, 0);  // Q'' (K-major) x K'' (K-major)
 constexpr uint32_t kIdescO2 = idesc_bf16_f32(128, 128, 0, 1); // Q~ (K-major) x KV (N-major)
 constexpr uint32_t kIdescKV = idesc_bf16_f32(128, 64, 1, 1);  // K~^T (M-major) x V (N-major)
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 64, 0, 1);  // P (TMEM) x V (N-major)
@@ -200,9 +212,9 @@ prefill_cw_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     auto len_of = [&](int c) { return min(BC, L - c * BC); };
     const bool has_init = initial_state != nullptr;
     auto bar = [&](const uint64_t &b) { return smem_u32(&b); };
-    const uint32_t pw_s = sb + kOffPw;  // lambda_i^e at pw_s + 4 (e D + i)
+    const uint32_t pw_s = sb + kOffPw;  // lambda_i^e at pw_s + 4 (e kPwRow + i)
     const float *pw = reinterpret_cast<const float *>(base + kOffPw);
-    float *dg = reinterpret_cast<float *>(base + kOffDg);
+    const uint32_t pd_s = sb + kOffPd;  // mu_i^e at pd_s + 4 ((e + 8) kPdRow + i)
     volatile int *abort_flag = &cs.abort;
 
     // ---- set-up ----
@@ -213,7 +225,7 @@ prefill_cw_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         mbar_init(bar(cs.s_done), 1);
         mbar_init(bar(cs.mma_done), 1);
         mbar_init(bar(cs.pv_done), 1);
-        mbar_init(bar(cs.drained), 1);
+        mbar_init(bar(cs.drained), 2);  // one commit per issuing warp
         cs.abort = 0;
         fence_mbar_init();
     }
@@ -221,7 +233,13 @@ prefill_cw_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         float *pwm = reinterpret_cast<float *>(base + kOffPw);
         for (int idx = tid; idx < (kMaxExp + 1) * D; idx += kThreads) {
             const int e = idx / D, i = idx % D;
-            pwm[idx] = powf(__ldg(decay + h * D + i), (float)e);
+            pwm[e * kPwRow + i] = powf(__ldg(decay + h * D + i), (float)e);
+        }
+        float *pdm = reinterpret_cast<float *>(base + kOffPd);
+        for (int idx = tid; idx < 17 * D; idx += kThreads) {
+            const int e = idx / D - 8, i = idx % D;
+            const float mu = fmaxf(__ldg(decay + h * D + i), kMuMin);
+            pdm[(e + 8) * kPdRow + i] = powf(mu, (float)e);
         }
     }
     if (warp == 0) {
@@ -234,7 +252,9 @@ prefill_cw_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     const uint32_t tmem = __shfl_sync(0xffffffffu, cs.tmem_base, 0);
     const bool tmem_ok = tmem == 0;  // an allocation of all 512 columns starts at 0
 
-    int n_qk = 0, n_v = 0;  // loads issued (thread 0)
+    // TMA loads: issued by one elected lane of warp kWarpS; every lane of
+    // that warp keeps the counts
+    int n_qk = 0, n_v = 0;
     auto load_qk = [&](int c) {
         mbar_arrive_expect_tx(bar(cs.full_qk), 4 * kPiece);
         const int row = t0 + c * BC;
@@ -242,22 +262,25 @@ prefill_cw_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         tma_load_2d(sb + kOffQ + kPiece, &tmQ, bar(cs.full_qk), h * D + 64, row);
         tma_load_2d(sb + kOffK, &tmK, bar(cs.full_qk), h * D, row);
         tma_load_2d(sb + kOffK + kPiece, &tmK, bar(cs.full_qk), h * D + 64, row);
-        ++n_qk;
     };
     auto load_v = [&](int c) {
         const int st = c & 1;
         mbar_arrive_expect_tx(bar(cs.full_v[st]), kPiece);
         tma_load_2d(sb + kOffV + st * kPiece, &tmV, bar(cs.full_v[st]), h * D + vs * DV,
                     t0 + c * BC);
-        ++n_v;
     };
-    if (tid == 0 && tmem_ok && nch > 0) {
-        tma_prefetch_desc(&tmQ);
-        tma_prefetch_desc(&tmK);
-        tma_prefetch_desc(&tmV);
-        load_qk(0);
-        load_v(0);
-        if (nch > 1) load_v(1);
+    if (warp == kWarpS && tmem_ok && nch > 0) {
+        if (elect_one()) {
+            tma_prefetch_desc(&tmQ);
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
+            load_qk(0);
+            load_v(0);
+            if (nch > 1) load_v(1);
+        }
+        __syncwarp();
+        n_qk = 1;
+        n_v = nch > 1 ? 2 : 1;
     }
 
     // ---- the state before the first block: KV_{-1} = S0 or 0 ----
@@ -285,7 +308,7 @@ prefill_cw_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     };
     // lambda_i^e kv into the state accumulator
     auto write_back = [&](const float(&kv)[16], int e) {
-        const float g = pw[e * D + srow];
+        const float g = pw[e * kPwRow + srow];
         uint32_t w[16];
 #pragma unroll
         for (int m = 0; m < 16; ++m) w[m] = __float_as_uint(kv[m] * g);
@@ -332,20 +355,29 @@ prefill_cw_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         cw_wait(bar(cs.full_qk), ph, abort_flag);
         cw_wait(bar(cs.full_v[c & 1]), (c >> 1) & 1, abort_flag);
 
-        // ---- B: derived operands and the diagonal sub-block scores ----
+        // ---- B: derived operands ----
         // Q items: (row j, 8-channel piece cc), two per thread
 #pragma unroll 1
         for (int it = tid; it < BC * 16; it += kThreads) {
             const int j = it >> 4, cc = it & 15;
             const uint32_t off = swz(j, cc, kPiece);
             uint32_t qh[4] = {0u, 0u, 0u, 0u}, th[4] = {0u, 0u, 0u, 0u}, tl[4] = {0u, 0u, 0u, 0u};
+            uint32_t qd2[4] = {0u, 0u, 0u, 0u};
             if (j < Lc) {
                 float q[8];
                 unpack8(ld_shared_v4(sb + kOffQ + off), q);
-                const float4 a0 = ld_shared_f4(pw_s + 4u * (uint32_t)((j & 15) * D + 8 * cc));
-                const float4 a1 = ld_shared_f4(pw_s + 4u * (uint32_t)((j & 15) * D + 8 * cc + 4));
-                const float4 b0 = ld_shared_f4(pw_s + 4u * (uint32_t)((j + 1) * D + 8 * cc));
-                const float4 b1 = ld_shared_f4(pw_s + 4u * (uint32_t)((j + 1) * D + 8 * cc + 4));
+                {  // Q''_j = q_j mu^(j mod 16 - 8), over the raw row
+                    const uint32_t r = pd_s + 4u * (uint32_t)((j & 15) * kPdRow + 8 * cc);
+                    const float4 m0 = ld_shared_f4(r), m1 = ld_shared_f4(r + 16);
+                    const float gm[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+#pragma unroll
+                    for (int m = 0; m < 4; ++m)
+                        qd2[m] = pack_bf16_rn(q[2 * m] * gm[2 * m], q[2 * m + 1] * gm[2 * m + 1]);
+                }
+                const float4 a0 = ld_shared_f4(pw_s + 4u * (uint32_t)((j & 15) * kPwRow + 8 * cc));
+                const float4 a1 = ld_shared_f4(pw_s + 4u * (uint32_t)((j & 15) * kPwRow + 8 * cc + 4));
+                const float4 b0 = ld_shared_f4(pw_s + 4u * (uint32_t)((j + 1) * kPwRow + 8 * cc));
+                const float4 b1 = ld_shared_f4(pw_s + 4u * (uint32_t)((j + 1) * kPwRow + 8 * cc + 4));
                 const float ga[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
                 const float gb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
@@ -355,6 +387,7 @@ prefill_cw_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 }
             }
             st_shared_v4(sb + kOffQh + off, qh[0], qh[1], qh[2], qh[3]);
+            st_shared_v4(sb + kOffQ + off, qd2[0], qd2[1], qd2[2], qd2[3]);
             st_shared_v4(sb + kOffQt + off, th[0], th[1], th[2], th[3]);
             st_shared_v4(sb + kOffQt + 2 * kPiece + off, tl[0], tl[1], tl[2], tl[3]);
         }
@@ -366,12 +399,24 @@ prefill_cw_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             const bool live = l < Lc;
             float k[8];
             unpack8(ld_shared_v4(sb + kOffK + off), k);
+            {  // K''_l = k_l mu^(8 - l mod 16), over the raw row
+                uint32_t kd2[4] = {0u, 0u, 0u, 0u};
+                if (live) {
+                    const uint32_t r = pd_s + 4u * (uint32_t)((16 - (l & 15)) * kPdRow + 8 * cc);
+                    const float4 m0 = ld_shared_f4(r), m1 = ld_shared_f4(r + 16);
+                    const float gm[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+#pragma unroll
+                    for (int m = 0; m < 4; ++m)
+                        kd2[m] = pack_bf16_rn(k[2 * m] * gm[2 * m], k[2 * m + 1] * gm[2 * m + 1]);
+                }
+                st_shared_v4(sb + kOffK + off, kd2[0], kd2[1], kd2[2], kd2[3]);
+            }
             {
                 uint32_t th[4] = {0u, 0u, 0u, 0u}, tl[4] = {0u, 0u, 0u, 0u};
                 if (live) {
                     const int e = Lc - 1 - l;
-                    const float4 b0 = ld_shared_f4(pw_s + 4u * (uint32_t)(e * D + 8 * cc));
-                    const float4 b1 = ld_shared_f4(pw_s + 4u * (uint32_t)(e * D + 8 * cc + 4));
+                    const float4 b0 = ld_shared_f4(pw_s + 4u * (uint32_t)(e * kPwRow + 8 * cc));
+                    const float4 b1 = ld_shared_f4(pw_s + 4u * (uint32_t)(e * kPwRow + 8 * cc + 4));
                     const float gb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
                     for (int m = 0; m < 4; ++m)
@@ -387,8 +432,8 @@ prefill_cw_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 uint32_t kh[4] = {0u, 0u, 0u, 0u};
                 if (live) {
                     const int e = 16 * m + 16 - (l & 15);
-                    const float4 a0 = ld_shared_f4(pw_s + 4u * (uint32_t)(e * D + 8 * cc));
-                    const float4 a1 = ld_shared_f4(pw_s + 4u * (uint32_t)(e * D + 8 * cc + 4));
+                    const float4 a0 = ld_shared_f4(pw_s + 4u * (uint32_t)(e * kPwRow + 8 * cc));
+                    const float4 a1 = ld_shared_f4(pw_s + 4u * (uint32_t)(e * kPwRow + 8 * cc + 4));
                     const float ga[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
 #pragma unroll
                     for (int u = 0; u < 4; ++u)
@@ -397,104 +442,68 @@ prefill_cw_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 st_shared_v4(sb + kOffKh + swz(n, cc, kKhHalf), kh[0], kh[1], kh[2], kh[3]);
             }
         }
-        // Diagonal sub-blocks: thread = (sub-block b, 4 x 4 tile t, channel
-        // group g of 16); the eight channel groups of a tile are consecutive
-        // lanes and are summed with shuffles.
-        {
-            const int g = tid & 7, t = (tid >> 3) & 15, b = tid >> 7;
-            const int tj = t >> 2, tl = t & 3;
-            float acc[4][4];
-#pragma unroll
-            for (int r = 0; r < 4; ++r)
-#pragma unroll
-                for (int cl = 0; cl < 4; ++cl) acc[r][cl] = 0.f;
-            if (tl <= tj) {
-                const int dlt = 4 * (tj - tl);  // j - l = dlt + r - cl
-#pragma unroll 1
-                for (int u = 0; u < 2; ++u) {  // 8 channels at a time
-                    const int cc = 2 * g + u;  // piece of channels 8 cc .. 8 cc + 7
-                    float qv[4][8], kv[4][8];
-#pragma unroll
-                    for (int r = 0; r < 4; ++r) {
-                        const int j = 16 * b + 4 * tj + r, l = 16 * b + 4 * tl + r;
-                        unpack8(ld_shared_v4(sb + kOffQ + swz(j, cc, kPiece)), qv[r]);
-                        unpack8(ld_shared_v4(sb + kOffK + swz(l, cc, kPiece)), kv[r]);
-                    }
-#pragma unroll
-                    for (int dd = -3; dd <= 3; ++dd) {
-                        const int e = dlt + dd;
-                        if (e < 0) continue;  // above the diagonal: masked later
-                        const float4 w0 = ld_shared_f4(pw_s + 4u * (uint32_t)(e * D + 8 * cc));
-                        const float4 w1 = ld_shared_f4(pw_s + 4u * (uint32_t)(e * D + 8 * cc + 4));
-                        const float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-                        for (int r = 0; r < 4; ++r) {
-                            const int cl = r - dd;
-                            if (cl < 0 || cl > 3) continue;
-#pragma unroll
-                            for (int x = 0; x < 8; ++x) acc[r][cl] = fmaf(qv[r][x] * kv[cl][x], w[x], acc[r][cl]);
-                        }
-                    }
-                }
-            }
-#pragma unroll
-            for (int r = 0; r < 4; ++r)
-#pragma unroll
-                for (int cl = 0; cl < 4; ++cl) {
-                    float a = acc[r][cl];
-                    a += __shfl_xor_sync(0xffffffffu, a, 1);
-                    a += __shfl_xor_sync(0xffffffffu, a, 2);
-                    a += __shfl_xor_sync(0xffffffffu, a, 4);
-                    acc[r][cl] = a;
-                }
-            if (g == 0) {
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    float *p = dg + (b * 16 + 4 * tj + r) * 16 + 4 * tl;
-                    *reinterpret_cast<float4 *>(p) = make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
-                }
-            }
-        }
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
 
-        // ---- C: the block's MMAs and the next block's loads ----
-        if (tid == 0) {
+        // ---- C: the block's MMAs ----
+        // Each issuing warp is converged and issues from one elected lane, so
+        // the operands are warp-uniform values and each tcgen05.mma is a
+        // single issue.
+        if (warp == kWarpS) {
             tc_fence_after();
-            if (!*abort_flag) {
-                const uint64_t dqh = sdesc_sw128(sb + kOffQh, 16, 1024);
-                const uint64_t dkh = sdesc_sw128(sb + kOffKh, 16, 1024);
+            const bool go_w = __shfl_sync(0xffffffffu, (int)!*abort_flag, 0) != 0;
+            const uint64_t dqh = sdesc_sw128(sb + kOffQh, 16, 1024);
+            const uint64_t dkh = sdesc_sw128(sb + kOffKh, 16, 1024);
+            // (the Q and K load of block c + 1 waits until S has read Q'' and K'')
+            if (go_w && c + 1 < nch && c + 1 >= 2) ++n_v;
+            const uint64_t dqd = sdesc_sw128(sb + kOffQ, 16, 1024);
+            const uint64_t dkd = sdesc_sw128(sb + kOffK, 16, 1024);
+            if (go_w && elect_one()) {
                 mma_group_ss<2, kPiece / 16, 2, kKhHalf / 16>(tmem + kColS, dqh, dkh, kIdescS, 0u);
+                mma_group_ss<2, kPiece / 16, 2, kPiece / 16>(tmem + kColSd, dqd, dkd, kIdescSd, 0u);
                 mma_commit(bar(cs.s_done));
-                const uint64_t dkvb = sdesc_sw128(sb + kOffKVb, kKVAtom, 1024);
-                mma_group_ss<2, kPiece / 16, kMNMajorS1, kMNMajorS2>(
-                    tmem + kColO2, sdesc_sw128(sb + kOffQt, 16, 1024), dkvb, kIdescO2, 0u);
-                mma_group_ss<2, kPiece / 16, kMNMajorS1, kMNMajorS2>(
-                    tmem + kColO2, sdesc_sw128(sb + kOffQt + 2 * kPiece, 16, 1024), dkvb, kIdescO2,
-                    1u);
-                const uint64_t dv = sdesc_sw128(sb + kOffV + (c & 1) * kPiece, kPiece, 1024);
-                const uint64_t dkth = sdesc_sw128(sb + kOffKt, kPiece, 1024);
-                const uint64_t dktl = sdesc_sw128(sb + kOffKt + 2 * kPiece, kPiece, 1024);
+                // V slot (c + 1) & 1 was released by block c - 1's MMAs
+                if (c + 1 < nch && c + 1 >= 2) load_v(c + 1);
+            }
+            __syncwarp();
+        } else if (warp == kWarpKV) {
+            tc_fence_after();
+            const bool go_w = __shfl_sync(0xffffffffu, (int)!*abort_flag, 0) != 0;
+            const uint64_t dkvb = sdesc_sw128(sb + kOffKVb, kKVAtom, 1024);
+            const uint64_t dqth = sdesc_sw128(sb + kOffQt, 16, 1024);
+            const uint64_t dqtl = sdesc_sw128(sb + kOffQt + 2 * kPiece, 16, 1024);
+            const uint64_t dv = sdesc_sw128(sb + kOffV + (c & 1) * kPiece, kPiece, 1024);
+            const uint64_t dkth = sdesc_sw128(sb + kOffKt, kPiece, 1024);
+            const uint64_t dktl = sdesc_sw128(sb + kOffKt + 2 * kPiece, kPiece, 1024);
+            const uint32_t acc0 = (c > 0 || has_init) ? 1u : 0u;
+            if (go_w && elect_one()) {
+                mma_group_ss<2, kPiece / 16, kMNMajorS1, kMNMajorS2>(tmem + kColO2, dqth, dkvb,
+                                                                    kIdescO2, 0u);
+                mma_group_ss<2, kPiece / 16, kMNMajorS1, kMNMajorS2>(tmem + kColO2, dqtl, dkvb,
+                                                                    kIdescO2, 1u);
 #pragma unroll
                 for (uint32_t kk = 0; kk < 4; ++kk)
                     mma_bf16(tmem + kColKV, dkth + 128u * kk, dv + 128u * kk, kIdescKV,
-                             (kk > 0 || c > 0 || has_init) ? 1u : 0u);
+                             kk > 0 ? 1u : acc0);
 #pragma unroll
                 for (uint32_t kk = 0; kk < 4; ++kk)
                     mma_bf16(tmem + kColKV, dktl + 128u * kk, dv + 128u * kk, kIdescKV, 1u);
                 mma_commit(bar(cs.mma_done));
-                // the raw Q and K of this block have been read (step B)
-                if (c + 1 < nch) load_qk(c + 1);
-                // V slot (c + 1) & 1 was released by block c - 1's MMAs
-                if (c + 1 < nch && c + 1 >= 2) load_v(c + 1);
             }
+            __syncwarp();
         }
-
         // ---- D: P from S and the diagonal sums; P V ----
         if (qd < 2) {
             cw_wait(bar(cs.s_done), ph, abort_flag);
             tc_fence_after();
+            if (warp == kWarpS) {  // S has read Q'' and K'' (the raw tiles)
+                if (__shfl_sync(0xffffffffu, (int)!*abort_flag, 0) && c + 1 < nch) {
+                    if (elect_one()) load_qk(c + 1);
+                    __syncwarp();
+                    ++n_qk;
+                }
+            }
             const int j = qd * 32 + lane;  // query row = TMEM lane
             const int bj = j >> 4;
             const int b = wq;               // key sub-block of this warp
@@ -503,24 +512,19 @@ prefill_cw_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             {
                 // the two halves of the warp sit in sub-blocks 2 qd and 2 qd + 1
                 const int m_lo = 2 * qd - b - 1, m_hi = 2 * qd - b;
-                float s_lo[16], s_hi[16];
+                float s_lo[16], s_hi[16], s_d[16];
                 if (m_lo >= 0 && m_lo <= 2) tmem_ld16(srow_t + slab_col(m_lo), s_lo);
                 if (m_hi >= 0 && m_hi <= 2) tmem_ld16(srow_t + slab_col(m_hi), s_hi);
+                if (b == 2 * qd || b == 2 * qd + 1)  // this warp's block is a diagonal one
+                    tmem_ld16(tmem + lane_off + kColSd + 16 * b, s_d);
                 tmem_wait_ld();
                 const bool lo_half = lane < 16;
                 if (b < bj) {
 #pragma unroll
                     for (int x = 0; x < 16; ++x) sv[x] = lo_half ? s_lo[x] : s_hi[x];
                 } else if (b == bj) {
-                    const float *p = dg + (b * 16 + (j & 15)) * 16;
 #pragma unroll
-                    for (int x = 0; x < 16; x += 4) {
-                        const float4 f = *reinterpret_cast<const float4 *>(p + x);
-                        sv[x] = f.x;
-                        sv[x + 1] = f.y;
-                        sv[x + 2] = f.z;
-                        sv[x + 3] = f.w;
-                    }
+                    for (int x = 0; x < 16; ++x) sv[x] = s_d[x];
                 } else {
 #pragma unroll
                     for (int x = 0; x < 16; ++x) sv[x] = 0.f;
@@ -539,10 +543,11 @@ prefill_cw_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             tmem_wait_st();
             tc_fence_before();
             named_barrier_sync(1, 256);
-            if (tid == 0) {
+            if (warp == kWarpS) {
                 tc_fence_after();
-                if (!*abort_flag) {
-                    const uint64_t dv = sdesc_sw128(sb + kOffV + (c & 1) * kPiece, kPiece, 1024);
+                const bool go = !*abort_flag;
+                const uint64_t dv = sdesc_sw128(sb + kOffV + (c & 1) * kPiece, kPiece, 1024);
+                if (__shfl_sync(0xffffffffu, (int)go, 0) && elect_one()) {
 #pragma unroll
                     for (uint32_t kk = 0; kk < 4; ++kk)
                         mma_bf16_tmem_a(tmem + kColO1, tmem + kColPh + 8 * kk, dv + 128u * kk,
@@ -553,6 +558,7 @@ prefill_cw_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                                         kIdescPV, 1u);
                     mma_commit(bar(cs.pv_done));
                 }
+                __syncwarp();
             }
         }
 
@@ -603,9 +609,14 @@ prefill_cw_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     }
 
     // ---- teardown: no copy may still be landing, no MMA still running ----
-    if (tid == 0 && tmem_ok) {
+    if (warp == kWarpKV && tmem_ok) {
+        if (elect_one()) mma_commit(bar(cs.drained));
+        __syncwarp();
+    }
+    if (warp == kWarpS && tmem_ok) {
         int no_abort = 0;
-        mma_commit(bar(cs.drained));
+        if (elect_one()) mma_commit(bar(cs.drained));
+        __syncwarp();
         mbar_wait(bar(cs.drained), 0, &no_abort, kTimeoutNs);
         // the latest load on each barrier (the only ones that can still be
         // in flight after an abort)

@@ -38,6 +38,7 @@ METRIC = ("prefill tokens/s + % bf16 tensor peak; decode tokens/s + % HBM BW (1Ã
 _CSRC = os.path.join(ROOT, "lightning_attention_attn_gb300", "csrc")
 PREFILL_KERNEL_SRC = [os.path.join(_CSRC, f) for f in ("prefill_tc.cu", "sm100_ptx.cuh")]
 DECODE_KERNEL_SRC = [os.path.join(_CSRC, "decode.cu")]
+CW_KERNEL_SRC = [os.path.join(_CSRC, f) for f in ("prefill_cw_tc.cu", "sm100_ptx.cuh")]
 
 
 # ---------------------------------------------------------------- helpers
@@ -386,14 +387,17 @@ def run_ours(args, ws, rank, local):
                              "achieved": round(byts / (ms / 1e3) / 1e9, 1), "peak": pk["hbm"],
                              "unit": "GB/s", "frac": round(byts / (ms / 1e3) / 1e9 / pk["hbm"], 4)}}
 
-    def time_channel_decay(lengths, reps):
+    def time_channel_decay(lengths, reps, chunk=64):
+        """Per-channel decay (lambda_h scaled by 1 - 0.01 i / (d - 1) for key
+        channel i): 64-token blocks run the tcgen05 kernel, 32-token blocks
+        the CUDA-core kernel."""
         pin = wl.prefill_inputs(lengths, H, d, dtype=torch.bfloat16, seed=0, device=dev)
         lam_cw = pin.decay[:, None].repeat(1, d).contiguous()
         lam_cw = lam_cw * (1.0 - 0.01 * torch.linspace(0, 1, d, device=dev))[None, :]
         pout = torch.empty_like(pin.q)
 
         def run():
-            la.prefill_channel_decay(pin.q, pin.k, pin.v, lam_cw, pin.cu_seqlens, chunk=64,
+            la.prefill_channel_decay(pin.q, pin.k, pin.v, lam_cw, pin.cu_seqlens, chunk=chunk,
                                      out=pout, stream=stream)
         run()
         torch.cuda.synchronize()
@@ -404,12 +408,28 @@ def run_ours(args, ws, rank, local):
             run()
         a1.record(stream)
         torch.cuda.synchronize()
+        la.device_status(stream)
         ms = a0.elapsed_time(a1) / reps
         Tn = sum(lengths)
-        byts, flops = prefill_alg(Tn, H, d, 64, len(lengths))
-        return {"ms_per_launch": round(ms, 3), "tokens_per_s": round(Tn / (ms / 1e3), 1),
-                "chunk": 64, "kernel": "prefill_simt_kernel (FFMA), per-channel decay",
-                "roofline": cuda_core_roofline(flops, byts, ms, pk, sms)}
+        byts, flops = prefill_alg(Tn, H, d, chunk, len(lengths))
+        byts -= len(lengths) * H * d * d * 4  # no final state requested
+        byts += H * d * 4                      # the decay table
+        if chunk != 64:
+            return {"ms_per_launch": round(ms, 3), "tokens_per_s": round(Tn / (ms / 1e3), 1),
+                    "chunk": chunk, "kernel": "prefill_simt_kernel (FFMA), per-channel decay",
+                    "roofline": cuda_core_roofline(flops, byts, ms, pk, sms)}
+        return {"ms_per_launch": round(ms, 4), "tokens_per_s": round(Tn / (ms / 1e3), 1),
+                "chunk": chunk, "kernel": "prefill_cw_tc_kernel (tcgen05), per-channel decay",
+                "roofline": {"bound": "hbm", "alg_bytes": byts,
+                             "achieved": round(byts / (ms / 1e3) / 1e9, 1), "peak": pk["hbm"],
+                             "unit": "GB/s", "frac": round(byts / (ms / 1e3) / 1e9 / pk["hbm"], 4),
+                             "traffic": ncu_traffic("prefill_cw_tc_kernel", CW_KERNEL_SRC)},
+                "tensor": {"alg_flops": flops,
+                           "frac_of_bf16_peak": round(flops / (ms / 1e3) / 1e12 / pk["bf16"], 4),
+                           "note": "the tensor pipe runs about 6x the algorithmic flops: hi/lo "
+                                   "operand pairs stacked on the M rows, three decay slabs, "
+                                   "diagonal sub-blocks as whole tiles, and the query-key "
+                                   "products repeated in both value-slice CTAs of a head"}}
 
     def time_snapshots(lengths, interval, reps):
         """Prefill of the layer that also writes the state every `interval`
@@ -445,6 +465,7 @@ def run_ours(args, ws, rank, local):
 
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     more = {"prefill_8k_channel_decay": time_channel_decay([8192], 10),
+            "prefill_8k_channel_decay_cuda_cores": time_channel_decay([8192], 3, chunk=32),
             "prefill_8k_snapshots_every_1024": time_snapshots([8192], 1024, 10),
             "prefill_8k_snapshots_every_128": time_snapshots([8192], 128, 10),
             "prefill_8k_chunk64": time_prefill([8192], 64, 10),
@@ -781,6 +802,10 @@ def run_ours(args, ws, rank, local):
                                   "prefill_128k_chunk64", "prefill_128k",
                                   "prefill_128k_chunk256")},
         "varlen_16_hbm_frac": frac(more.get("varlen_16")),
+        "channel_decay_8k": {
+            "tensor_cores_ms": more["prefill_8k_channel_decay"]["ms_per_launch"],
+            "tensor_cores_hbm_frac": frac(more["prefill_8k_channel_decay"]),
+            "cuda_cores_ms": more["prefill_8k_channel_decay_cuda_cores"]["ms_per_launch"]},
     }
     return line
 
@@ -803,7 +828,7 @@ def run_only(args):
         for _ in range(args.warmup + args.steps):
             la.prefill(inp.q, inp.k, inp.v, inp.decay, inp.cu_seqlens, out=out, final_state=fs)
     elif args.only in ("channel_decay", "prefill_chunk64", "prefill_fp32"):
-        # the 8K-token layer: per-channel decay on the CUDA-core kernel
+        # the 8K-token layer: per-channel decay on the tensor-core kernel
         # (lambda_h scaled by 1 - 0.01 i / (d - 1) for key channel i), the
         # scalar decay with 64-token blocks on the tensor cores, or fp32
         # inputs (chunk 64) on the CUDA-core kernel

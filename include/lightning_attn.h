@@ -178,8 +178,14 @@ int64_t lightning_attn_snapshot_count(const int32_t *cu_seqlens_host, int32_t nu
  *            + sum_i q_t[i] lam_i^(t+1) S0[i][:]  (from a cached state S0).
  * Arguments as for lightning_attn_prefill_with_state, except
  *   decay  [num_heads, head_dim] fp32, each in (0, 1].
- * Runs on the CUDA-core (FFMA) kernel: chunk 0 (= 64), 16, 32 or 64;
- * 128 and 256 return LA_ERR_UNSUPPORTED.
+ * Kernels: bf16 with head_dim 128 and chunk 0 or 64 runs the tensor-core
+ * kernel (64-token blocks; intra-block scores from 16-token sub-blocks whose
+ * decay factors are split between the query and key sides, every operand a
+ * hi/lo bf16 pair but the key side of the off-diagonal scores).  For its
+ * diagonal sub-blocks lambda is raised to 2^-12 where smaller: a score term
+ * at distance 1..15 then moves by less than 2^-12 |q_t[i] k_u[i]|.  Every
+ * other case runs the CUDA-core (FFMA) kernel: chunk 0 (= 64), 16, 32 or 64
+ * (fp32, or head_dim 64); 128 and 256 return LA_ERR_UNSUPPORTED.
  */
 la_status lightning_attn_prefill_channel_decay(const void *q, const void *k, const void *v,
                                                const float *decay, const int32_t *cu_seqlens,

@@ -328,12 +328,13 @@ prefill_cw_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             st_shared_v4(a + kKVAtom, lo[0], lo[1], lo[2], lo[3]);
         }
     };
-    // lambda_i^e kv into the state accumulator (i = srow)
+    // lambda_i^e kv into the state accumulator (i = srow); e is the length
+    // of the next block: BC, or that of the sequence's last block
     const float lam_row = __ldg(lam_h + srow);
     const float lam_row64 = powf(lam_row, (float)BC);
+    const float lam_row_last = nch > 0 ? powf(lam_row, (float)len_of(nch - 1)) : 1.f;
     auto write_back = [&](const float(&kv)[16], int e) {
-        float g = lam_row64;
-        if (e != BC) g = powf(lam_row, (float)e);
+        const float g = e == BC ? lam_row64 : lam_row_last;
         uint32_t w[16];
 #pragma unroll
         for (int m = 0; m < 16; ++m) w[m] = __float_as_uint(kv[m] * g);

@@ -133,6 +133,43 @@ def test_channel_decay_tensor_core_layer_heads():
     assert_close(st, ref_st, TOL_BF16, "tc channel decay 64 heads state")
 
 
+def test_channel_decay_tensor_core_long_varlen_with_states():
+    """Long packed sequences (about 31 K tokens, 8 heads) with cached states:
+    hundreds of blocks per CTA carry the state through the TMEM accumulator
+    and its hi/lo copy; every head, every token and the final states."""
+    H, d = 8, 128
+    lengths = [20000, 7000, 1, 4129]
+    inp = wl.prefill_inputs(lengths, H, d, dtype=torch.bfloat16, seed=67, device="cuda")
+    lam = inp.decay.cpu()[:, None].repeat(1, d)
+    lam = (lam * (1.0 - 0.05 * torch.rand((H, d), generator=torch.Generator().manual_seed(68))))
+    lam = lam.to(torch.float32)
+    s0 = wl.cached_states(len(lengths), H, d, seed=69, device="cuda")
+    out, st = la.prefill_channel_decay(inp.q, inp.k, inp.v, lam.cuda(), inp.cu_seqlens,
+                                       initial_state=s0)
+    torch.cuda.synchronize()
+    la.device_status()
+    ref, ref_st = oracle.recurrent_cw(inp.q, inp.k, inp.v, lam, inp.cu_seqlens.cpu(),
+                                      initial_state=s0.cpu())
+    assert_close(out, ref, TOL_BF16, "tc channel decay long varlen out")
+    assert_close(st, ref_st, TOL_BF16, "tc channel decay long varlen state")
+
+
+def test_channel_decay_tensor_core_many_sequences():
+    """More CTAs than SMs (300 short sequences x 2 heads x 2 value slices):
+    sequences are taken longest first across several waves."""
+    H, d = 2, 128
+    g = torch.Generator().manual_seed(70)
+    lengths = torch.randint(0, 300, (300,), generator=g).tolist()
+    inp = wl.prefill_inputs(lengths, H, d, dtype=torch.bfloat16, seed=71, device="cuda")
+    lam = channel_decays(H, d, 72)
+    out, st = la.prefill_channel_decay(inp.q, inp.k, inp.v, lam.cuda(), inp.cu_seqlens)
+    torch.cuda.synchronize()
+    la.device_status()
+    ref, ref_st = oracle.recurrent_cw(inp.q, inp.k, inp.v, lam, inp.cu_seqlens.cpu())
+    assert_close(out, ref, TOL_BF16, "tc channel decay 300 sequences out")
+    assert_close(st, ref_st, TOL_BF16, "tc channel decay 300 sequences state")
+
+
 def test_channel_decay_tensor_core_matches_cuda_cores():
     """The tcgen05 kernel (chunk 64) and the CUDA-core kernel (chunk 32) agree
     to the bf16 bound on the same inputs."""

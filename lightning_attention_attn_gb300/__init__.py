@@ -336,7 +336,9 @@ def prefill_channel_decay(q, k, v, decay, cu_seqlens=None, *, chunk: int = 0, ou
                           final_state=None, return_state: bool = True, stream=None,
                           initial_state=None):
     """Prefill with one decay per head and key channel: ``decay`` fp32
-    [H, d].  Otherwise as :func:`prefill` (CUDA-core kernel, chunk <= 64)."""
+    [H, d].  Otherwise as :func:`prefill`, with chunk 0, 16, 32 or 64: bf16
+    with d = 128 and chunk 0 or 64 runs the tensor-core kernel, the rest the
+    CUDA-core kernel."""
     if q.dim() != 3:
         raise ValueError("q must be [T, H, d]")
     T, H, d = q.shape

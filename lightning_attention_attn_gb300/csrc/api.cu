@@ -235,7 +235,7 @@ la_status lightning_attn_prefill_channel_decay(const void *q, const void *k, con
     if (st != LA_OK || !work) return st;
     if (chunk == 128 || chunk == 256)
         return fail(LA_ERR_UNSUPPORTED,
-                    "channel-wise decay runs on the CUDA-core kernel: chunk 0, 16, 32 or 64");
+                    "channel-wise decay takes chunk 0, 16, 32 or 64");
     la::PrefillArgs a{q, k, v, decay, cu_seqlens, num_seqs, total_tokens, num_heads,
                       head_dim, chunk, out, final_state, static_cast<cudaStream_t>(stream),
                       initial_state};

@@ -2,7 +2,8 @@
 //
 // This is the fp32 path (tensor-core tf32 would not meet a 1e-4 relative
 // bound), the path for head_dim 64 and chunks 16-64, and the channel-wise
-// decay.  One CTA owns one (sequence, head, 64-column value slice) and walks
+// decay where the tensor-core kernel does not take it (fp32, head_dim 64,
+// chunks 16 and 32).  One CTA owns one (sequence, head, 64-column value slice) and walks
 // its chunks in order, keeping its d x 64 slice of the state in shared memory:
 //   MiniMax-01 report (CSDN translation) §2.2.1 -- intra-block left product
 //   [(Q_i K_i^T) (.) M] V_i, inter-block right product Q_i KV_{i-1} and the

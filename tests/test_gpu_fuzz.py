@@ -1,7 +1,8 @@
 """Seeded random configurations against the fp64 CPU oracle: dtype, head_dim,
 block size, ragged lengths (including empty and one-token sequences), per-head
-decays anywhere in (0, 1], cached states on or off, and the backward pass on
-the tensor-core path.  Each case is small enough for the oracle to finish at
+decays anywhere in (0, 1], cached states on or off, the backward pass on
+the tensor-core path, and the channel-wise decay on both of its kernels.  Each
+case is small enough for the oracle to finish at
 once; together they cover combinations the hand-picked cases do not."""
 import random
 
@@ -83,3 +84,44 @@ def test_random_backward_matches_oracle(seed):
     ref = oracle.backward(inp.q, inp.k, inp.v, inp.decay, inp.cu_seqlens.cpu(), dout)
     for x, r, name in zip(got, ref, ("dq", "dk", "dv")):
         assert_close(x, r, TOL_BF16, f"seed {seed}: B={chunk} lengths={lengths} {name}")
+
+
+def random_cw_case(seed):
+    """A channel-wise case: per (head, key channel) decays drawn from 1, a
+    moderate range, a small range and 1e-20 (every power above the first
+    underflows), mixed within each head."""
+    rng = random.Random(seed)
+    dtype = rng.choice([torch.bfloat16, torch.bfloat16, torch.bfloat16, torch.float32])
+    d = rng.choice([64, 128, 128, 128])
+    chunk = rng.choice([0, 64, 64, 32, 16])
+    nseq = rng.randint(1, 5)
+    lengths = [rng.choice([0, 1, rng.randint(2, 70), rng.randint(71, 500)]) for _ in range(nseq)]
+    if sum(lengths) == 0:
+        lengths[0] = 9
+    H = rng.randint(1, 3)
+    lam = torch.empty((H, d), dtype=torch.float64)
+    for h in range(H):
+        for i in range(d):
+            lam[h, i] = rng.choice([1.0, rng.uniform(0.3, 1.0), rng.uniform(0.3, 1.0),
+                                    rng.uniform(1e-3, 0.3), 1e-20])
+    with_state = rng.random() < 0.5
+    return dtype, d, chunk, lengths, H, lam.to(torch.float32), with_state
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_random_channel_decay_prefill_matches_oracle(seed):
+    dtype, d, chunk, lengths, H, lam, with_state = random_cw_case(3000 + seed)
+    inp = wl.prefill_inputs(lengths, H, d, dtype=dtype, seed=seed + 300, device="cuda")
+    s0 = wl.cached_states(len(lengths), H, d, seed=seed + 377, device="cuda") \
+        if with_state else None
+    out, st = la.prefill_channel_decay(inp.q, inp.k, inp.v, lam.cuda(), inp.cu_seqlens,
+                                       chunk=chunk, initial_state=s0)
+    torch.cuda.synchronize()
+    la.device_status()
+    ref, ref_st = oracle.recurrent_cw(inp.q, inp.k, inp.v, lam, inp.cu_seqlens.cpu(),
+                                      initial_state=None if s0 is None else s0.cpu())
+    tol = TOL_FP32 if dtype == torch.float32 else TOL_BF16
+    what = f"cw fuzz {seed}: {dtype} d={d} B={chunk} L={lengths} state={with_state}"
+    assert torch.isfinite(out.float()).all() and torch.isfinite(st).all(), what
+    assert_close(out, ref, tol, what + " out")
+    assert_close(st, ref_st, tol, what + " state")

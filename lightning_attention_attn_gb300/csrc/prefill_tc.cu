@@ -31,7 +31,7 @@
 // (P per row, V per chunk): no overflow, no subnormal loss, and the scale is
 // undone in fp32 in the epilogue.  The fp32 state itself lives in TMEM for
 // the whole sequence, as the sum of the two halves of the dKV accumulator:
-// the state warpgroup writes lambda^{B_{i+1}} KV_i back into it and the next
+// the worker warps write lambda^{B_{i+1}} KV_i back into it and the next
 // dKV MMA accumulates onto that.  Nothing but q, k, v (read once per CTA)
 // and out / final state (written once) touches HBM.
 //
@@ -433,7 +433,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             const int st = i & 1;
             const uint32_t sph = (i >> 1) & 1, ph = i & 1;
             // dKV += K_i^T [Vhat_hi | Vhat_lo]: the accumulator holds
-            // lambda^{B_i} KV_{i-1}, written back by the state warpgroup
+            // lambda^{B_i} KV_{i-1}, written back by the worker warps
             if (!warp_wait(bar(cs.full_k[st]), sph, abort_flag)) break;
             if (!warp_wait(bar(cs.dkv_ready), ph, abort_flag)) break;
             tc_fence_after();

@@ -184,10 +184,10 @@ int64_t lightning_attn_snapshot_count(const int32_t *cu_seqlens_host, int32_t nu
  * hi/lo bf16 pair but the key side of the off-diagonal scores).  For its
  * diagonal sub-blocks lambda is raised to 2^-12 where smaller: a score term
  * at distance 1..15 then moves by less than 2^-12 |q_t[i] k_u[i]|.  Those
- * factors reach mu^-8 = 1/max(lambda, 2^-12)^8 (up to 2^96) on the query side
- * and mu^-7 on the key side, so the kernel's input range is |q| * mu^-8 and
- * |k| * mu^-7 below the bf16 maximum (about 3.4e38): for lambda >= 2^-12 and
- * inputs of moderate size there is no limit in practice.  Every other case
+ * factors reach mu_i^-8 on the query side and mu_i^-7 on the key side, with
+ * mu_i = max(lambda_i, 2^-12), so the kernel needs |q_t[i]| mu_i^-8 and
+ * |k_u[i]| mu_i^-7 below the bf16 maximum (about 3.4e38): always true for
+ * |q| < 2^32 and |k| < 2^44.  Every other case
  * runs the CUDA-core (FFMA) kernel: chunk 0 (= 64), 16, 32 or 64 (fp32, or
  * head_dim 64); 128 and 256 return LA_ERR_UNSUPPORTED.
  */

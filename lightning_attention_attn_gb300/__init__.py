@@ -18,6 +18,7 @@ import ctypes
 import os
 import re
 import threading
+import weakref
 
 import torch
 
@@ -38,6 +39,30 @@ class LightningAttnError(RuntimeError):
     def __init__(self, status: int, message: str):
         super().__init__(message)
         self.status = status
+
+
+# Decay tensors already found inside (0, 1]: id -> (weak reference, version).
+# Reading the values back costs a device synchronisation, so each tensor is
+# checked once per in-place version rather than on every call.
+_decay_checked: dict = {}
+
+
+def check_decay_range(decay: torch.Tensor) -> None:
+    """Raise ValueError unless every lambda in ``decay`` lies in (0, 1] (the
+    range the method's decay factors assume).  Checked once per tensor and
+    in-place version; skipped while a CUDA stream is being captured, where no
+    value can be read back."""
+    key = id(decay)
+    hit = _decay_checked.get(key)
+    if hit is not None and hit[0]() is decay and hit[1] == decay._version:
+        return
+    if decay.is_cuda and torch.cuda.is_current_stream_capturing():
+        return
+    if not bool(((decay > 0) & (decay <= 1)).all()):
+        raise ValueError("decay values must lie in (0, 1]")
+    if len(_decay_checked) > 256:
+        _decay_checked.clear()
+    _decay_checked[key] = (weakref.ref(decay), decay._version)
 
 
 def header_functions(path: str = HEADER) -> list[str]:
@@ -161,6 +186,7 @@ def prefill(q, k, v, decay, cu_seqlens=None, *, chunk: int = 0, out=None,
         raise ValueError("cu_seqlens must be a 1-D int32 tensor")
     if decay.dtype != torch.float32 or decay.numel() != H:
         raise ValueError("decay must be fp32 [H]")
+    check_decay_range(decay)
     nseq = cu_seqlens.numel() - 1
     if out is None:
         out = torch.empty_like(q)
@@ -219,6 +245,7 @@ def backward(q, k, v, decay, cu_seqlens, dout, *, chunk: int = 0, dq=None, dk=No
         raise ValueError("cu_seqlens must be a 1-D int32 tensor")
     if decay.dtype != torch.float32 or decay.numel() != H:
         raise ValueError("decay must be fp32 [H]")
+    check_decay_range(decay)
     nseq = cu_seqlens.numel() - 1
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(q) if dk is None else dk
@@ -260,6 +287,7 @@ def mixed_step(q, k, v, decay, cu_seqlens, state, *, out=None, prefill_stream=No
         raise ValueError("cu_seqlens must be a 1-D int32 tensor")
     if decay.dtype != torch.float32 or decay.numel() != H:
         raise ValueError("decay must be fp32 [H]")
+    check_decay_range(decay)
     nseq = cu_seqlens.numel() - 1
     if state.dtype != torch.float32 or tuple(state.shape) != (nseq, H, d, d):
         raise ValueError("state must be fp32 [nseq, H, d, d]")
@@ -308,6 +336,7 @@ def prefill_snapshots(q, k, v, decay, cu_seqlens, snapshot_interval: int, *, chu
         raise ValueError("cu_seqlens must be a 1-D int32 tensor")
     if decay.dtype != torch.float32 or decay.numel() != H:
         raise ValueError("decay must be fp32 [H]")
+    check_decay_range(decay)
     nseq = cu_seqlens.numel() - 1
     if snapshots is None:
         # sizing needs the lengths on the host (one synchronising copy); pass
@@ -349,6 +378,7 @@ def prefill_channel_decay(q, k, v, decay, cu_seqlens=None, *, chunk: int = 0, ou
         cu_seqlens = torch.tensor([0, T], dtype=torch.int32, device=q.device)
     if decay.dtype != torch.float32 or tuple(decay.shape) != (H, d):
         raise ValueError("decay must be fp32 [H, d]")
+    check_decay_range(decay)
     nseq = cu_seqlens.numel() - 1
     if out is None:
         out = torch.empty_like(q)
@@ -369,6 +399,7 @@ def decode_channel_decay(q, k, v, decay, state, *, out=None, stream=None):
     Bn, H, d = q.shape
     if decay.dtype != torch.float32 or tuple(decay.shape) != (H, d):
         raise ValueError("decay must be fp32 [H, d]")
+    check_decay_range(decay)
     if out is None:
         out = torch.empty_like(q)
     st = load().lightning_attn_decode_channel_decay(
@@ -394,6 +425,7 @@ def decode(q, k, v, decay, state, *, out=None, stream=None):
         raise ValueError("state must be fp32 [B, H, d, d]")
     if decay.dtype != torch.float32 or decay.numel() != H:
         raise ValueError("decay must be fp32 [H]")
+    check_decay_range(decay)
     if out is None:
         out = torch.empty_like(q)
     lib = load()

@@ -269,3 +269,24 @@ def test_snapshot_count(lib):
     bad = (ctypes.c_int32 * 3)(0, 10, 5)
     assert g(bad, 2, 64) == -1
     assert la.snapshot_count(torch.tensor([0, 100, 356, 356, 1000], dtype=torch.int32), 128) == 7
+
+
+def test_binding_checks_the_decay_range():
+    """The binding rejects lambda outside (0, 1] (0, above 1, NaN) before any
+    launch, checks a tensor once per in-place version, and re-checks after an
+    in-place change."""
+    import torch
+    good = torch.tensor([0.5, 1.0, 1e-30], dtype=torch.float32)
+    la.check_decay_range(good)
+    la.check_decay_range(good)  # cached
+    for bad in ([0.5, 0.0], [1.5, 0.5], [float("nan"), 0.5], [-0.1, 0.5]):
+        with pytest.raises(ValueError, match="decay"):
+            la.check_decay_range(torch.tensor(bad, dtype=torch.float32))
+    good[0] = 2.0  # in place: a new version, checked again
+    with pytest.raises(ValueError, match="decay"):
+        la.check_decay_range(good)
+    cw = torch.full((2, 4), 0.9, dtype=torch.float32)
+    la.check_decay_range(cw)
+    cw[1, 3] = 0.0
+    with pytest.raises(ValueError, match="decay"):
+        la.check_decay_range(cw)

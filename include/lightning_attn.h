@@ -66,9 +66,10 @@ typedef enum la_dtype {
  * q, k, v      [total_tokens, num_heads, head_dim], dtype `dtype`, row-major;
  *              token-major packed: sequence s owns rows
  *              [cu_seqlens[s], cu_seqlens[s+1]).
- * decay        [num_heads] fp32, lambda_h, each in (0, 1] (not checked on the
- *              device; values outside give the formula's value, possibly
- *              inf/nan).
+ * decay        [num_heads] fp32, lambda_h, each in (0, 1] (not checked here:
+ *              this entry point does not read device memory on the host;
+ *              values outside give the formula's value, possibly inf/nan.
+ *              The Python binding checks the range before the call).
  * cu_seqlens   [num_seqs + 1] int32 DEVICE array, cu_seqlens[0] = 0,
  *              non-decreasing, cu_seqlens[num_seqs] = total_tokens.  Empty
  *              sequences are allowed (their final state is zero).

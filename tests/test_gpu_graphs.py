@@ -106,3 +106,22 @@ def test_mixed_step_in_a_graph():
     st.copy_(st0)
     replay(g, s)
     assert torch.equal(out, out_ref) and torch.equal(st, st_ref)
+
+
+def test_channel_decay_prefill_in_a_graph():
+    """The channel-wise tensor-core kernel replayed from a graph gives the
+    eager result bit for bit (cached states, an empty sequence)."""
+    inp = wl.prefill_inputs([300, 0, 129, 700], 4, 128, dtype=torch.bfloat16, seed=78,
+                            device="cuda")
+    jitter = torch.rand((4, 128), generator=torch.Generator().manual_seed(79))
+    lam = (inp.decay.cpu()[:, None] * (1.0 - 0.3 * jitter)).to(torch.float32).cuda()
+    s0 = wl.cached_states(4, 4, 128, seed=80, device="cuda")
+    ref, ref_st = la.prefill_channel_decay(inp.q, inp.k, inp.v, lam, inp.cu_seqlens,
+                                           initial_state=s0)
+    out = torch.empty_like(inp.q)
+    st = torch.empty_like(ref_st)
+    g, s = capture(lambda s: la.prefill_channel_decay(inp.q, inp.k, inp.v, lam, inp.cu_seqlens,
+                                                      out=out, final_state=st,
+                                                      initial_state=s0, stream=s))
+    replay(g, s)
+    assert torch.equal(out, ref) and torch.equal(st, ref_st)

@@ -56,6 +56,12 @@ decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
     constexpr int kRowsPerPass = 16;
     using V = typename VecT<VEC>::type;
 
+    // launched as a dependent launch: wait for the previous kernel in the
+    // stream (e.g. the step before, which wrote this state) to complete and
+    // its writes to be visible, then let the next step be scheduled
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
     __shared__ float qs[D], ks[D];
     __shared__ float red[kWarps][D];
 
@@ -130,11 +136,11 @@ cudaError_t launch(const DecodeArgs &a) {
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffffL) return cudaErrorInvalidConfiguration;
     auto kern = a.channel_decay ? decode_kernel<T, D, true> : decode_kernel<T, D, false>;
-    kern<<<(unsigned)grid, kThreads, 0, a.stream>>>(
-        static_cast<const T *>(a.q), static_cast<const T *>(a.k),
-        static_cast<const T *>(a.v), a.decay, a.state, a.num_heads,
+    const cudaError_t e = launch_dependent(
+        kern, (unsigned)grid, kThreads, 0, a.stream, static_cast<const T *>(a.q),
+        static_cast<const T *>(a.k), static_cast<const T *>(a.v), a.decay, a.state, a.num_heads,
         static_cast<T *>(a.out), a.cu_seqlens, a.total_tokens);
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <typename T>

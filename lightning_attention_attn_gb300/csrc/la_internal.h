@@ -9,6 +9,27 @@
 
 namespace la {
 
+// Launches `kern` with programmatic stream serialization: it may be scheduled
+// while the kernel before it in the stream is finishing, and waits
+// (grid_dependency_wait) before its first global-memory access, so stream
+// order is kept for every memory effect.  Only kernels that begin with that
+// wait are launched this way.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent(void (*kern)(KArgs...), unsigned grid, unsigned block,
+                                    size_t smem, cudaStream_t stream, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+}
+
 struct PrefillArgs {
     const void *q, *k, *v;      // [T, H, D]
     const float *decay;         // [H]

@@ -213,6 +213,8 @@ prefill_cw_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     Ctrl &cs = *reinterpret_cast<Ctrl *>(base + kOffCtrl);
     const uint32_t sb = smem_u32(base);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    grid_dependency_wait();    // the previous kernel's writes are visible from here on
+    grid_launch_dependents();  // the next dependent launch may be scheduled
 
     const int vs = blockIdx.x % NVS;
     const int h = (blockIdx.x / NVS) % H;
@@ -761,10 +763,10 @@ cudaError_t prefill_cw_tc_bf16(const PrefillArgs &a) {
     const long grid = (long)a.nseq * a.num_heads * NVS;
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffffL) return cudaErrorInvalidConfiguration;
-    prefill_cw_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, a.stream>>>(
-        mq, mk, mv, a.decay, a.cu_seqlens, a.nseq, a.total_tokens, a.num_heads, a.initial_state,
-        static_cast<__nv_bfloat16 *>(a.out), a.final_state);
-    return cudaGetLastError();
+    e = launch_dependent(prefill_cw_tc_kernel, (unsigned)grid, kThreads, kSmemBytes, a.stream, mq,
+                         mk, mv, a.decay, a.cu_seqlens, a.nseq, a.total_tokens, a.num_heads,
+                         a.initial_state, static_cast<__nv_bfloat16 *>(a.out), a.final_state);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace la

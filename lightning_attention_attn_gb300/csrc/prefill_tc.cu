@@ -231,6 +231,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     Ctrl &cs = *reinterpret_cast<Ctrl *>(base + kOffCtrl);
     const uint32_t sb = smem_u32(base);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    grid_dependency_wait();    // the previous kernel's writes are visible from here on
+    grid_launch_dependents();  // the next dependent launch may be scheduled
 
     // ---- which (sequence, head, value slice) ----
     const int vs = blockIdx.x % NVS;
@@ -1095,11 +1097,11 @@ cudaError_t prefill_tc_bf16(const PrefillArgs &a) {
     const long grid = (long)(a.rank_limit > 0 ? a.rank_limit : a.nseq) * a.num_heads * NVS;
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffffL) return cudaErrorInvalidConfiguration;
-    kern<<<(unsigned)grid, kThreads, kSmemBytes, a.stream>>>(
-        mq, mk, mv, a.decay, a.cu_seqlens, a.nseq, a.total_tokens, a.num_heads,
-        a.initial_state, static_cast<__nv_bfloat16 *>(a.out), a.final_state, a.min_len,
-        a.snapshots, a.snapshot_interval);
-    return cudaGetLastError();
+    e = launch_dependent(kern, (unsigned)grid, kThreads, kSmemBytes, a.stream, mq, mk, mv, a.decay,
+                         a.cu_seqlens, a.nseq, a.total_tokens, a.num_heads, a.initial_state,
+                         static_cast<__nv_bfloat16 *>(a.out), a.final_state, a.min_len,
+                         a.snapshots, a.snapshot_interval);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t take_device_error(cudaStream_t stream, unsigned int *err) {

@@ -318,6 +318,20 @@ __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// ------------------------------------------------------- dependent launch
+// A kernel launched with programmatic stream serialization may start while
+// the kernel before it in the stream is finishing.  grid_dependency_wait()
+// returns once that kernel has completed and its memory operations are
+// visible, so it comes before a kernel's first global-memory access;
+// grid_launch_dependents() lets the next such kernel be scheduled (it still
+// waits in its own grid_dependency_wait()).
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------- descriptors
 // Shared-memory matrix descriptor (tcgen05 format, version 1) for a
 // 128-byte-swizzled operand whose 8-row x 128-byte swizzle atoms start at

@@ -224,3 +224,21 @@ def test_channel_decay_tensor_core_repeatable():
         torch.cuda.synchronize()
         assert torch.equal(out, first) and torch.equal(st, first_st)
     la.device_status()
+
+
+def test_channel_decay_tensor_core_state_in_place():
+    """initial_state may be final_state itself (the prefix cache updated in
+    place): the same result as with separate buffers."""
+    H, d = 4, 128
+    lengths = [300, 0, 129, 65]
+    inp = wl.prefill_inputs(lengths, H, d, dtype=torch.bfloat16, seed=82, device="cuda")
+    lam = channel_decays(H, d, 83).cuda()
+    s0 = wl.cached_states(len(lengths), H, d, seed=84, device="cuda")
+    ref, ref_st = la.prefill_channel_decay(inp.q, inp.k, inp.v, lam, inp.cu_seqlens,
+                                           initial_state=s0)
+    cache = s0.clone()
+    out = torch.empty_like(inp.q)
+    la.prefill_channel_decay(inp.q, inp.k, inp.v, lam, inp.cu_seqlens, out=out,
+                             final_state=cache, initial_state=cache)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref) and torch.equal(cache, ref_st)

@@ -290,3 +290,19 @@ def test_binding_checks_the_decay_range():
     cw[1, 3] = 0.0
     with pytest.raises(ValueError, match="decay"):
         la.check_decay_range(cw)
+
+
+def test_entry_points_reject_decay_out_of_range():
+    """prefill, decode and the channel-wise calls refuse lambda outside (0, 1]
+    before the library is called (CPU tensors: the check needs no device)."""
+    import torch
+    T, H, d = 8, 2, 64
+    q = torch.zeros((T, H, d), dtype=torch.float32)
+    cu = torch.tensor([0, T], dtype=torch.int32)
+    with pytest.raises(ValueError, match="decay"):
+        la.prefill(q, q, q, torch.tensor([0.5, 1.5]), cu)
+    with pytest.raises(ValueError, match="decay"):
+        la.prefill_channel_decay(q, q, q, torch.full((H, d), 0.0), cu)
+    state = torch.zeros((1, H, d, d), dtype=torch.float32)
+    with pytest.raises(ValueError, match="decay"):
+        la.decode(q[:1], q[:1], q[:1], torch.tensor([float("nan"), 0.5]), state)

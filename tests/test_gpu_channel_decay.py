@@ -242,3 +242,23 @@ def test_channel_decay_tensor_core_state_in_place():
                              final_state=cache, initial_state=cache)
     torch.cuda.synchronize()
     assert torch.equal(out, ref) and torch.equal(cache, ref_st)
+
+
+def test_channel_decay_tensor_core_128k_context():
+    """One 131072-token sequence x 64 heads (2048 blocks per CTA): heads 0,
+    31 and 63 (the fastest, a middle and the slowest decay) against the
+    oracle, all tokens and final states; every head finite."""
+    H, d = 64, 128
+    inp = wl.prefill_inputs([131072], H, d, dtype=torch.bfloat16, seed=85, device="cuda")
+    lam = (inp.decay[:, None] * (1.0 - 0.01 * torch.linspace(0, 1, d, device="cuda"))[None, :])
+    lam = lam.to(torch.float32).contiguous()
+    out, st = la.prefill_channel_decay(inp.q, inp.k, inp.v, lam, inp.cu_seqlens)
+    torch.cuda.synchronize()
+    la.device_status()
+    assert torch.isfinite(out.float()).all() and torch.isfinite(st).all()
+    heads = [0, 31, 63]
+    sel = lambda t: t[:, heads].contiguous()
+    ref, ref_st = oracle.recurrent_cw(sel(inp.q), sel(inp.k), sel(inp.v), lam[heads].cpu(),
+                                      inp.cu_seqlens.cpu())
+    assert_close(out[:, heads], ref, TOL_BF16, "tc channel decay 128k out (heads 0, 31, 63)")
+    assert_close(st[:, heads], ref_st, TOL_BF16, "tc channel decay 128k state (heads 0, 31, 63)")

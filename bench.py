@@ -423,7 +423,8 @@ def run_ours(args, ws, rank, local):
                 "roofline": {"bound": "hbm", "alg_bytes": byts,
                              "achieved": round(byts / (ms / 1e3) / 1e9, 1), "peak": pk["hbm"],
                              "unit": "GB/s", "frac": round(byts / (ms / 1e3) / 1e9 / pk["hbm"], 4),
-                             "traffic": ncu_traffic("prefill_cw_tc_kernel", CW_KERNEL_SRC)},
+                             "traffic": ncu_traffic("prefill_cw_tc_kernel", CW_KERNEL_SRC)
+                             if Tn == 8192 else None},  # the counters are of the 8K layer
                 "tensor": {"alg_flops": flops,
                            "frac_of_bf16_peak": round(flops / (ms / 1e3) / 1e12 / pk["bf16"], 4),
                            "note": "the tensor pipe runs about 6x the algorithmic flops: hi/lo "
@@ -466,6 +467,7 @@ def run_ours(args, ws, rank, local):
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     more = {"prefill_8k_channel_decay": time_channel_decay([8192], 10),
             "prefill_8k_channel_decay_cuda_cores": time_channel_decay([8192], 3, chunk=32),
+            "prefill_128k_channel_decay": time_channel_decay([131072], 3),
             "prefill_8k_snapshots_every_1024": time_snapshots([8192], 1024, 10),
             "prefill_8k_snapshots_every_128": time_snapshots([8192], 128, 10),
             "prefill_8k_chunk64": time_prefill([8192], 64, 10),
@@ -805,7 +807,8 @@ def run_ours(args, ws, rank, local):
         "channel_decay_8k": {
             "tensor_cores_ms": more["prefill_8k_channel_decay"]["ms_per_launch"],
             "tensor_cores_hbm_frac": frac(more["prefill_8k_channel_decay"]),
-            "cuda_cores_ms": more["prefill_8k_channel_decay_cuda_cores"]["ms_per_launch"]},
+            "cuda_cores_ms": more["prefill_8k_channel_decay_cuda_cores"]["ms_per_launch"],
+            "tensor_cores_128k_ms": more["prefill_128k_channel_decay"]["ms_per_launch"]},
     }
     return line
 
